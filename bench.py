@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the MLA hot path on GB300.
+
+A step is one whole MLA decode layer step on the DeepSeek-V2-shaped decode
+workload (d_model 5120, 128 heads, d_nope 128, d_rope 64, r_kv 512, r_q 1536,
+batch 64, per-sequence cache lengths ~ U[1024, 4096], seed 0):
+latent + query projection with the cache append, weight absorption, split-KV
+latent attention, combine, W_UV, and the output projection.  ``value`` is
+latent-cache bytes read per step (sum over sequences of L_b * (r_kv + d_rope)
+* 2) divided by the step time, summed over ranks.  The prefill workload
+(B=4, S=4096, same dims) is timed as a secondary figure in TFLOP/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank runs an independent replica (the path has no
+cross-GPU exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_synth as syn  # noqa: E402
+
+METRIC = "MLA decode latent-cache HBM GB/s (% of peak); prefill TFLOP/s (% bf16 peak)"
+DECODE = syn.WORKLOADS["dsv2_decode"]
+PREFILL = syn.WORKLOADS["dsv2_prefill"]
+L2_FLUSH_BYTES = 512 << 20
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def decode_bytes(lens) -> int:
+    return int(np.sum(lens)) * (DECODE.r_kv + DECODE.d_rope) * 2
+
+
+def decode_flops(lens) -> float:
+    w = DECODE
+    return float(np.sum(lens)) * w.n_heads * 2 * ((w.r_kv + w.d_rope) + w.r_kv)
+
+
+def prefill_flops(w=PREFILL) -> float:
+    T = w.batch * w.seq
+    H = w.n_heads
+    proj = 2 * T * (w.d_model * (w.r_q + w.r_kv + w.d_rope) + w.r_q * H * (w.d_nope + w.d_rope)
+                    + w.r_kv * H * (w.d_nope + w.d_v) + H * w.d_v * w.d_model)
+    attn = w.batch * H * (w.seq * (w.seq + 1) / 2) * 2 * ((w.d_nope + w.d_rope) + w.d_v)
+    return proj + attn, attn
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=5)
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            rows.append((ts, f))
+        inside = [r for r in rows if any(a - 0.05 <= r[0] <= b + 0.05 for a, b in self.windows)]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        sm = [float(f[2]) for _, f in use if f[2].replace(".", "").isdigit()]
+        smax = [float(f[3]) for _, f in use if f[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, f in use:
+            for i, n in enumerate(names):
+                if f[6 + i].lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def to_dev(stored, device):
+    import torch
+    if stored.dtype == np.uint16:
+        return torch.from_numpy(stored.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(stored).to(device)
+
+
+def build_layer(w, device, max_batch, max_seq, max_tokens, ws_max_len):
+    import head_latent_attention_gb300 as mla
+    cfg = mla.make_config(w.variant, w.dtype, w.d_model, w.n_heads, w.d_nope, w.d_rope, w.d_v,
+                          w.r_kv, w.r_q, w.n_latent_heads, w.rope_base, max_batch, max_seq)
+    dev_w = {k: to_dev(s, device) for k, (s, _) in syn.weights(w).items()}
+    return mla.MlaLayer(cfg, dev_w, max_tokens, device=device, ws_max_len=ws_max_len)
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    import torch.distributed as dist
+    from head_latent_attention_gb300 import _build
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    import head_latent_attention_gb300 as mla
+
+    hbm_peak, tf_peak, tf_sust, peak_src = peaks()
+    w = DECODE
+    B = w.batch
+    lens = syn.lengths(w)
+    lay = build_layer(w, device, B, w.seq, B, 0)
+    for b in range(B):
+        ls, _ = syn.cache_rows(w, b, int(lens[b]))
+        lay.cache_lat[b, :lens[b]] = to_dev(ls, device)
+        rs, _ = syn.cache_rows(w, b, int(lens[b]), "cache_rope")
+        lay.cache_rope[b, :lens[b]] = to_dev(rs, device)
+    xs, _ = syn.activations(w, B)
+    x = to_dev(xs, device)
+    seq = torch.arange(B, dtype=torch.int32, device=device)
+    pos = torch.from_numpy(lens - 1).to(device)
+    sl = torch.from_numpy(lens).to(device)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def step(x_in, pos_in, sl_in):
+        qn, qr = lay.project_latent(x_in, seq, pos_in)
+        o = lay.decode(qn, qr, sl_in)
+        return lay.out_proj(o)
+
+    for _ in range(max(args.warmup, 3)):
+        step(x, pos, sl)
+    torch.cuda.synchronize()
+
+    uuid = str(getattr(torch.cuda.get_device_properties(device), "uuid", ""))
+    sampler = ClockSampler(("GPU-" + uuid) if uuid and not uuid.startswith("GPU-") else
+                           (uuid or str(torch.cuda.current_device())))
+    sampler.start()
+    time.sleep(0.2)
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n_launch0 = mla.mla_launch_count()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_ATTENTION, kev[i][0], kev[i][1])
+        ev[i][0].record(stream)
+        step(x, pos, sl)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_ATTENTION, None, None)
+    launches = mla.mla_launch_count() - n_launch0
+    sampler.mark(t0, t1)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    ms = sum(step_ms) / K
+    kms = sum(kern_ms) / K
+
+    # End to end through the C ABI from pinned host buffers: H2D of the step's
+    # inputs (token activations, positions, lengths) and D2H of its output.
+    x_h = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).pin_memory()
+    pos_h = torch.from_numpy(lens - 1).pin_memory()
+    sl_h = torch.from_numpy(lens.copy()).pin_memory()
+    y_h = torch.empty(B, w.d_model, dtype=torch.bfloat16).pin_memory()
+    x_d = torch.empty_like(x)
+    pos_d = torch.empty_like(pos)
+    sl_d = torch.empty_like(sl)
+    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    torch.cuda.synchronize()
+    t2 = time.time()
+    for i in range(K):
+        flush.zero_()
+        eev[i][0].record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        pos_d.copy_(pos_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        y = step(x_d, pos_d, sl_d)
+        y_h.copy_(y, non_blocking=True)
+        eev[i][1].record(stream)
+    torch.cuda.synchronize()
+    t3 = time.time()
+    sampler.mark(t2, t3)
+    e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / K
+    h2d = x_h.numel() * 2 + pos_h.numel() * 4 + sl_h.numel() * 4
+    d2h = y_h.numel() * 2
+
+    # Secondary: prefill layer (project + causal attention + output projection).
+    pre = run_prefill(args, lay_device=device) if args.prefill else None
+    sampler.stop()
+    clocks = sampler.summary()
+
+    nbytes = decode_bytes(lens)
+    if world > 1:
+        t = torch.tensor([ms, e2e_ms, kms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms, kms = t.tolist()
+    value = world * nbytes / (ms * 1e-3) / 1e9
+    e2e_val = world * nbytes / (e2e_ms * 1e-3) / 1e9
+    achieved = nbytes / (kms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) caches/activations, N(0,1/fan_in) weights)",
+        "config": {"workload": "dsv2_decode", "batch": B, "cache_len": "U[1024,4096] seed 0",
+                   "sum_len": int(np.sum(lens)), "d_model": w.d_model, "heads": w.n_heads,
+                   "d_nope": w.d_nope, "d_rope": w.d_rope, "r_kv": w.r_kv, "r_q": w.r_q,
+                   "cache_bytes_per_step": nbytes,
+                   "l2": "flushed between steps (512 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "decode split-KV latent attention",
+                     "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
+                     "kernel_ms": round(kms, 5), "traffic": None},
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if pre:
+        out["prefill"] = pre
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args)
+    return out
+
+
+def run_prefill(args, lay_device):
+    import torch
+    import head_latent_attention_gb300 as mla
+    hbm_peak, tf_peak, tf_sust, peak_src = peaks()
+    w = PREFILL
+    B, S = w.batch, w.seq
+    lay = build_layer(w, lay_device, B, S, B * S, S)
+    xs, _ = syn.activations(w, B * S)
+    x = to_dev(xs, lay_device)
+    pos = torch.arange(S, dtype=torch.int32, device=lay_device).repeat(B)
+    seq = torch.arange(B, dtype=torch.int32, device=lay_device).repeat_interleave(S)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qn, qr = lay.project_latent(x, seq, pos)
+        o = lay.prefill(qn, qr, B, S)
+        return lay.out_proj(o)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    K = args.prefill_steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, kev[i][0], kev[i][1])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, None, None)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    kms = sum(a.elapsed_time(b) for a, b in kev) / K
+    total, attn = prefill_flops(w)
+    tf = total / (ms * 1e-3) / 1e12
+    katt = attn / (kms * 1e-3) / 1e12
+    del lay
+    torch.cuda.empty_cache()
+    return {"workload": "dsv2_prefill", "batch": B, "seq": S, "steps": K,
+            "ms_per_step": round(ms, 4), "tflops": round(tf, 2), "unit": "TFLOP/s",
+            "frac_of_bf16_peak": round(tf / tf_peak, 4), "flops_per_step": total,
+            "roofline": {"bound": "tensor", "kernel": "causal flash attention",
+                         "achieved": round(katt, 2), "peak": tf_peak, "unit": "TFLOP/s",
+                         "frac": round(katt / tf_peak, 4), "peak_source": peak_src,
+                         "kernel_ms": round(kms, 4)}}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample of the decode workload
+# ---------------------------------------------------------------------------
+
+def oracle_decode_sample(bs, lens, Wx, n_threads):
+    import oracle
+    w = DECODE
+    xs, xe = syn.activations(w, w.batch)
+    lat = np.zeros((len(bs), int(max(lens[b] for b in bs)), w.r_kv))
+    rope = np.zeros((len(bs), lat.shape[1], w.d_rope))
+    for i, b in enumerate(bs):
+        lat[i, :lens[b]] = syn.cache_rows(w, b, int(lens[b]))[1]
+        rope[i, :lens[b]] = syn.cache_rows(w, b, int(lens[b]), "cache_rope")[1]
+    sub = w.replace(seq=lat.shape[1])
+    t0 = time.perf_counter()
+    oracle.decode(sub, xe[bs], np.asarray([lens[b] for b in bs], np.int32), lat, rope, Wx,
+                  absorbed=True, n_threads=n_threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(args):
+    import oracle
+    oracle.build()
+    n_threads = os.cpu_count() or 1
+    w = DECODE
+    lens = syn.lengths(w)
+    Wx = {k: e for k, (_, e) in syn.weights(w).items()}
+    done, secs, bs = 0, 0.0, []
+    for b in range(w.batch):
+        secs += oracle_decode_sample([b], lens, Wx, n_threads)
+        bs.append(b)
+        if secs >= args.cpu_seconds:
+            break
+    nbytes = decode_bytes(lens[bs])
+    return {"value": round(nbytes / secs / 1e9, 5), "unit": "GB/s", "cores": n_threads,
+            "kind": "oracle",
+            "sample": f"oracle decode step (projection, absorbed attention, W_UV, W_O; fp64) "
+                      f"for sequences 0..{len(bs) - 1} of the dsv2_decode workload "
+                      f"({int(np.sum(lens[bs]))} cached tokens, {secs:.1f} s)"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is one sequence of the decode
+    workload run through the fp64 oracle on the host cores."""
+    import oracle
+    oracle.build()
+    n_threads = os.cpu_count() or 1
+    w = DECODE
+    lens = syn.lengths(w)
+    Wx = {k: e for k, (_, e) in syn.weights(w).items()}
+    for i in range(args.warmup):
+        oracle_decode_sample([i % w.batch], lens, Wx, n_threads)
+    secs, nbytes = 0.0, 0
+    for i in range(args.steps):
+        b = (args.warmup + i) % w.batch
+        secs += oracle_decode_sample([b], lens, Wx, n_threads)
+        nbytes += decode_bytes(lens[[b]])
+    v = nbytes / secs / 1e9
+    sample = (f"each step: one sequence of dsv2_decode through the fp64 oracle decode step "
+              f"(sequences {args.warmup % w.batch}.., {nbytes // 1152} cached tokens over "
+              f"{args.steps} steps)")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "dsv2_decode", "batch": w.batch,
+                       "cache_len": "U[1024,4096] seed 0"},
+            "cpu_baseline": {"value": round(v, 6), "unit": "GB/s", "cores": n_threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--prefill-steps", type=int, default=3)
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    device = f"cuda:{local}"
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(device))
+    out = run_ours(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

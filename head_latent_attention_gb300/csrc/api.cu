@@ -1,0 +1,483 @@
+// C ABI entry points: argument validation, workspace layout, kernel dispatch.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "mla_internal.cuh"
+
+using namespace mla;
+
+namespace mla {
+
+static unsigned long long g_launches = 0;
+static cudaEvent_t g_prof_begin[MLA_PROFILE_COUNT] = {};
+static cudaEvent_t g_prof_end[MLA_PROFILE_COUNT] = {};
+
+void note_launch(int n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
+
+void profile_begin(int which, cudaStream_t s)
+{
+    if (g_prof_begin[which]) cudaEventRecord(g_prof_begin[which], s);
+}
+
+void profile_end(int which, cudaStream_t s)
+{
+    if (g_prof_end[which]) cudaEventRecord(g_prof_end[which], s);
+}
+
+}  // namespace mla
+
+namespace {
+
+constexpr int kDecodeChunk = 512;  // keys per split of the CUDA-core decode
+constexpr double kLog2e = 1.4426950408889634;
+
+size_t esize(const mla_config &c) { return c.dtype == MLA_DTYPE_F32 ? 4 : 2; }
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int rope_dim_of(const mla_config &c)
+{
+    if (c.variant == MLA_VARIANT_DECOUPLED) return c.d_rope;
+    if (c.variant == MLA_VARIANT_SMALL) return c.d_nope;
+    return 0;
+}
+
+// Latent width one head attends over, and heads that share one latent block.
+int r_lat_of(const mla_config &c) { return c.r_kv / c.n_latent_heads; }
+int heads_per_block_of(const mla_config &c) { return c.n_heads / c.n_latent_heads; }
+
+int decode_splits(const mla_config &c) { return (c.max_seq + kDecodeChunk - 1) / kDecodeChunk; }
+
+// Workspace regions, each 256-byte aligned, after the status header.
+struct ProjectWs { size_t cq, end; };
+struct DecodeWs { size_t q_abs, o_lat, o_part, ml_part, end; };
+struct PrefillWs { size_t start_pos, k, v, end; };
+
+ProjectWs project_ws(const mla_config &c, int64_t T)
+{
+    ProjectWs w;
+    w.cq = kWsHeader;
+    size_t n = c.variant == MLA_VARIANT_DECOUPLED ? (size_t)T * c.r_q * esize(c) : 0;
+    w.end = round_up(w.cq + n, 256);
+    return w;
+}
+
+DecodeWs decode_ws(const mla_config &c, int B)
+{
+    DecodeWs w;
+    size_t lat = (size_t)B * c.n_heads * r_lat_of(c);
+    size_t parts = (size_t)B * decode_splits(c) * c.n_heads;
+    w.q_abs = kWsHeader;
+    w.o_lat = round_up(w.q_abs + lat * esize(c), 256);
+    w.o_part = round_up(w.o_lat + lat * esize(c), 256);
+    w.ml_part = round_up(w.o_part + parts * r_lat_of(c) * 4, 256);
+    w.end = round_up(w.ml_part + parts * 2 * 4, 256);
+    return w;
+}
+
+PrefillWs prefill_ws(const mla_config &c, int B, int64_t kv_rows)
+{
+    PrefillWs w;
+    size_t rows = (size_t)B * kv_rows * c.n_heads;
+    w.start_pos = kWsHeader;
+    w.k = round_up(w.start_pos + (size_t)B * 4, 256);
+    w.v = round_up(w.k + rows * c.d_nope * esize(c), 256);
+    w.end = round_up(w.v + rows * c.d_v * esize(c), 256);
+    return w;
+}
+
+mla_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+#define MLA_TRY_CUDA(expr)                              \
+    do {                                                \
+        cudaError_t _e = (expr);                        \
+        if (_e != cudaSuccess) return MLA_ERR_CUDA;     \
+    } while (0)
+
+// Every tensor the library reads or writes must be 16-byte aligned when the
+// dtype is bfloat16 (tensor-memory-access copies need it).
+bool align_ok(const mla_config &c, std::initializer_list<const void *> ptrs)
+{
+    if (c.dtype != MLA_DTYPE_BF16) return true;
+    for (const void *p : ptrs)
+        if (p && !aligned16(p)) return false;
+    return true;
+}
+
+GemmArgs linear_args(const void *A, int64_t lda, const void *W, int64_t ldw, int M, int N, int K,
+                     void *out, int64_t ldc)
+{
+    GemmArgs g;
+    g.A = A; g.lda = lda;
+    g.B = W; g.ldb = ldw;
+    g.M = M; g.N = N; g.K = K;
+    g.epi.out = out; g.epi.ldc = ldc;
+    return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_check_config(const mla_config *c)
+{
+    if (!c) return MLA_ERR_INVALID_ARG;
+    if (c->variant < MLA_VARIANT_DECOUPLED || c->variant > MLA_VARIANT_MLRA) return MLA_ERR_INVALID_ARG;
+    if (c->dtype != MLA_DTYPE_F32 && c->dtype != MLA_DTYPE_BF16) return MLA_ERR_INVALID_ARG;
+    if (c->d_model <= 0 || c->n_heads <= 0 || c->d_nope <= 0 || c->d_v <= 0 || c->r_kv <= 0 ||
+        c->max_batch <= 0 || c->max_seq <= 0 || c->n_latent_heads <= 0 || !(c->rope_base > 0.0))
+        return MLA_ERR_INVALID_ARG;
+    if (c->d_v != c->d_nope) return MLA_ERR_INVALID_ARG;
+    switch (c->variant) {
+    case MLA_VARIANT_DECOUPLED:
+        // deepseek-mla __init__: d_c < d_embed and d_c1 < d_embed;
+        // apply_rotary_emb: the rotated width is even.
+        if (c->d_rope <= 0 || c->d_rope % 2 || c->r_q <= 0 || c->n_latent_heads != 1)
+            return MLA_ERR_INVALID_ARG;
+        if (c->r_kv >= c->d_model || c->r_q >= c->d_model) return MLA_ERR_INVALID_ARG;
+        break;
+    case MLA_VARIANT_SMALL:
+        // mla_attn __init__: head_dim = hidden_size / num_heads, divisible.
+        if (c->d_rope != 0 || c->r_q != 0 || c->n_latent_heads != 1) return MLA_ERR_INVALID_ARG;
+        if (c->d_model % c->n_heads || c->d_nope != c->d_model / c->n_heads || c->d_nope % 2)
+            return MLA_ERR_INVALID_ARG;
+        break;
+    case MLA_VARIANT_MLRA:
+        // mlra_attn __init__: L | latent_rank and L | num_heads * head_dim.
+        if (c->d_rope != 0 || c->r_q != 0) return MLA_ERR_INVALID_ARG;
+        if (c->d_model % c->n_heads || c->d_nope != c->d_model / c->n_heads) return MLA_ERR_INVALID_ARG;
+        if (c->r_kv % c->n_latent_heads || (c->n_heads * c->d_nope) % c->n_latent_heads)
+            return MLA_ERR_INVALID_ARG;
+        // Each head must read exactly one latent block.
+        if ((c->n_heads * c->d_nope / c->n_latent_heads) % c->d_nope) return MLA_ERR_UNSUPPORTED;
+        break;
+    }
+    int rd = rope_dim_of(*c);
+    if (rd > 0 && (rd > 64 || 64 % rd)) return MLA_ERR_UNSUPPORTED;
+    if (c->d_v > 128 || c->d_nope + c->d_rope > 256) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+mla_status mla_create(const mla_config *cfg, mla_handle **out)
+{
+    if (!out) return MLA_ERR_INVALID_ARG;
+    *out = nullptr;
+    mla_status st = mla_check_config(cfg);
+    if (st != MLA_OK) return st;
+    mla_handle *h = new (std::nothrow) mla_handle();
+    if (!h) return MLA_ERR_CUDA;
+    h->cfg = *cfg;
+    h->rope_dim = rope_dim_of(*cfg);
+    h->rope_table = nullptr;
+    if (cudaGetDevice(&h->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        delete h;
+        return MLA_ERR_CUDA;
+    }
+    if (h->rope_dim > 0) {
+        // cos/sin of pos * base^(-2i/d) (deepseek-mla precompute_freqs_cis,
+        // mla_attn _apply_rope), evaluated in double and stored as float.
+        int half = h->rope_dim / 2;
+        std::vector<float2> tab((size_t)cfg->max_seq * half);
+        for (int p = 0; p < cfg->max_seq; ++p)
+            for (int i = 0; i < half; ++i) {
+                double theta = pow(cfg->rope_base, -2.0 * i / (double)h->rope_dim);
+                double a = (double)p * theta;
+                tab[(size_t)p * half + i] = make_float2((float)cos(a), (float)sin(a));
+            }
+        if (cudaMalloc(&h->rope_table, tab.size() * sizeof(float2)) != cudaSuccess) {
+            delete h;
+            return MLA_ERR_CUDA;
+        }
+        if (cudaMemcpy(h->rope_table, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+            cudaSuccess) {
+            cudaFree(h->rope_table);
+            delete h;
+            return MLA_ERR_CUDA;
+        }
+    }
+    *out = h;
+    return MLA_OK;
+}
+
+void mla_destroy(mla_handle *h)
+{
+    if (!h) return;
+    if (h->rope_table) cudaFree(h->rope_table);
+    delete h;
+}
+
+size_t mla_workspace_size(const mla_handle *h, int batch, int max_len, int64_t n_tokens)
+{
+    if (!h || batch < 0 || max_len < 0 || n_tokens < 0) return 0;
+    const mla_config &c = h->cfg;
+    size_t need = kWsHeader;
+    need = std::max(need, project_ws(c, n_tokens).end);
+    if (c.variant != MLA_VARIANT_SMALL) need = std::max(need, decode_ws(c, batch).end);
+    need = std::max(need, prefill_ws(c, batch, max_len).end);
+    return need;
+}
+
+mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x, int64_t T,
+                              const int32_t *seq_idx, const int32_t *pos, const mla_cache *cache,
+                              void *q_nope, void *q_rope, void *ws, size_t ws_bytes, void *stream)
+{
+    if (!h || !w || !cache || T < 0) return MLA_ERR_INVALID_ARG;
+    if (T == 0) return MLA_OK;
+    const mla_config &c = h->cfg;
+    if (T > (int64_t)c.max_batch * c.max_seq || T > INT32_MAX) return MLA_ERR_INVALID_ARG;
+    if (!x || !seq_idx || !pos || !q_nope || !ws || !cache->lat || !w->W_DKV) return MLA_ERR_INVALID_ARG;
+    const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
+    if (dec) {
+        if (!q_rope || !cache->rope || !w->W_DQ || !w->W_UQ || !w->W_QR || !w->W_KR) return MLA_ERR_INVALID_ARG;
+        if (cache->rope_stride < c.d_rope) return MLA_ERR_INVALID_ARG;
+    } else if (q_rope || !w->W_Q) {
+        return MLA_ERR_INVALID_ARG;
+    }
+    if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
+    if (!align_ok(c, {x, q_nope, q_rope, cache->lat, cache->rope, w->W_DQ, w->W_UQ, w->W_QR, w->W_DKV,
+                      w->W_KR, w->W_Q, ws}))
+        return MLA_ERR_INVALID_ARG;
+    ProjectWs L = project_ws(c, T);
+    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t *status = (uint32_t *)ws;
+    const int M = (int)T, H = c.n_heads;
+    char *wsb = (char *)ws;
+
+    // Latent and (decoupled) rope key, written straight into the caches.
+    GemmArgs g = linear_args(x, c.d_model, w->W_DKV, c.d_model, M, c.r_kv, c.d_model, cache->lat,
+                             cache->lat_stride);
+    g.epi.row_seq = seq_idx; g.epi.row_pos = pos; g.epi.seq_rows = c.max_seq;
+    g.epi.max_batch = c.max_batch; g.epi.max_seq = c.max_seq; g.epi.status = status;
+    MLA_TRY_CUDA(gemm_simt(c.dtype, g, s));
+    if (dec) {
+        GemmArgs r = g;
+        r.B = w->W_KR; r.N = c.d_rope;
+        r.epi.out = cache->rope; r.epi.ldc = cache->rope_stride;
+        r.epi.rope_mode = kRopeInterleaved; r.epi.rope_dim = c.d_rope;
+        r.epi.rope_table = h->rope_table; r.epi.rope_pos = pos;
+        MLA_TRY_CUDA(gemm_simt(c.dtype, r, s));
+
+        void *cq = wsb + L.cq;
+        GemmArgs a = linear_args(x, c.d_model, w->W_DQ, c.d_model, M, c.r_q, c.d_model, cq, c.r_q);
+        MLA_TRY_CUDA(gemm_simt(c.dtype, a, s));
+        GemmArgs qn = linear_args(cq, c.r_q, w->W_UQ, c.r_q, M, H * c.d_nope, c.r_q, q_nope,
+                                  (int64_t)H * c.d_nope);
+        MLA_TRY_CUDA(gemm_simt(c.dtype, qn, s));
+        GemmArgs qr = linear_args(cq, c.r_q, w->W_QR, c.r_q, M, H * c.d_rope, c.r_q, q_rope,
+                                  (int64_t)H * c.d_rope);
+        qr.epi.rope_mode = kRopeInterleaved; qr.epi.rope_dim = c.d_rope;
+        qr.epi.rope_table = h->rope_table; qr.epi.rope_pos = pos;
+        qr.epi.max_seq = c.max_seq; qr.epi.status = status;
+        MLA_TRY_CUDA(gemm_simt(c.dtype, qr, s));
+    } else {
+        GemmArgs q = linear_args(x, c.d_model, w->W_Q, c.d_model, M, H * c.d_nope, c.d_model, q_nope,
+                                 (int64_t)H * c.d_nope);
+        if (c.variant == MLA_VARIANT_SMALL) {
+            q.epi.rope_mode = kRopeHalf; q.epi.rope_dim = c.d_nope;
+            q.epi.rope_table = h->rope_table; q.epi.rope_pos = pos;
+            q.epi.max_seq = c.max_seq; q.epi.status = status;
+        }
+        MLA_TRY_CUDA(gemm_simt(c.dtype, q, s));
+    }
+    return MLA_OK;
+}
+
+mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
+                       const mla_cache *cache, int B, int S, const int32_t *start_pos, void *o,
+                       void *ws, size_t ws_bytes, void *stream)
+{
+    if (!h || !w || !cache || B < 0 || S < 0) return MLA_ERR_INVALID_ARG;
+    if (B == 0 || S == 0) return MLA_OK;
+    const mla_config &c = h->cfg;
+    const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
+    if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
+    if (!q_nope || !o || !ws || !cache->lat || !w->W_UK || !w->W_UV) return MLA_ERR_INVALID_ARG;
+    if (dec && (!q_rope || !cache->rope || cache->rope_stride < c.d_rope)) return MLA_ERR_INVALID_ARG;
+    if (!dec && q_rope) return MLA_ERR_INVALID_ARG;
+    if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
+    if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
+        return MLA_ERR_INVALID_ARG;
+    int64_t kv_rows = 0;
+    for (int b = 0; b < B; ++b) {
+        int sp = start_pos ? start_pos[b] : 0;
+        if (sp < 0) return MLA_ERR_INVALID_ARG;
+        if ((int64_t)sp + S > c.max_seq) return MLA_ERR_CACHE_OVERFLOW;
+        kv_rows = std::max<int64_t>(kv_rows, (int64_t)sp + S);
+    }
+    PrefillWs L = prefill_ws(c, B, kv_rows);
+    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *wsb = (char *)ws;
+    int32_t *d_sp = (int32_t *)(wsb + L.start_pos);
+    if (start_pos) MLA_TRY_CUDA(cudaMemcpyAsync(d_sp, start_pos, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s));
+    else MLA_TRY_CUDA(cudaMemsetAsync(d_sp, 0, sizeof(int32_t) * B, s));
+    void *kbuf = wsb + L.k, *vbuf = wsb + L.v;
+    const int H = c.n_heads;
+    const int64_t ldk = (int64_t)H * c.d_nope, ldv = (int64_t)H * c.d_v;
+
+    // Keys and values of every cached row in use (deepseek-mla forward:
+    // UK_proj / UV_proj of the cached latent; mla_attn: k is then rotated;
+    // mlra_attn: block-wise up-projections concatenated per head).
+    int nblk = c.variant == MLA_VARIANT_MLRA ? c.n_latent_heads : 1;
+    int sub_rank = c.r_kv / nblk, sub_k = H * c.d_nope / nblk, sub_v = H * c.d_v / nblk;
+    for (int blk = 0; blk < nblk; ++blk) {
+        GemmArgs gk;
+        gk.A = (const char *)cache->lat + (size_t)blk * sub_rank * esize(c);
+        gk.lda = cache->lat_stride;
+        gk.batch_stride_a = (int64_t)c.max_seq * cache->lat_stride;
+        gk.B = (const char *)w->W_UK + (size_t)blk * sub_k * sub_rank * esize(c);
+        gk.ldb = sub_rank;
+        gk.M = (int)kv_rows; gk.N = sub_k; gk.K = sub_rank; gk.batch = B;
+        gk.epi.out = (char *)kbuf + (size_t)blk * sub_k * esize(c);
+        gk.epi.ldc = ldk;
+        gk.epi.batch_stride = kv_rows * ldk;
+        if (c.variant == MLA_VARIANT_SMALL) {
+            gk.epi.rope_mode = kRopeHalf; gk.epi.rope_dim = c.d_nope;
+            gk.epi.rope_table = h->rope_table; gk.epi.max_seq = c.max_seq;
+        }
+        MLA_TRY_CUDA(gemm_simt(c.dtype, gk, s));
+        GemmArgs gv = gk;
+        gv.B = (const char *)w->W_UV + (size_t)blk * sub_v * sub_rank * esize(c);
+        gv.N = sub_v;
+        gv.epi = Epilogue();
+        gv.epi.out = (char *)vbuf + (size_t)blk * sub_v * esize(c);
+        gv.epi.ldc = ldv;
+        gv.epi.batch_stride = kv_rows * ldv;
+        MLA_TRY_CUDA(gemm_simt(c.dtype, gv, s));
+    }
+    PrefillArgs p;
+    p.dtype = c.dtype;
+    p.B = B; p.S = S; p.H = H;
+    p.d_qk_nope = c.d_nope; p.d_rope = dec ? c.d_rope : 0; p.d_v = c.d_v;
+    p.q_nope = q_nope; p.q_rope = dec ? q_rope : nullptr;
+    p.k = kbuf; p.v = vbuf; p.kv_rows = kv_rows;
+    p.rope = dec ? cache->rope : nullptr; p.rope_stride = cache->rope_stride;
+    p.max_seq = c.max_seq;
+    p.start_pos = d_sp;
+    p.scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
+    p.o = o;
+    MLA_TRY_CUDA(prefill_simt(p, s));
+    return MLA_OK;
+}
+
+mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
+                      const mla_cache *cache, const int32_t *seq_lens, int B, void *o, void *ws,
+                      size_t ws_bytes, void *stream)
+{
+    if (!h || !w || !cache || B < 0) return MLA_ERR_INVALID_ARG;
+    const mla_config &c = h->cfg;
+    if (c.variant == MLA_VARIANT_SMALL) return MLA_ERR_UNSUPPORTED;
+    if (B == 0) return MLA_OK;
+    const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
+    if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
+    if (!q_nope || !o || !ws || !seq_lens || !cache->lat || !w->W_UK || !w->W_UV) return MLA_ERR_INVALID_ARG;
+    if (dec && (!q_rope || !cache->rope || cache->rope_stride < c.d_rope)) return MLA_ERR_INVALID_ARG;
+    if (!dec && q_rope) return MLA_ERR_INVALID_ARG;
+    if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
+    if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
+        return MLA_ERR_INVALID_ARG;
+    DecodeWs L = decode_ws(c, B);
+    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    char *wsb = (char *)ws;
+    const int H = c.n_heads, r_lat = r_lat_of(c);
+    void *q_abs = wsb + L.q_abs, *o_lat = wsb + L.o_lat;
+
+    // q_abs[b, h] = W_UK,h^T q_nope[b, h]: per head h, [B, d_nope] x [d_nope, r_lat].
+    // (MLRA: the L stacked blocks [L, H*d/L, r/L] read as [H*d, r/L] rows.)
+    GemmArgs ga;
+    ga.A = q_nope; ga.lda = (int64_t)H * c.d_nope; ga.batch_stride_a = c.d_nope;
+    ga.B = w->W_UK; ga.ldb = r_lat; ga.batch_stride_b = (int64_t)c.d_nope * r_lat; ga.trans_b = true;
+    ga.M = B; ga.N = r_lat; ga.K = c.d_nope; ga.batch = H;
+    ga.epi.out = q_abs; ga.epi.ldc = (int64_t)H * r_lat; ga.epi.batch_stride = r_lat;
+    MLA_TRY_CUDA(gemm_simt(c.dtype, ga, s));
+
+    DecodeArgs d;
+    d.dtype = c.dtype;
+    d.B = B; d.H = H; d.r_lat = r_lat; d.d_rope = dec ? c.d_rope : 0;
+    d.heads_per_block_lat = heads_per_block_of(c);
+    d.q_abs = q_abs; d.q_rope = dec ? q_rope : nullptr;
+    d.lat = cache->lat; d.lat_stride = cache->lat_stride;
+    d.rope = dec ? cache->rope : nullptr; d.rope_stride = cache->rope_stride;
+    d.max_seq = c.max_seq;
+    d.seq_lens = seq_lens;
+    d.scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
+    d.o_part = (float *)(wsb + L.o_part);
+    d.ml_part = (float *)(wsb + L.ml_part);
+    d.n_split = decode_splits(c);
+    d.chunk = kDecodeChunk;
+    d.o_lat = o_lat;
+    d.status = (uint32_t *)ws;
+    if (d.n_split > 64) return MLA_ERR_UNSUPPORTED;
+    MLA_TRY_CUDA(decode_simt(d, s));
+
+    // o[b, h] = W_UV,h o_lat[b, h]: per head h, [B, r_lat] x [r_lat, d_v].
+    GemmArgs gv;
+    gv.A = o_lat; gv.lda = (int64_t)H * r_lat; gv.batch_stride_a = r_lat;
+    gv.B = w->W_UV; gv.ldb = r_lat; gv.batch_stride_b = (int64_t)c.d_v * r_lat;
+    gv.M = B; gv.N = c.d_v; gv.K = r_lat; gv.batch = H;
+    gv.epi.out = o; gv.epi.ldc = (int64_t)H * c.d_v; gv.epi.batch_stride = c.d_v;
+    MLA_TRY_CUDA(gemm_simt(c.dtype, gv, s));
+    return MLA_OK;
+}
+
+mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int64_t T, void *y,
+                        void *stream)
+{
+    if (!h || !w || T < 0) return MLA_ERR_INVALID_ARG;
+    if (T == 0) return MLA_OK;
+    const mla_config &c = h->cfg;
+    if (!o || !y || !w->W_O || T > INT32_MAX) return MLA_ERR_INVALID_ARG;
+    if (!align_ok(c, {o, y, w->W_O})) return MLA_ERR_INVALID_ARG;
+    const int K = c.n_heads * c.d_v;
+    GemmArgs g = linear_args(o, K, w->W_O, K, (int)T, c.d_model, K, y, c.d_model);
+    MLA_TRY_CUDA(gemm_simt(c.dtype, g, (cudaStream_t)stream));
+    return MLA_OK;
+}
+
+mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t *bits)
+{
+    if (!h || !ws) return MLA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t v = 0;
+    MLA_TRY_CUDA(cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s));
+    MLA_TRY_CUDA(cudaStreamSynchronize(s));
+    MLA_TRY_CUDA(cudaMemsetAsync(ws, 0, sizeof(uint32_t), s));
+    MLA_TRY_CUDA(cudaStreamSynchronize(s));
+    if (bits) *bits = v;
+    return v ? MLA_ERR_DEVICE_DATA : MLA_OK;
+}
+
+uint64_t mla_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+mla_status mla_set_profile_events(int which, void *begin, void *end)
+{
+    if (which < 0 || which >= MLA_PROFILE_COUNT || (!begin) != (!end)) return MLA_ERR_INVALID_ARG;
+    g_prof_begin[which] = (cudaEvent_t)begin;
+    g_prof_end[which] = (cudaEvent_t)end;
+    return MLA_OK;
+}
+
+const char *mla_status_string(mla_status st)
+{
+    switch (st) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape or variant";
+    case MLA_ERR_WORKSPACE: return "workspace too small";
+    case MLA_ERR_CACHE_OVERFLOW: return "position beyond cache capacity";
+    case MLA_ERR_CUDA: return "CUDA error";
+    case MLA_ERR_TIMEOUT: return "bounded device wait timed out";
+    case MLA_ERR_DEVICE_DATA: return "device-side index data out of range";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,119 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "mla.h"
+
+struct mla_handle {
+    mla_config cfg;
+    int device;
+    int num_sms;
+    int rope_dim;        // rotated width: d_rope (decoupled), d_nope (small), 0 (MLRA)
+    float2 *rope_table;  // [max_seq, rope_dim / 2] (cos, sin) of pos * base^(-2i/rope_dim)
+};
+
+namespace mla {
+
+// Launch bookkeeping and the optional timing hook (api.cu).
+void note_launch(int n = 1);
+void profile_begin(int which, cudaStream_t s);
+void profile_end(int which, cudaStream_t s);
+
+// Workspace status bits (mirrors the values documented in mla.h).
+constexpr uint32_t kStatusPos = 1u;
+constexpr uint32_t kStatusSeq = 2u;
+constexpr uint32_t kStatusLen = 4u;
+
+// Workspace: the first 256 bytes hold the status word; call scratch follows.
+constexpr size_t kWsHeader = 256;
+
+enum RopeMode { kRopeNone = 0, kRopeInterleaved = 1, kRopeHalf = 2 };
+
+// Element types the kernels are instantiated for.
+using bf16 = __nv_bfloat16;
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<bf16>(bf16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// Output stage of a projection GEMM C[M, N] = A[M, K] B^T.
+//  - Row destination: row m goes to out + m * ldc, or, when row_seq is set, to
+//    cache row (row_seq[m], row_pos[m]) = out + (seq * seq_rows + pos) * ldc
+//    (rows whose sequence or position is out of range are skipped and flagged).
+//  - Optional RoPE on every column (groups of rope_dim columns; tiles never
+//    straddle a group): the position of row m is rope_pos[m], or m when
+//    rope_pos is null.
+struct Epilogue {
+    void *out = nullptr;
+    int64_t ldc = 0;
+    int64_t batch_stride = 0;  // elements between batch entries of out
+    const int32_t *row_seq = nullptr;
+    const int32_t *row_pos = nullptr;
+    int64_t seq_rows = 0;
+    int max_batch = 0;
+    int max_seq = 0;
+    int rope_mode = kRopeNone;
+    int rope_dim = 0;
+    const float2 *rope_table = nullptr;
+    const int32_t *rope_pos = nullptr;
+    uint32_t *status = nullptr;
+};
+
+struct GemmArgs {
+    const void *A = nullptr;
+    int64_t lda = 0, batch_stride_a = 0;
+    const void *B = nullptr;
+    int64_t ldb = 0, batch_stride_b = 0;
+    bool trans_b = false;  // false: B is [N, K] (K contiguous); true: B is [K, N]
+    int M = 0, N = 0, K = 0, batch = 1;
+    Epilogue epi;
+};
+
+// CUDA-core kernels (every dtype; the float32 path and small shapes).
+cudaError_t gemm_simt(int dtype, const GemmArgs &a, cudaStream_t s);
+
+struct DecodeArgs {
+    int dtype;
+    int B, H, r_lat, d_rope;   // r_lat: latent width one head attends over
+    int heads_per_block_lat;   // heads sharing one latent block (H for MLA, H/L for MLRA)
+    const void *q_abs;         // [B, H, r_lat]
+    const void *q_rope;        // [B, H, d_rope] or null
+    const void *lat;           // cache latent rows
+    int64_t lat_stride;
+    const void *rope;          // cache rope rows or null
+    int64_t rope_stride;
+    int max_seq;
+    const int32_t *seq_lens;   // device [B]
+    float scale_log2;          // softmax scale * log2(e)
+    float *o_part;             // [B, n_split, H, r_lat]
+    float *ml_part;            // [B, n_split, H, 2] (running max in log2 units, sum)
+    int n_split, chunk;
+    void *o_lat;               // [B, H, r_lat] (dtype)
+    uint32_t *status;
+};
+cudaError_t decode_simt(const DecodeArgs &a, cudaStream_t s);
+
+struct PrefillArgs {
+    int dtype;
+    int B, S, H, d_qk_nope, d_rope, d_v;
+    const void *q_nope;        // [B, S, H, d_qk_nope]
+    const void *q_rope;        // [B, S, H, d_rope] or null
+    const void *k;             // [B, kv_rows, H, d_qk_nope]
+    const void *v;             // [B, kv_rows, H, d_v]
+    int64_t kv_rows;
+    const void *rope;          // cache rope rows (decoupled) or null
+    int64_t rope_stride;
+    int max_seq;
+    const int32_t *start_pos;  // device [B]
+    float scale_log2;
+    void *o;                   // [B, S, H, d_v]
+};
+cudaError_t prefill_simt(const PrefillArgs &a, cudaStream_t s);
+
+}  // namespace mla

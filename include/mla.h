@@ -1,0 +1,222 @@
+/*
+ * mla.h — C ABI of the GB300 (sm_103a) Multi-Head Latent Attention library.
+ *
+ * The library computes the hot path of Multi-Head Latent Attention over a
+ * compressed latent KV cache, in three forms taken from web pages on the
+ * subject:
+ *
+ *  DECOUPLED  DeepSeek-V2-style MLA ("bird-of-paradise/deepseek-mla",
+ *             src/mla.py, MultiHeadLatentAttention): c_Q = W_DQ x,
+ *             q_C = W_UQ c_Q, q_R = RoPE(W_QR c_Q) per head, c_KV = W_DKV x,
+ *             k_R = RoPE(W_KR x) shared by all heads; scores
+ *             (q_C . W_UK c_KV + q_R . k_R) / sqrt(d_nope + d_rope), causal
+ *             softmax, weighted sum of W_UV c_KV, output projection W_O.
+ *             RoPE pairs elements (2i, 2i+1) (apply_rotary_emb).
+ *  SMALL      small-model MLA ("frankenstein-transformer", latent/mla_attn.py,
+ *             MLAAttention): q = W_Q x, k = W_UK c_KV, v = W_UV c_KV, RoPE on
+ *             the decompressed q and k with half-split pairs (i, i + d/2)
+ *             (_apply_rope), scale 1/sqrt(d).
+ *  MLRA       multi-head low-rank attention ("frankenstein-transformer",
+ *             latent/mlra_attn.py, MLRAAttention): the latent is split into L
+ *             disjoint blocks of rank r_kv/L, each with its own up-projections;
+ *             no RoPE, scale 1/sqrt(d).
+ *
+ * Readings of the pages that this ABI fixes: attention is always causal (the
+ * query at absolute position p sees keys 0..p); positions are absolute and
+ * 0-based for queries and cached keys alike; the rope-key cache holds k_R
+ * after rotation; there are no biases and no dropout; d_v == d_nope.
+ *
+ * Conventions for every entry point
+ *  - Tensors are caller-owned device memory, row-major, in the handle's
+ *    dtype (float32 or bfloat16) unless stated.  Weights use the nn.Linear
+ *    layout [out, in].  Index arrays are int32.  The library allocates
+ *    nothing during compute calls: scratch comes from the caller's workspace
+ *    `ws` (device memory, 256-byte aligned, at least mla_workspace_size()
+ *    bytes, zero-filled once before first use).
+ *  - Pointers handed to the tensor-core path must be 16-byte aligned and row
+ *    strides multiples of 16 bytes; violations return MLA_ERR_INVALID_ARG.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream).  Host-side validation happens before anything is
+ *    enqueued and returns synchronously; launch failures return MLA_ERR_CUDA.
+ *    Bad index data that only the device can see (a position or length out
+ *    of range) never traps: the kernel skips that row and sets a bit in the
+ *    workspace status word, read with mla_get_device_status().
+ *  - A handle is immutable after mla_create(); calls on different streams
+ *    are safe when their output buffers and workspaces differ.
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misalignment */
+    MLA_ERR_UNSUPPORTED = 2,    /* dims or variant this build does not run */
+    MLA_ERR_WORKSPACE = 3,      /* ws_bytes smaller than required */
+    MLA_ERR_CACHE_OVERFLOW = 4, /* host-known position beyond max_seq */
+    MLA_ERR_CUDA = 5,           /* a CUDA runtime or driver call failed */
+    MLA_ERR_TIMEOUT = 6,        /* a bounded device wait gave up */
+    MLA_ERR_DEVICE_DATA = 7     /* device-side index data was out of range */
+} mla_status;
+
+typedef enum {
+    MLA_VARIANT_DECOUPLED = 0,
+    MLA_VARIANT_SMALL = 1,
+    MLA_VARIANT_MLRA = 2
+} mla_variant;
+
+typedef enum { MLA_DTYPE_F32 = 0, MLA_DTYPE_BF16 = 1 } mla_dtype;
+
+/* Layer shape.  Field names follow the pages' notation.
+ *  d_nope          per-head query/key width (the pages' d_head)
+ *  d_rope          decoupled rope-key width (DECOUPLED only, even; else 0)
+ *  d_v             per-head value width (== d_nope)
+ *  r_kv            latent rank (the cached width)
+ *  r_q             query compression rank (DECOUPLED only; else 0)
+ *  n_latent_heads  L (MLRA only; 1 otherwise)
+ *  rope_base       RoPE base (10000 on the pages)
+ *  max_batch, max_seq  cache capacity: positions must lie in [0, max_seq)
+ * Checks (mla_check_config): positive sizes; DECOUPLED r_kv < d_model and
+ * r_q < d_model (deepseek-mla __init__ asserts) and even d_rope
+ * (apply_rotary_emb); SMALL even d_nope; MLRA L | r_kv and L | H*d_nope
+ * (MLRAAttention.__init__), and H*d_nope/L a multiple of d_nope so that each
+ * head reads one latent block. */
+typedef struct {
+    int variant;    /* mla_variant */
+    int dtype;      /* mla_dtype */
+    int d_model, n_heads, d_nope, d_rope, d_v, r_kv, r_q, n_latent_heads;
+    double rope_base;
+    int max_batch, max_seq;
+} mla_config;
+
+/* Device weight pointers, nn.Linear layout [out, in]; unused ones NULL.
+ *  DECOUPLED: W_DQ [r_q, d_model], W_UQ [H*d_nope, r_q], W_QR [H*d_rope, r_q],
+ *             W_DKV [r_kv, d_model], W_KR [d_rope, d_model],
+ *             W_UK [H*d_nope, r_kv], W_UV [H*d_v, r_kv], W_O [d_model, H*d_v]
+ *  SMALL:     W_Q [H*d_nope, d_model], W_DKV, W_UK, W_UV, W_O as above
+ *  MLRA:      W_Q, W_DKV, W_O as above; W_UK [L, H*d_nope/L, r_kv/L] and
+ *             W_UV [L, H*d_v/L, r_kv/L] (the L stacked block projections) */
+typedef struct {
+    const void *W_DQ, *W_UQ, *W_QR, *W_DKV, *W_KR, *W_UK, *W_UV, *W_O, *W_Q;
+} mla_weights;
+
+/* Caches (deepseek-mla __init__: cache_kv [max_batch, max_seq, d_c] and
+ * cache_rk [max_batch, max_seq, d_rotate]).  lat: [max_batch, max_seq] rows
+ * of lat_stride elements, the first r_kv used; rope: same with rope_stride
+ * and d_rope used (DECOUPLED only, else NULL).  A packed layout with
+ * rope == lat + r_kv and both strides r_kv + d_rope is allowed. */
+typedef struct {
+    void *lat;
+    void *rope;
+    int64_t lat_stride, rope_stride;
+} mla_cache;
+
+typedef struct mla_handle mla_handle;
+
+/* Validate a configuration without touching any device.  Returns MLA_OK,
+ * MLA_ERR_INVALID_ARG (sizes, null) or MLA_ERR_UNSUPPORTED. */
+mla_status mla_check_config(const mla_config *cfg);
+
+/* Create a handle on the current CUDA device: validates cfg and builds the
+ * float32 RoPE cos/sin table for positions [0, max_seq) (angles evaluated in
+ * double precision on the host).  *out is NULL on failure. */
+mla_status mla_create(const mla_config *cfg, mla_handle **out);
+
+/* Release a handle and its table (NULL is allowed).  Synchronises nothing;
+ * the caller must not destroy a handle with work still in flight. */
+void mla_destroy(mla_handle *h);
+
+/* Workspace bytes that any call on up to `batch` sequences of up to
+ * `max_len` keys, or on up to `n_tokens` projected tokens, needs.
+ * Returns 0 if h is NULL or a size is negative. */
+size_t mla_workspace_size(const mla_handle *h, int batch, int max_len,
+                          int64_t n_tokens);
+
+/* Latent projection, query projection and cache append, per token t of
+ * sequence seq_idx[t] at absolute position pos[t] (deepseek-mla forward,
+ * query path and use_cache branch; mla_attn / mlra_attn forward):
+ *  DECOUPLED: cache.lat[seq, pos] = W_DKV x,  cache.rope[seq, pos] =
+ *             RoPE_pos(W_KR x), q_nope = W_UQ W_DQ x  [T, H, d_nope],
+ *             q_rope = RoPE_pos(W_QR W_DQ x) per head [T, H, d_rope]
+ *  SMALL:     cache.lat[seq, pos] = W_DKV x, q_nope = RoPE_half,pos(W_Q x)
+ *             [T, H, d_nope]; q_rope must be NULL
+ *  MLRA:      cache.lat[seq, pos] = W_DKV x, q_nope = W_Q x; q_rope NULL
+ * x [T, d_model]; seq_idx, pos: device int32 [T].  T == 0 is a no-op.
+ * Tokens whose seq_idx or pos is out of range are skipped and flagged in the
+ * workspace status word.  Workspace: the c_Q intermediate (DECOUPLED). */
+mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x,
+                              int64_t T, const int32_t *seq_idx, const int32_t *pos,
+                              const mla_cache *cache, void *q_nope, void *q_rope,
+                              void *ws, size_t ws_bytes, void *stream);
+
+/* Causal prefill attention of S new queries per sequence against the cache
+ * (deepseek-mla forward; mla_attn / mlra_attn forward in decoder mode).
+ * Query i of sequence b sits at position start_pos[b] + i and sees cached
+ * keys 0..start_pos[b] + i (which mla_project_latent must have written).
+ * q_nope [B, S, H, d_nope], q_rope [B, S, H, d_rope] (DECOUPLED, else NULL),
+ * o [B, S, H, d_v].  start_pos: HOST int32 [B] (NULL means all zero);
+ * start_pos[b] + S > max_seq returns MLA_ERR_CACHE_OVERFLOW.  The keys and
+ * values of every cached row in use are up-projected into the workspace. */
+mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope,
+                       const void *q_rope, const mla_cache *cache, int B, int S,
+                       const int32_t *start_pos, void *o, void *ws, size_t ws_bytes,
+                       void *stream);
+
+/* One decode step for B sequences, weight-absorbed: the query of sequence b
+ * sits at position seq_lens[b] - 1 and sees cached keys 0..seq_lens[b] - 1
+ * (the length includes the new token, which mla_project_latent must have
+ * appended).  DECOUPLED: q_abs = W_UK,h^T q_nope,h; scores q_abs . c_j +
+ * q_rope,h . k_R,j over the latent cache; o_lat = softmax-weighted sum of c_j;
+ * o_h = W_UV,h o_lat.  MLRA: the same per latent block.  SMALL returns
+ * MLA_ERR_UNSUPPORTED (RoPE sits between W_UK and the query, so there is no
+ * absorbed form).  q_nope [B, H, d_nope], q_rope [B, H, d_rope] or NULL,
+ * o [B, H, d_v]; seq_lens: DEVICE int32 [B], each in [1, max_seq] (others
+ * skipped and flagged).  B <= max_batch. */
+mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope,
+                      const void *q_rope, const mla_cache *cache,
+                      const int32_t *seq_lens, int B, void *o, void *ws,
+                      size_t ws_bytes, void *stream);
+
+/* Output projection y = W_O [o_1 ‖ ... ‖ o_H] (deepseek-mla output_proj;
+ * out_proj in mla_attn / mlra_attn).  o [T, H*d_v], y [T, d_model]. */
+mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int64_t T,
+                        void *y, void *stream);
+
+/* Synchronise `stream`, read and clear the workspace status word.  *bits
+ * receives the flags (1: position out of range, 2: sequence index out of
+ * range, 4: decode length out of range); the return value is MLA_OK when no
+ * flag was set, MLA_ERR_DEVICE_DATA otherwise. */
+mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t *bits);
+
+/* Static English text for a status code. */
+const char *mla_status_string(mla_status s);
+
+/* ---- Diagnostics (used by the benchmark; not needed for computing) ---- */
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t mla_launch_count(void);
+
+typedef enum {
+    MLA_PROFILE_DECODE_ATTENTION = 0,  /* the split-KV latent attention kernel */
+    MLA_PROFILE_PREFILL_ATTENTION = 1, /* the causal flash attention kernel */
+    MLA_PROFILE_COUNT = 2
+} mla_profile_point;
+
+/* Process-wide timing hook: while set, every launch of the kernel named by
+ * `which` is bracketed by cudaEventRecord(begin) / cudaEventRecord(end) on the
+ * stream of the call that launches it.  begin/end are cudaEvent_t handles
+ * owned by the caller; NULL clears the hook.  Not thread-safe: set it only
+ * while no other thread is calling into the library. */
+mla_status mla_set_profile_events(int which, void *begin, void *end);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */
