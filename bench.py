@@ -135,6 +135,21 @@ class ClockSampler:
 # Our arm
 # ---------------------------------------------------------------------------
 
+def timing_events(n):
+    """n (begin, end) pairs of timing events, created eagerly (torch creates
+    the underlying cudaEvent_t lazily, on first record) so that their handles
+    can be handed to the library's profiling hook."""
+    import torch
+    out = []
+    for _ in range(n):
+        pair = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        for e in pair:
+            e.record()
+        out.append(pair)
+    torch.cuda.synchronize()
+    return out
+
+
 def to_dev(stored, device):
     import torch
     if stored.dtype == np.uint16:
@@ -193,8 +208,8 @@ def run_ours(args, rank, world, device):
     sampler.start()
     time.sleep(0.2)
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev = timing_events(K)
+    kev = timing_events(K)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -227,7 +242,7 @@ def run_ours(args, rank, world, device):
     x_d = torch.empty_like(x)
     pos_d = torch.empty_like(pos)
     sl_d = torch.empty_like(sl)
-    eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    eev = timing_events(K)
     torch.cuda.synchronize()
     t2 = time.time()
     for i in range(K):
@@ -308,8 +323,8 @@ def run_prefill(args, lay_device):
         step()
     torch.cuda.synchronize()
     K = args.prefill_steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev = timing_events(K)
+    kev = timing_events(K)
     for i in range(K):
         mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, kev[i][0], kev[i][1])
         ev[i][0].record(stream)

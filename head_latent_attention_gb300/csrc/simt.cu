@@ -19,7 +19,7 @@ __device__ __forceinline__ float rope_elem(const float *row, int c, int dim, int
                                           const float2 *table, int pos)
 {
     if (mode == kRopeInterleaved) {
-        int i = c >> 1;
+        int i = (c % dim) >> 1;
         float2 cs = table[(int64_t)pos * (dim / 2) + i];
         float x0 = row[c & ~1], x1 = row[c | 1];
         return (c & 1) ? x0 * cs.y + x1 * cs.x : x0 * cs.x - x1 * cs.y;

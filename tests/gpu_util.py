@@ -8,7 +8,11 @@ import mla_synth as syn
 
 # Tolerances of the workload statement: float32 normwise max relative error
 # <= 1e-4; bfloat16 relative L2 error <= 1e-2 and max absolute error <= 3e-2
-# on outputs normalised to unit RMS.
+# on unit-scale outputs.  "Unit scale" is applied per output vector (the last
+# axis: one head's output of one token, or one token's projected row): each
+# vector is divided by the RMS of its reference.  Attention outputs that
+# average many keys are much smaller than those of the first rows, so one
+# global RMS would fail even an exactly computed output rounded to bfloat16.
 F32_MAX_REL = 1e-4
 BF16_REL_L2 = 1e-2
 BF16_MAX_ABS_UNIT = 3e-2
@@ -35,9 +39,9 @@ def compare(got, ref, dtype: int, what: str):
         m = float(np.max(np.abs(diff)) / max(np.max(np.abs(ref)), 1e-300))
         assert m <= F32_MAX_REL, f"{what}: normwise max rel err {m:.3e} > {F32_MAX_REL}"
         return {"max_rel": m}
-    rms = float(np.sqrt(np.mean(ref ** 2)))
+    rms = np.sqrt(np.mean(ref ** 2, axis=-1, keepdims=True))
     l2 = float(np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-300))
-    mabs = float(np.max(np.abs(diff)) / max(rms, 1e-300))
+    mabs = float(np.max(np.abs(diff) / np.maximum(rms, 1e-300))) if diff.size else 0.0
     assert l2 <= BF16_REL_L2, f"{what}: rel L2 {l2:.3e} > {BF16_REL_L2}"
     assert mabs <= BF16_MAX_ABS_UNIT, f"{what}: max abs (unit rms) {mabs:.3e} > {BF16_MAX_ABS_UNIT}"
     return {"rel_l2": l2, "max_abs_unit": mabs}
