@@ -109,16 +109,34 @@ bool align_ok(const mla_config &c, std::initializer_list<const void *> ptrs)
     return true;
 }
 
-GemmArgs linear_args(const void *A, int64_t lda, const void *W, int64_t ldw, int M, int N, int K,
+// y[M, N] = x[M, K] W^T with x, W row-major (W in nn.Linear layout [N, K]).
+GemmArgs linear_args(const void *x, int64_t ldx, const void *W, int64_t ldw, int M, int N, int K,
                      void *out, int64_t ldc)
 {
     GemmArgs g;
-    g.A = A; g.lda = lda;
-    g.B = W; g.ldb = ldw;
+    g.A = Mat2D{x, M, K, ldx};
+    g.B = Mat2D{W, N, K, ldw};
     g.M = M; g.N = N; g.K = K;
     g.epi.out = out; g.epi.ldc = ldc;
     return g;
 }
+
+// bfloat16 runs on the tensor cores, float32 on the CUDA cores.
+mla_status run_gemm(const mla_handle *h, GemmArgs g, uint32_t *status, cudaStream_t s)
+{
+    if (!g.epi.status) g.epi.status = status;
+    if (h->cfg.dtype == MLA_DTYPE_BF16) {
+        if (!gemm_tc_supported(g)) return MLA_ERR_UNSUPPORTED;
+        return cuda_status(gemm_tc(g, h->num_sms, s));
+    }
+    return cuda_status(gemm_simt(MLA_DTYPE_F32, g, s));
+}
+
+#define MLA_TRY(expr)                       \
+    do {                                    \
+        mla_status _st = (expr);            \
+        if (_st != MLA_OK) return _st;      \
+    } while (0)
 
 }  // namespace
 
@@ -174,9 +192,15 @@ mla_status mla_create(const mla_config *cfg, mla_handle **out)
     h->cfg = *cfg;
     h->rope_dim = rope_dim_of(*cfg);
     h->rope_table = nullptr;
+    h->status = nullptr;
     if (cudaGetDevice(&h->device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess ||
+        cudaMalloc(&h->status, 256) != cudaSuccess) {
         delete h;
+        return MLA_ERR_CUDA;
+    }
+    if (cudaMemset(h->status, 0, 256) != cudaSuccess) {
+        mla_destroy(h);
         return MLA_ERR_CUDA;
     }
     if (h->rope_dim > 0) {
@@ -190,14 +214,10 @@ mla_status mla_create(const mla_config *cfg, mla_handle **out)
                 double a = (double)p * theta;
                 tab[(size_t)p * half + i] = make_float2((float)cos(a), (float)sin(a));
             }
-        if (cudaMalloc(&h->rope_table, tab.size() * sizeof(float2)) != cudaSuccess) {
-            delete h;
-            return MLA_ERR_CUDA;
-        }
-        if (cudaMemcpy(h->rope_table, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
-            cudaSuccess) {
-            cudaFree(h->rope_table);
-            delete h;
+        if (cudaMalloc(&h->rope_table, tab.size() * sizeof(float2)) != cudaSuccess ||
+            cudaMemcpy(h->rope_table, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) !=
+                cudaSuccess) {
+            mla_destroy(h);
             return MLA_ERR_CUDA;
         }
     }
@@ -209,6 +229,7 @@ void mla_destroy(mla_handle *h)
 {
     if (!h) return;
     if (h->rope_table) cudaFree(h->rope_table);
+    if (h->status) cudaFree(h->status);
     delete h;
 }
 
@@ -254,37 +275,38 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
     GemmArgs g = linear_args(x, c.d_model, w->W_DKV, c.d_model, M, c.r_kv, c.d_model, cache->lat,
                              cache->lat_stride);
     g.epi.row_seq = seq_idx; g.epi.row_pos = pos; g.epi.seq_rows = c.max_seq;
-    g.epi.max_batch = c.max_batch; g.epi.max_seq = c.max_seq; g.epi.status = status;
-    MLA_TRY_CUDA(gemm_simt(c.dtype, g, s));
+    g.epi.max_batch = c.max_batch; g.epi.max_seq = c.max_seq;
+    MLA_TRY(run_gemm(h, g, status, s));
     if (dec) {
         GemmArgs r = g;
-        r.B = w->W_KR; r.N = c.d_rope;
+        r.B = Mat2D{w->W_KR, c.d_rope, c.d_model, c.d_model};
+        r.N = c.d_rope;
         r.epi.out = cache->rope; r.epi.ldc = cache->rope_stride;
         r.epi.rope_mode = kRopeInterleaved; r.epi.rope_dim = c.d_rope;
         r.epi.rope_table = h->rope_table; r.epi.rope_pos = pos;
-        MLA_TRY_CUDA(gemm_simt(c.dtype, r, s));
+        MLA_TRY(run_gemm(h, r, status, s));
 
         void *cq = wsb + L.cq;
         GemmArgs a = linear_args(x, c.d_model, w->W_DQ, c.d_model, M, c.r_q, c.d_model, cq, c.r_q);
-        MLA_TRY_CUDA(gemm_simt(c.dtype, a, s));
+        MLA_TRY(run_gemm(h, a, status, s));
         GemmArgs qn = linear_args(cq, c.r_q, w->W_UQ, c.r_q, M, H * c.d_nope, c.r_q, q_nope,
                                   (int64_t)H * c.d_nope);
-        MLA_TRY_CUDA(gemm_simt(c.dtype, qn, s));
+        MLA_TRY(run_gemm(h, qn, status, s));
         GemmArgs qr = linear_args(cq, c.r_q, w->W_QR, c.r_q, M, H * c.d_rope, c.r_q, q_rope,
                                   (int64_t)H * c.d_rope);
         qr.epi.rope_mode = kRopeInterleaved; qr.epi.rope_dim = c.d_rope;
         qr.epi.rope_table = h->rope_table; qr.epi.rope_pos = pos;
-        qr.epi.max_seq = c.max_seq; qr.epi.status = status;
-        MLA_TRY_CUDA(gemm_simt(c.dtype, qr, s));
+        qr.epi.max_seq = c.max_seq;
+        MLA_TRY(run_gemm(h, qr, status, s));
     } else {
         GemmArgs q = linear_args(x, c.d_model, w->W_Q, c.d_model, M, H * c.d_nope, c.d_model, q_nope,
                                  (int64_t)H * c.d_nope);
         if (c.variant == MLA_VARIANT_SMALL) {
             q.epi.rope_mode = kRopeHalf; q.epi.rope_dim = c.d_nope;
             q.epi.rope_table = h->rope_table; q.epi.rope_pos = pos;
-            q.epi.max_seq = c.max_seq; q.epi.status = status;
+            q.epi.max_seq = c.max_seq;
         }
-        MLA_TRY_CUDA(gemm_simt(c.dtype, q, s));
+        MLA_TRY(run_gemm(h, q, status, s));
     }
     return MLA_OK;
 }
@@ -329,11 +351,11 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
     int sub_rank = c.r_kv / nblk, sub_k = H * c.d_nope / nblk, sub_v = H * c.d_v / nblk;
     for (int blk = 0; blk < nblk; ++blk) {
         GemmArgs gk;
-        gk.A = (const char *)cache->lat + (size_t)blk * sub_rank * esize(c);
-        gk.lda = cache->lat_stride;
-        gk.batch_stride_a = (int64_t)c.max_seq * cache->lat_stride;
-        gk.B = (const char *)w->W_UK + (size_t)blk * sub_k * sub_rank * esize(c);
-        gk.ldb = sub_rank;
+        gk.A = Mat2D{(const char *)cache->lat + (size_t)blk * sub_rank * esize(c),
+                     (int64_t)c.max_batch * c.max_seq, sub_rank, cache->lat_stride};
+        gk.a_row_batch = c.max_seq;
+        gk.B = Mat2D{(const char *)w->W_UK + (size_t)blk * sub_k * sub_rank * esize(c), sub_k, sub_rank,
+                     sub_rank};
         gk.M = (int)kv_rows; gk.N = sub_k; gk.K = sub_rank; gk.batch = B;
         gk.epi.out = (char *)kbuf + (size_t)blk * sub_k * esize(c);
         gk.epi.ldc = ldk;
@@ -342,15 +364,16 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
             gk.epi.rope_mode = kRopeHalf; gk.epi.rope_dim = c.d_nope;
             gk.epi.rope_table = h->rope_table; gk.epi.max_seq = c.max_seq;
         }
-        MLA_TRY_CUDA(gemm_simt(c.dtype, gk, s));
+        MLA_TRY(run_gemm(h, gk, (uint32_t *)ws, s));
         GemmArgs gv = gk;
-        gv.B = (const char *)w->W_UV + (size_t)blk * sub_v * sub_rank * esize(c);
+        gv.B = Mat2D{(const char *)w->W_UV + (size_t)blk * sub_v * sub_rank * esize(c), sub_v, sub_rank,
+                     sub_rank};
         gv.N = sub_v;
         gv.epi = Epilogue();
         gv.epi.out = (char *)vbuf + (size_t)blk * sub_v * esize(c);
         gv.epi.ldc = ldv;
         gv.epi.batch_stride = kv_rows * ldv;
-        MLA_TRY_CUDA(gemm_simt(c.dtype, gv, s));
+        MLA_TRY(run_gemm(h, gv, (uint32_t *)ws, s));
     }
     PrefillArgs p;
     p.dtype = c.dtype;
@@ -393,11 +416,14 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     // q_abs[b, h] = W_UK,h^T q_nope[b, h]: per head h, [B, d_nope] x [d_nope, r_lat].
     // (MLRA: the L stacked blocks [L, H*d/L, r/L] read as [H*d, r/L] rows.)
     GemmArgs ga;
-    ga.A = q_nope; ga.lda = (int64_t)H * c.d_nope; ga.batch_stride_a = c.d_nope;
-    ga.B = w->W_UK; ga.ldb = r_lat; ga.batch_stride_b = (int64_t)c.d_nope * r_lat; ga.trans_b = true;
+    ga.A = Mat2D{q_nope, B, (int64_t)H * c.d_nope, (int64_t)H * c.d_nope};
+    ga.a_col_batch = c.d_nope;
+    ga.B = Mat2D{w->W_UK, (int64_t)H * c.d_nope, r_lat, r_lat};
+    ga.b_row_batch = c.d_nope;
+    ga.trans_b = true;
     ga.M = B; ga.N = r_lat; ga.K = c.d_nope; ga.batch = H;
     ga.epi.out = q_abs; ga.epi.ldc = (int64_t)H * r_lat; ga.epi.batch_stride = r_lat;
-    MLA_TRY_CUDA(gemm_simt(c.dtype, ga, s));
+    MLA_TRY(run_gemm(h, ga, (uint32_t *)ws, s));
 
     DecodeArgs d;
     d.dtype = c.dtype;
@@ -420,11 +446,13 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
 
     // o[b, h] = W_UV,h o_lat[b, h]: per head h, [B, r_lat] x [r_lat, d_v].
     GemmArgs gv;
-    gv.A = o_lat; gv.lda = (int64_t)H * r_lat; gv.batch_stride_a = r_lat;
-    gv.B = w->W_UV; gv.ldb = r_lat; gv.batch_stride_b = (int64_t)c.d_v * r_lat;
+    gv.A = Mat2D{o_lat, B, (int64_t)H * r_lat, (int64_t)H * r_lat};
+    gv.a_col_batch = r_lat;
+    gv.B = Mat2D{w->W_UV, (int64_t)H * c.d_v, r_lat, r_lat};
+    gv.b_row_batch = c.d_v;
     gv.M = B; gv.N = c.d_v; gv.K = r_lat; gv.batch = H;
     gv.epi.out = o; gv.epi.ldc = (int64_t)H * c.d_v; gv.epi.batch_stride = c.d_v;
-    MLA_TRY_CUDA(gemm_simt(c.dtype, gv, s));
+    MLA_TRY(run_gemm(h, gv, (uint32_t *)ws, s));
     return MLA_OK;
 }
 
@@ -438,21 +466,24 @@ mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int6
     if (!align_ok(c, {o, y, w->W_O})) return MLA_ERR_INVALID_ARG;
     const int K = c.n_heads * c.d_v;
     GemmArgs g = linear_args(o, K, w->W_O, K, (int)T, c.d_model, K, y, c.d_model);
-    MLA_TRY_CUDA(gemm_simt(c.dtype, g, (cudaStream_t)stream));
-    return MLA_OK;
+    return run_gemm(h, g, h->status, (cudaStream_t)stream);
 }
 
 mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t *bits)
 {
-    if (!h || !ws) return MLA_ERR_INVALID_ARG;
+    if (!h) return MLA_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    uint32_t v = 0;
-    MLA_TRY_CUDA(cudaMemcpyAsync(&v, ws, sizeof(v), cudaMemcpyDeviceToHost, s));
+    uint32_t v[2] = {0, 0};
+    if (ws) MLA_TRY_CUDA(cudaMemcpyAsync(&v[0], ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
+    MLA_TRY_CUDA(cudaMemcpyAsync(&v[1], h->status, sizeof(uint32_t), cudaMemcpyDeviceToHost, s));
     MLA_TRY_CUDA(cudaStreamSynchronize(s));
-    MLA_TRY_CUDA(cudaMemsetAsync(ws, 0, sizeof(uint32_t), s));
+    if (ws) MLA_TRY_CUDA(cudaMemsetAsync(ws, 0, sizeof(uint32_t), s));
+    MLA_TRY_CUDA(cudaMemsetAsync(h->status, 0, sizeof(uint32_t), s));
     MLA_TRY_CUDA(cudaStreamSynchronize(s));
-    if (bits) *bits = v;
-    return v ? MLA_ERR_DEVICE_DATA : MLA_OK;
+    const uint32_t all = v[0] | v[1];
+    if (bits) *bits = all;
+    if (all & kStatusTimeout) return MLA_ERR_TIMEOUT;
+    return all ? MLA_ERR_DEVICE_DATA : MLA_OK;
 }
 
 uint64_t mla_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }

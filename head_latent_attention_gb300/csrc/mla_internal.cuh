@@ -13,6 +13,7 @@ struct mla_handle {
     int num_sms;
     int rope_dim;        // rotated width: d_rope (decoupled), d_nope (small), 0 (MLRA)
     float2 *rope_table;  // [max_seq, rope_dim / 2] (cos, sin) of pos * base^(-2i/rope_dim)
+    uint32_t *status;    // device status word for calls without a workspace
 };
 
 namespace mla {
@@ -26,6 +27,7 @@ void profile_end(int which, cudaStream_t s);
 constexpr uint32_t kStatusPos = 1u;
 constexpr uint32_t kStatusSeq = 2u;
 constexpr uint32_t kStatusLen = 4u;
+constexpr uint32_t kStatusTimeout = 8u;
 
 // Workspace: the first 256 bytes hold the status word; call scratch follows.
 constexpr size_t kWsHeader = 256;
@@ -62,21 +64,38 @@ struct Epilogue {
     int rope_dim = 0;
     const float2 *rope_table = nullptr;
     const int32_t *rope_pos = nullptr;
-    uint32_t *status = nullptr;
+    uint32_t *status = nullptr;  // device status word (index flags, timeouts)
 };
 
+// Row-major 2-D view of a tensor: rows x cols elements, row stride ld.
+struct Mat2D {
+    const void *ptr = nullptr;
+    int64_t rows = 0, cols = 0, ld = 0;
+};
+
+// C[M, N] = A[M, K] B^T per batch entry z.  Batch entry z reads A from the
+// block at (z * a_row_batch, z * a_col_batch) of the A view and B from
+// (z * b_row_batch, z * b_col_batch) of the B view.  B holds element (n, k)
+// at (row n, col k) (K contiguous, "K-major") unless trans_b, in which case
+// at (row k, col n) (N contiguous, "MN-major").
 struct GemmArgs {
-    const void *A = nullptr;
-    int64_t lda = 0, batch_stride_a = 0;
-    const void *B = nullptr;
-    int64_t ldb = 0, batch_stride_b = 0;
-    bool trans_b = false;  // false: B is [N, K] (K contiguous); true: B is [K, N]
+    Mat2D A;
+    int64_t a_row_batch = 0, a_col_batch = 0;
+    Mat2D B;
+    int64_t b_row_batch = 0, b_col_batch = 0;
+    bool trans_b = false;
     int M = 0, N = 0, K = 0, batch = 1;
     Epilogue epi;
 };
 
-// CUDA-core kernels (every dtype; the float32 path and small shapes).
+// CUDA-core kernels (the float32 path).
 cudaError_t gemm_simt(int dtype, const GemmArgs &a, cudaStream_t s);
+
+// Tensor-core (tcgen05) projection GEMM for bfloat16.  Requirements checked by
+// gemm_tc_supported(): 16-byte aligned views and row strides, N % 32 == 0,
+// batch offsets on 16-byte boundaries, output rows 16-byte aligned.
+bool gemm_tc_supported(const GemmArgs &a);
+cudaError_t gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t s);
 
 struct DecodeArgs {
     int dtype;

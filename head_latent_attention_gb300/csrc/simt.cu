@@ -39,8 +39,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a)
     __shared__ float Bs[kTileK][kTile + 4];
     __shared__ float Cs[kTile][kTile + 1];
     const int z = blockIdx.z;
-    const T *A = (const T *)a.A + (int64_t)z * a.batch_stride_a;
-    const T *Bm = (const T *)a.B + (int64_t)z * a.batch_stride_b;
+    const T *A = (const T *)a.A.ptr + (int64_t)z * (a.a_row_batch * a.A.ld + a.a_col_batch);
+    const T *Bm = (const T *)a.B.ptr + (int64_t)z * (a.b_row_batch * a.B.ld + a.b_col_batch);
     const int m0 = blockIdx.y * kTile, n0 = blockIdx.x * kTile;
     const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
     float acc[4][4] = {};
@@ -48,13 +48,13 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GemmArgs a)
         for (int i = tid; i < kTile * kTileK; i += 256) {
             int r = i / kTileK, c = i % kTileK;
             int m = m0 + r, k = k0 + c;
-            As[c][r] = (m < a.M && k < a.K) ? to_f32(A[(int64_t)m * a.lda + k]) : 0.f;
+            As[c][r] = (m < a.M && k < a.K) ? to_f32(A[(int64_t)m * a.A.ld + k]) : 0.f;
             int n, kk;
             if (kTransB) { n = n0 + i % kTile; kk = k0 + i / kTile; }
             else { n = n0 + r; kk = k; }
             float bv = 0.f;
             if (n < a.N && kk < a.K)
-                bv = kTransB ? to_f32(Bm[(int64_t)kk * a.ldb + n]) : to_f32(Bm[(int64_t)n * a.ldb + kk]);
+                bv = kTransB ? to_f32(Bm[(int64_t)kk * a.B.ld + n]) : to_f32(Bm[(int64_t)n * a.B.ld + kk]);
             if (kTransB) Bs[i / kTile][i % kTile] = bv;
             else Bs[c][r] = bv;
         }

@@ -188,10 +188,12 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope,
 mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int64_t T,
                         void *y, void *stream);
 
-/* Synchronise `stream`, read and clear the workspace status word.  *bits
- * receives the flags (1: position out of range, 2: sequence index out of
- * range, 4: decode length out of range); the return value is MLA_OK when no
- * flag was set, MLA_ERR_DEVICE_DATA otherwise. */
+/* Synchronise `stream`, read and clear the status words of the workspace
+ * (ws may be NULL) and of the handle (used by calls without a workspace).
+ * *bits receives the flags OR-ed together (1: position out of range,
+ * 2: sequence index out of range, 4: decode length out of range, 8: a bounded
+ * device wait timed out and the kernel gave up).  Returns MLA_OK when no flag
+ * was set, MLA_ERR_TIMEOUT when bit 8 was, MLA_ERR_DEVICE_DATA otherwise. */
 mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t *bits);
 
 /* Static English text for a status code. */

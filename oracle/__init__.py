@@ -272,16 +272,26 @@ def out_proj(o, Wts: Dict[str, np.ndarray], n_threads: Optional[int] = None) -> 
 # Whole passes
 # --------------------------------------------------------------------------
 
+def _keep(a):
+    return a
+
+
 def prefill(w, x, Wts: Dict[str, np.ndarray], start_pos: Sequence[int] = None,
             cache_lat=None, cache_rope=None, use_rope: bool = True,
-            n_threads: Optional[int] = None) -> Dict[str, np.ndarray]:
+            n_threads: Optional[int] = None, store=None) -> Dict[str, np.ndarray]:
     """Causal prefill of x [B, S, d_model] appended at start_pos[b].
 
     Projects every token, writes c_KV (and rotated k_R) into the caches at
     (b, start_pos[b] + i), attends each query against keys
     0..start_pos[b] + i, and applies W_O.  Caches default to zeros of length
     max(start_pos) + S.
+
+    ``store``, when given, is applied to every tensor that a staged
+    implementation hands from one stage to the next in its storage type (the
+    cache rows, the projected queries and the attention output), e.g. a
+    rounding to bfloat16; all arithmetic stays in double precision.
     """
+    store = store or _keep
     x = _f64(x)
     B, S, _ = x.shape
     sp = np.zeros(B, np.int32) if start_pos is None else _i32(start_pos)
@@ -294,6 +304,7 @@ def prefill(w, x, Wts: Dict[str, np.ndarray], start_pos: Sequence[int] = None,
                       else _f64(cache_rope).copy())
     pos = (sp[:, None] + np.arange(S, dtype=np.int32)[None, :]).astype(np.int32)
     pr = project(w, x.reshape(B * S, -1), pos.reshape(-1), Wts, use_rope, n_threads)
+    pr = {k: store(v) for k, v in pr.items()}
     q_b = np.repeat(np.arange(B, dtype=np.int32), S)
     for b in range(B):
         cache_lat[b, sp[b]:sp[b] + S] = pr["c_kv"][b * S:(b + 1) * S]
@@ -301,21 +312,24 @@ def prefill(w, x, Wts: Dict[str, np.ndarray], start_pos: Sequence[int] = None,
             cache_rope[b, sp[b]:sp[b] + S] = pr["k_r"][b * S:(b + 1) * S]
     o = attend(w, q_b, pos.reshape(-1), pr, cache_lat, cache_rope, Wts, use_rope,
                n_threads=n_threads)
-    y = out_proj(o, Wts, n_threads)
+    y = out_proj(store(o), Wts, n_threads)
     return {"y": y.reshape(B, S, -1), "o": o.reshape(B, S, w.n_heads, w.d_v),
             "cache_lat": cache_lat, "cache_rope": cache_rope, **pr}
 
 
 def decode(w, x, seq_lens, cache_lat, cache_rope, Wts: Dict[str, np.ndarray],
-           absorbed: bool = False, n_threads: Optional[int] = None) -> Dict[str, np.ndarray]:
+           absorbed: bool = False, n_threads: Optional[int] = None,
+           store=None) -> Dict[str, np.ndarray]:
     """One decode step: the new token x[b] sits at position seq_lens[b] - 1
     (the length includes it); it is projected and appended, then attends keys
-    0..seq_lens[b] - 1, and W_O is applied."""
+    0..seq_lens[b] - 1, and W_O is applied.  ``store`` as in ``prefill``."""
+    store = store or _keep
     x = _f64(x)
     B = x.shape[0]
     sl = _i32(seq_lens)
     pos = (sl - 1).astype(np.int32)
     pr = project(w, x, pos, Wts, True, n_threads)
+    pr = {k: store(v) for k, v in pr.items()}
     cache_lat = _f64(cache_lat).copy()
     if w.variant == VARIANT_DECOUPLED:
         cache_rope = _f64(cache_rope).copy()
@@ -326,5 +340,5 @@ def decode(w, x, seq_lens, cache_lat, cache_rope, Wts: Dict[str, np.ndarray],
     q_b = np.arange(B, dtype=np.int32)
     o = attend(w, q_b, pos, pr, cache_lat, cache_rope, Wts, absorbed=absorbed,
                n_threads=n_threads)
-    y = out_proj(o, Wts, n_threads)
+    y = out_proj(store(o), Wts, n_threads)
     return {"y": y, "o": o, "cache_lat": cache_lat, "cache_rope": cache_rope, **pr}

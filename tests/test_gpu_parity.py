@@ -50,6 +50,12 @@ def subset_heads(w: syn.Workload, Wx, heads):
     return out
 
 
+def boundary(w: syn.Workload):
+    """Rounding of the tensors the C ABI hands between calls (cache rows,
+    projected queries, attention output) to the workload's storage type."""
+    return lambda a: syn.store(a, w.dtype)[1]
+
+
 def make_layer(mla, w, dev_w, max_tokens, max_batch=None, max_seq=None, ws_max_len=None):
     return mla.MlaLayer(config_of(w, max_batch, max_seq), dev_w, max_tokens, ws_max_len=ws_max_len)
 
@@ -85,7 +91,7 @@ def run_prefill_e2e(mla, oracle_mod, w, B, S, start_pos=None):
     st, bits = lay.device_status()
     assert st == 0 and bits == 0
     ref = oracle_mod.prefill(w, xe.reshape(B, S, -1), ex_w, start_pos=sp, cache_lat=cache_lat_e,
-                             cache_rope=cache_rope_e)
+                             cache_rope=cache_rope_e, store=boundary(w))
     dt = w.dtype
     compare(to_f64(qn), ref["q_nope" if w.variant == syn.VARIANT_DECOUPLED else "q"], dt, "q_nope")
     if qr is not None:
@@ -228,7 +234,8 @@ def run_decode_e2e(mla, oracle_mod, w, lens):
     o = lay.decode(qn, qr, torch.tensor(lens, dtype=torch.int32, device="cuda"))
     y = lay.out_proj(o)
     torch.cuda.synchronize()
-    ref = oracle_mod.decode(w, xe, np.asarray(lens, np.int32), lat_e, rope_e, ex_w, absorbed=True)
+    ref = oracle_mod.decode(w, xe, np.asarray(lens, np.int32), lat_e, rope_e, ex_w, absorbed=True,
+                            store=boundary(w))
     compare(to_f64(o), ref["o"], w.dtype, "decode o")
     compare(to_f64(y), ref["y"], w.dtype, "decode y")
 
