@@ -289,7 +289,9 @@ def prefill(w, x, Wts: Dict[str, np.ndarray], start_pos: Sequence[int] = None,
     ``store``, when given, is applied to every tensor that a staged
     implementation hands from one stage to the next in its storage type (the
     cache rows, the projected queries and the attention output), e.g. a
-    rounding to bfloat16; all arithmetic stays in double precision.
+    rounding to bfloat16; all arithmetic stays in double precision.  The
+    returned stage outputs (``c_kv``, ``k_r``, ``q*``, ``o``, ``y``) are the
+    values before that rounding; the returned caches hold the stored values.
     """
     store = store or _keep
     x = _f64(x)
@@ -304,13 +306,13 @@ def prefill(w, x, Wts: Dict[str, np.ndarray], start_pos: Sequence[int] = None,
                       else _f64(cache_rope).copy())
     pos = (sp[:, None] + np.arange(S, dtype=np.int32)[None, :]).astype(np.int32)
     pr = project(w, x.reshape(B * S, -1), pos.reshape(-1), Wts, use_rope, n_threads)
-    pr = {k: store(v) for k, v in pr.items()}
+    st = {k: store(v) for k, v in pr.items()}
     q_b = np.repeat(np.arange(B, dtype=np.int32), S)
     for b in range(B):
-        cache_lat[b, sp[b]:sp[b] + S] = pr["c_kv"][b * S:(b + 1) * S]
+        cache_lat[b, sp[b]:sp[b] + S] = st["c_kv"][b * S:(b + 1) * S]
         if w.variant == VARIANT_DECOUPLED:
-            cache_rope[b, sp[b]:sp[b] + S] = pr["k_r"][b * S:(b + 1) * S]
-    o = attend(w, q_b, pos.reshape(-1), pr, cache_lat, cache_rope, Wts, use_rope,
+            cache_rope[b, sp[b]:sp[b] + S] = st["k_r"][b * S:(b + 1) * S]
+    o = attend(w, q_b, pos.reshape(-1), st, cache_lat, cache_rope, Wts, use_rope,
                n_threads=n_threads)
     y = out_proj(store(o), Wts, n_threads)
     return {"y": y.reshape(B, S, -1), "o": o.reshape(B, S, w.n_heads, w.d_v),
@@ -329,16 +331,16 @@ def decode(w, x, seq_lens, cache_lat, cache_rope, Wts: Dict[str, np.ndarray],
     sl = _i32(seq_lens)
     pos = (sl - 1).astype(np.int32)
     pr = project(w, x, pos, Wts, True, n_threads)
-    pr = {k: store(v) for k, v in pr.items()}
+    st = {k: store(v) for k, v in pr.items()}
     cache_lat = _f64(cache_lat).copy()
     if w.variant == VARIANT_DECOUPLED:
         cache_rope = _f64(cache_rope).copy()
     for b in range(B):
-        cache_lat[b, pos[b]] = pr["c_kv"][b]
+        cache_lat[b, pos[b]] = st["c_kv"][b]
         if w.variant == VARIANT_DECOUPLED:
-            cache_rope[b, pos[b]] = pr["k_r"][b]
+            cache_rope[b, pos[b]] = st["k_r"][b]
     q_b = np.arange(B, dtype=np.int32)
-    o = attend(w, q_b, pos, pr, cache_lat, cache_rope, Wts, absorbed=absorbed,
+    o = attend(w, q_b, pos, st, cache_lat, cache_rope, Wts, absorbed=absorbed,
                n_threads=n_threads)
     y = out_proj(store(o), Wts, n_threads)
     return {"y": y, "o": o, "cache_lat": cache_lat, "cache_rope": cache_rope, **pr}

@@ -52,7 +52,12 @@ def subset_heads(w: syn.Workload, Wx, heads):
 
 def boundary(w: syn.Workload):
     """Rounding of the tensors the C ABI hands between calls (cache rows,
-    projected queries, attention output) to the workload's storage type."""
+    projected queries, attention output) to the workload's storage type.
+    The oracle feeds these stored values to its next stage and compares each
+    GPU stage output with its own value before rounding, so the output's
+    rounding to bfloat16 is counted once (a second, independent rounding of
+    the reference could differ by one unit in the last place, 0.031 at
+    magnitude 4)."""
     return lambda a: syn.store(a, w.dtype)[1]
 
 
@@ -98,9 +103,10 @@ def run_prefill_e2e(mla, oracle_mod, w, B, S, start_pos=None):
         compare(to_f64(qr), ref["q_rope"], dt, "q_rope")
     for b in range(B):
         rows = slice(int(sp[b]), int(sp[b]) + S)
-        compare(to_f64(lay.cache_lat[b, rows]), ref["cache_lat"][b, rows], dt, f"cache_lat b={b}")
+        toks = slice(b * S, (b + 1) * S)
+        compare(to_f64(lay.cache_lat[b, rows]), ref["c_kv"][toks], dt, f"cache_lat b={b}")
         if w.d_rope:
-            compare(to_f64(lay.cache_rope[b, rows]), ref["cache_rope"][b, rows], dt, f"cache_rope b={b}")
+            compare(to_f64(lay.cache_rope[b, rows]), ref["k_r"][toks], dt, f"cache_rope b={b}")
     compare(to_f64(o), ref["o"], dt, "o")
     compare(to_f64(y).reshape(B, S, -1), ref["y"], dt, "y")
 
