@@ -55,7 +55,7 @@ int decode_splits(const mla_config &c) { return (c.max_seq + kDecodeChunk - 1) /
 
 // Workspace regions, each 256-byte aligned, after the status header.
 struct ProjectWs { size_t cq, end; };
-struct DecodeWs { size_t q_abs, o_lat, o_part, ml_part, end; };
+struct DecodeWs { size_t q_abs, o_lat, o_part, ml_part, prefix, end; };
 struct PrefillWs { size_t start_pos, k, v, end; };
 
 ProjectWs project_ws(const mla_config &c, int64_t T)
@@ -67,16 +67,26 @@ ProjectWs project_ws(const mla_config &c, int64_t T)
     return w;
 }
 
-DecodeWs decode_ws(const mla_config &c, int B)
+bool use_tc_decode(const mla_handle *h)
 {
+    const mla_config &c = h->cfg;
+    return c.dtype == MLA_DTYPE_BF16 && c.variant == MLA_VARIANT_DECOUPLED && h->decode_clusters > 0 &&
+           decode_tc_supported(c.n_heads, c.r_kv, c.d_rope);
+}
+
+DecodeWs decode_ws(const mla_handle *h, int B)
+{
+    const mla_config &c = h->cfg;
     DecodeWs w;
     size_t lat = (size_t)B * c.n_heads * r_lat_of(c);
-    size_t parts = (size_t)B * decode_splits(c) * c.n_heads;
+    size_t parts = use_tc_decode(h) ? (size_t)(h->decode_clusters + B) * c.n_heads
+                                    : (size_t)B * decode_splits(c) * c.n_heads;
     w.q_abs = kWsHeader;
     w.o_lat = round_up(w.q_abs + lat * esize(c), 256);
     w.o_part = round_up(w.o_lat + lat * esize(c), 256);
     w.ml_part = round_up(w.o_part + parts * r_lat_of(c) * 4, 256);
-    w.end = round_up(w.ml_part + parts * 2 * 4, 256);
+    w.prefix = round_up(w.ml_part + parts * 2 * 4, 256);
+    w.end = round_up(w.prefix + ((size_t)B + 2) * 4, 256);
     return w;
 }
 
@@ -203,6 +213,10 @@ mla_status mla_create(const mla_config *cfg, mla_handle **out)
         mla_destroy(h);
         return MLA_ERR_CUDA;
     }
+    h->decode_clusters = 0;
+    if (cfg->dtype == MLA_DTYPE_BF16 && cfg->variant == MLA_VARIANT_DECOUPLED &&
+        decode_tc_supported(cfg->n_heads, cfg->r_kv, cfg->d_rope))
+        h->decode_clusters = decode_tc_max_clusters();
     if (h->rope_dim > 0) {
         // cos/sin of pos * base^(-2i/d) (deepseek-mla precompute_freqs_cis,
         // mla_attn _apply_rope), evaluated in double and stored as float.
@@ -239,7 +253,7 @@ size_t mla_workspace_size(const mla_handle *h, int batch, int max_len, int64_t n
     const mla_config &c = h->cfg;
     size_t need = kWsHeader;
     need = std::max(need, project_ws(c, n_tokens).end);
-    if (c.variant != MLA_VARIANT_SMALL) need = std::max(need, decode_ws(c, batch).end);
+    if (c.variant != MLA_VARIANT_SMALL) need = std::max(need, decode_ws(h, batch).end);
     need = std::max(need, prefill_ws(c, batch, max_len).end);
     return need;
 }
@@ -406,7 +420,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
     if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
         return MLA_ERR_INVALID_ARG;
-    DecodeWs L = decode_ws(c, B);
+    DecodeWs L = decode_ws(h, B);
     if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     char *wsb = (char *)ws;
@@ -425,6 +439,27 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     ga.epi.out = q_abs; ga.epi.ldc = (int64_t)H * r_lat; ga.epi.batch_stride = r_lat;
     MLA_TRY(run_gemm(h, ga, (uint32_t *)ws, s));
 
+    const float scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
+    if (use_tc_decode(h)) {
+        DecodeTcArgs t;
+        t.B = B; t.H = H; t.r_kv = c.r_kv; t.d_rope = c.d_rope;
+        t.max_batch = c.max_batch; t.max_seq = c.max_seq; t.n_clusters = h->decode_clusters;
+        t.q_abs = q_abs; t.q_rope = q_rope;
+        t.lat = cache->lat; t.lat_stride = cache->lat_stride;
+        t.rope = cache->rope; t.rope_stride = cache->rope_stride;
+        t.seq_lens = seq_lens;
+        t.prefix = (int *)(wsb + L.prefix);
+        t.chunk = t.prefix + B + 1;
+        t.scale_log2 = scale_log2;
+        t.o_lat = o_lat;
+        t.o_part = (float *)(wsb + L.o_part);
+        t.ml_part = (float *)(wsb + L.ml_part);
+        t.status = (uint32_t *)ws;
+        if (!align_ok(c, {cache->lat, cache->rope}) || (cache->lat_stride * 2) % 16 ||
+            (cache->rope_stride * 2) % 16)
+            return MLA_ERR_INVALID_ARG;
+        MLA_TRY_CUDA(decode_tc(t, s));
+    } else {
     DecodeArgs d;
     d.dtype = c.dtype;
     d.B = B; d.H = H; d.r_lat = r_lat; d.d_rope = dec ? c.d_rope : 0;
@@ -434,7 +469,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     d.rope = dec ? cache->rope : nullptr; d.rope_stride = cache->rope_stride;
     d.max_seq = c.max_seq;
     d.seq_lens = seq_lens;
-    d.scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
+    d.scale_log2 = scale_log2;
     d.o_part = (float *)(wsb + L.o_part);
     d.ml_part = (float *)(wsb + L.ml_part);
     d.n_split = decode_splits(c);
@@ -443,6 +478,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     d.status = (uint32_t *)ws;
     if (d.n_split > 64) return MLA_ERR_UNSUPPORTED;
     MLA_TRY_CUDA(decode_simt(d, s));
+    }
 
     // o[b, h] = W_UV,h o_lat[b, h]: per head h, [B, r_lat] x [r_lat, d_v].
     GemmArgs gv;

@@ -14,6 +14,7 @@ struct mla_handle {
     int rope_dim;        // rotated width: d_rope (decoupled), d_nope (small), 0 (MLRA)
     float2 *rope_table;  // [max_seq, rope_dim / 2] (cos, sin) of pos * base^(-2i/rope_dim)
     uint32_t *status;    // device status word for calls without a workspace
+    int decode_clusters; // co-resident 2-CTA clusters of the tensor-core decode (0: not used)
 };
 
 namespace mla {
@@ -117,6 +118,29 @@ struct DecodeArgs {
     uint32_t *status;
 };
 cudaError_t decode_simt(const DecodeArgs &a, cudaStream_t s);
+
+// Tensor-core split-KV decode (decode_tc.cu): DECOUPLED, bfloat16, H <= 128,
+// r_kv == 512, d_rope == 64.
+struct DecodeTcArgs {
+    int B, H, r_kv, d_rope, max_batch, max_seq, n_clusters;
+    const void *q_abs;        // [B, H, r_kv]
+    const void *q_rope;       // [B, H, d_rope]
+    const void *lat;          // cache latent rows
+    int64_t lat_stride;
+    const void *rope;         // cache rope rows
+    int64_t rope_stride;
+    const int32_t *seq_lens;  // device [B]
+    int *prefix;              // workspace [B + 1]
+    int *chunk;               // workspace [1]
+    float scale_log2;
+    void *o_lat;              // [B, H, r_kv] bf16
+    float *o_part;            // [n_clusters + B, H, r_kv]
+    float *ml_part;           // [n_clusters + B, H, 2]
+    uint32_t *status;
+};
+int decode_tc_max_clusters();
+bool decode_tc_supported(int H, int r_kv, int d_rope);
+cudaError_t decode_tc(const DecodeTcArgs &a, cudaStream_t s);
 
 struct PrefillArgs {
     int dtype;
