@@ -56,7 +56,7 @@ int decode_splits(const mla_config &c) { return (c.max_seq + kDecodeChunk - 1) /
 // Workspace regions, each 256-byte aligned, after the status header.
 struct ProjectWs { size_t cq, end; };
 struct DecodeWs { size_t q_abs, o_lat, o_part, ml_part, prefix, end; };
-struct PrefillWs { size_t start_pos, k, v, end; };
+struct PrefillWs { size_t start_pos, k, v, kr, end; };
 
 ProjectWs project_ws(const mla_config &c, int64_t T)
 {
@@ -97,7 +97,8 @@ PrefillWs prefill_ws(const mla_config &c, int B, int64_t kv_rows)
     w.start_pos = kWsHeader;
     w.k = round_up(w.start_pos + (size_t)B * 4, 256);
     w.v = round_up(w.k + rows * c.d_nope * esize(c), 256);
-    w.end = round_up(w.v + rows * c.d_v * esize(c), 256);
+    w.kr = round_up(w.v + rows * c.d_v * esize(c), 256);
+    w.end = round_up(w.kr + (size_t)B * kv_rows * c.d_rope * 2, 256);
     return w;
 }
 
@@ -361,6 +362,7 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
     // Keys and values of every cached row in use (deepseek-mla forward:
     // UK_proj / UV_proj of the cached latent; mla_attn: k is then rotated;
     // mlra_attn: block-wise up-projections concatenated per head).
+    const bool tc = c.dtype == MLA_DTYPE_BF16 && prefill_tc_supported(c.d_nope, dec ? c.d_rope : 0, c.d_v);
     int nblk = c.variant == MLA_VARIANT_MLRA ? c.n_latent_heads : 1;
     int sub_rank = c.r_kv / nblk, sub_k = H * c.d_nope / nblk, sub_v = H * c.d_v / nblk;
     for (int blk = 0; blk < nblk; ++blk) {
@@ -374,6 +376,7 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
         gk.epi.out = (char *)kbuf + (size_t)blk * sub_k * esize(c);
         gk.epi.ldc = ldk;
         gk.epi.batch_stride = kv_rows * ldk;
+        gk.epi.out_f16 = tc;
         if (c.variant == MLA_VARIANT_SMALL) {
             gk.epi.rope_mode = kRopeHalf; gk.epi.rope_dim = c.d_nope;
             gk.epi.rope_table = h->rope_table; gk.epi.max_seq = c.max_seq;
@@ -387,7 +390,27 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
         gv.epi.out = (char *)vbuf + (size_t)blk * sub_v * esize(c);
         gv.epi.ldc = ldv;
         gv.epi.batch_stride = kv_rows * ldv;
+        gv.epi.out_f16 = tc;
         MLA_TRY(run_gemm(h, gv, (uint32_t *)ws, s));
+    }
+    const float scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
+    if (tc) {
+        if ((cache->rope_stride * 2) % 16 && dec) return MLA_ERR_INVALID_ARG;
+        PrefillTcArgs t;
+        t.B = B; t.S = S; t.H = H;
+        t.d_nope = c.d_nope; t.d_rope = dec ? c.d_rope : 0; t.d_v = c.d_v;
+        t.max_batch = c.max_batch; t.max_seq = c.max_seq;
+        t.kv_rows = kv_rows;
+        t.q_nope = q_nope; t.q_rope = dec ? q_rope : nullptr;
+        t.k = kbuf; t.v = vbuf;
+        t.rope = dec ? cache->rope : nullptr; t.rope_stride = cache->rope_stride;
+        t.k_rope16 = wsb + L.kr;
+        t.start_pos = d_sp;
+        t.scale_log2 = scale_log2;
+        t.o = o;
+        t.status = (uint32_t *)ws;
+        MLA_TRY_CUDA(prefill_tc(t, s));
+        return MLA_OK;
     }
     PrefillArgs p;
     p.dtype = c.dtype;
@@ -398,7 +421,7 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
     p.rope = dec ? cache->rope : nullptr; p.rope_stride = cache->rope_stride;
     p.max_seq = c.max_seq;
     p.start_pos = d_sp;
-    p.scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
+    p.scale_log2 = scale_log2;
     p.o = o;
     MLA_TRY_CUDA(prefill_simt(p, s));
     return MLA_OK;

@@ -162,6 +162,37 @@ struct SegIter {
     }
 };
 
+// Walks the tiles of this cluster's segments in order (g: global tile
+// index, t: tile within segment nseg).
+struct TileCursor {
+    SegIter it;
+    int b, k0, k1, nseg, t, ntiles, g;
+    bool whole, valid;
+    __device__ void init(const int *pf, int nb, int cid, int chunk)
+    {
+        it.init(pf, nb, cid, chunk);
+        nseg = -1;
+        g = 0;
+        valid = true;
+        next_segment();
+    }
+    __device__ void next_segment()
+    {
+        if (it.next(b, k0, k1, whole)) {
+            ++nseg;
+            t = 0;
+            ntiles = (k1 - k0 + kBKV - 1) / kBKV;
+        } else {
+            valid = false;
+        }
+    }
+    __device__ void step()
+    {
+        ++g;
+        if (++t == ntiles) next_segment();
+    }
+};
+
 template <int LA>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQR,
@@ -261,68 +292,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (ptx::elect_one()) {
+            // Non-blocking issue: poll both queues and issue whichever MMA
+            // group is ready, P.V first (it frees a KV stage for the next
+            // load); a QK^T waiting on its tile never holds back a P.V.
             constexpr uint32_t idesc_s = ptx::idesc_bf16(kH, kBKV, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, LA * 64, false, true);
             const uint32_t q0 = ptx::smem_u32(sQ), kv0 = ptx::smem_u32(sKV), p0 = ptx::smem_u32(sP);
-            SegIter it;
-            it.init(p.prefix, p.B, cid, chunk);
-            int b, k0, k1;
-            bool whole;
-            int nseg = 0, g = 0, s_cnt = 0, pv_cnt = 0;
-            bool have_pv = false;
-            int pv_stage = 0, pv_seg = 0;
-            bool pv_first = false;
-            auto issue_pv = [&]() -> bool {
-                if (pv_first && pv_seg > 0 && !ptx::mbar_wait(&bar->o_empty, (pv_seg - 1) & 1, abort_flag))
-                    return false;
-                if (!ptx::mbar_wait(&bar->p_full, pv_cnt & 1, abort_flag)) return false;
-                ptx::tc_fence_after();
-                const uint32_t vb = kv0 + pv_stage * C::kStageBytes;
+            TileCursor qk, pv;
+            qk.init(p.prefix, p.B, cid, chunk);
+            pv.init(p.prefix, p.B, cid, chunk);
+            long long last = clock64();
+            while (ok && pv.valid) {
+                bool progressed = false;
+                if (pv.g < qk.g) {
+                    bool ready = ptx::mbar_try_wait(ptx::smem_u32(&bar->p_full), pv.g & 1);
+                    if (ready && pv.t == 0 && pv.nseg > 0)
+                        ready = ptx::mbar_try_wait(ptx::smem_u32(&bar->o_empty), (pv.nseg - 1) & 1);
+                    if (ready) {
+                        ptx::tc_fence_after();
+                        const int st = pv.g & 1;
+                        const uint32_t vb = kv0 + st * C::kStageBytes;
 #pragma unroll
-                for (int k = 0; k < kBKV / 16; ++k)
-                    ptx::mma_bf16(tmem, ptx::sdesc_sw128(p0 + k * 32, 16, 1024),
-                                  ptx::sdesc_sw128(vb + k * 2048, C::kAtomBytes, 1024), idesc_o,
-                                  (pv_first && k == 0) ? 0u : 1u);
-                ptx::mma_commit(&bar->kv_empty[pv_stage]);
-                ptx::mma_commit(&bar->pv_done);
-                ++pv_cnt;
-                have_pv = false;
-                return true;
-            };
-            while (ok && it.next(b, k0, k1, whole)) {
-                if (!ptx::mbar_wait(&bar->q_full, nseg & 1, abort_flag)) { fail(); break; }
-                const int ntiles = (k1 - k0 + kBKV - 1) / kBKV;
-                for (int t = 0; t < ntiles; ++t, ++g) {
-                    if (t == 0 && have_pv && !issue_pv()) { fail(); break; }
-                    const int st = g & 1, sb = s_cnt & 1;
-                    if (!ptx::mbar_wait(&bar->kv_full[st], (g >> 1) & 1, abort_flag) ||
-                        !ptx::mbar_wait(&bar->s_empty[sb], ((s_cnt >> 1) & 1) ^ 1, abort_flag)) {
-                        fail();
-                        break;
+                        for (int k = 0; k < kBKV / 16; ++k)
+                            ptx::mma_bf16(tmem, ptx::sdesc_sw128(p0 + k * 32, 16, 1024),
+                                          ptx::sdesc_sw128(vb + k * 2048, C::kAtomBytes, 1024), idesc_o,
+                                          (pv.t == 0 && k == 0) ? 0u : 1u);
+                        ptx::mma_commit(&bar->kv_empty[st]);
+                        ptx::mma_commit(&bar->pv_done);
+                        pv.step();
+                        progressed = true;
                     }
-                    ptx::tc_fence_after();
-                    const uint32_t kb = kv0 + st * C::kStageBytes;
-                    const uint32_t d = tmem + C::kSCol + sb * kBKV;
-                    for (int a = 0; a < nq_atoms; ++a) {
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            ptx::mma_bf16(d, ptx::sdesc_sw128(q0 + a * kH * 128 + k * 32, 16, 1024),
-                                          ptx::sdesc_sw128(kb + a * C::kAtomBytes + k * 32, 16, 1024), idesc_s,
-                                          (a | k) != 0);
-                    }
-                    ptx::mma_commit(&bar->s_full[sb]);
-                    ++s_cnt;
-                    if (t == ntiles - 1) ptx::mma_commit(&bar->q_empty);
-                    if (have_pv && !issue_pv()) { fail(); break; }
-                    have_pv = true;
-                    pv_stage = st;
-                    pv_first = (t == 0);
-                    pv_seg = nseg;
                 }
-                if (!ok) break;
-                ++nseg;
+                if (qk.valid) {
+                    const int st = qk.g & 1;
+                    bool ready = qk.t > 0 || ptx::mbar_try_wait(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
+                    ready = ready && ptx::mbar_try_wait(ptx::smem_u32(&bar->kv_full[st]), (qk.g >> 1) & 1) &&
+                            ptx::mbar_try_wait(ptx::smem_u32(&bar->s_empty[st]), ((qk.g >> 1) & 1) ^ 1);
+                    if (ready) {
+                        ptx::tc_fence_after();
+                        const uint32_t kb = kv0 + st * C::kStageBytes;
+                        const uint32_t d = tmem + C::kSCol + st * kBKV;
+                        for (int a = 0; a < nq_atoms; ++a) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                ptx::mma_bf16(d, ptx::sdesc_sw128(q0 + a * kH * 128 + k * 32, 16, 1024),
+                                              ptx::sdesc_sw128(kb + a * C::kAtomBytes + k * 32, 16, 1024),
+                                              idesc_s, (a | k) != 0);
+                        }
+                        ptx::mma_commit(&bar->s_full[st]);
+                        if (qk.t == qk.ntiles - 1) ptx::mma_commit(&bar->q_empty);
+                        qk.step();
+                        progressed = true;
+                    }
+                }
+                if (progressed) last = clock64();
+                else if (*abort_flag || clock64() - last > ptx::kWaitCycles) fail();
             }
-            if (ok && have_pv && !issue_pv()) fail();
         }
     } else {
         const int quad = warp % 4;

@@ -90,25 +90,29 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams &p, int z, int m,
                 }
         }
     }
-    bf16 *dst;
+    uint16_t *dst;
     if (e.row_seq) {
         const int sq = e.row_seq[m], ps = e.row_pos[m];
         if (sq < 0 || sq >= e.max_batch || ps < 0 || ps >= e.max_seq) {
             if (n0 == 0 && e.status) atomicOr(e.status, (sq < 0 || sq >= e.max_batch) ? kStatusSeq : kStatusPos);
             return;
         }
-        dst = (bf16 *)e.out + ((int64_t)sq * e.seq_rows + ps) * e.ldc + n0;
+        dst = (uint16_t *)e.out + ((int64_t)sq * e.seq_rows + ps) * e.ldc + n0;
     } else {
-        dst = (bf16 *)e.out + (int64_t)z * e.batch_stride + (int64_t)m * e.ldc + n0;
+        dst = (uint16_t *)e.out + (int64_t)z * e.batch_stride + (int64_t)m * e.ldc + n0;
     }
+    if (e.out_f16) {
 #pragma unroll
-    for (int i = 0; i < NC; i += 8) {
-        uint4 w;
-        w.x = ptx::pack_bf16(v[i], v[i + 1]);
-        w.y = ptx::pack_bf16(v[i + 2], v[i + 3]);
-        w.z = ptx::pack_bf16(v[i + 4], v[i + 5]);
-        w.w = ptx::pack_bf16(v[i + 6], v[i + 7]);
-        *reinterpret_cast<uint4 *>(dst + i) = w;
+        for (int i = 0; i < NC; i += 8)
+            *reinterpret_cast<uint4 *>(dst + i) =
+                make_uint4(ptx::pack_f16(v[i], v[i + 1]), ptx::pack_f16(v[i + 2], v[i + 3]),
+                           ptx::pack_f16(v[i + 4], v[i + 5]), ptx::pack_f16(v[i + 6], v[i + 7]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < NC; i += 8)
+            *reinterpret_cast<uint4 *>(dst + i) =
+                make_uint4(ptx::pack_bf16(v[i], v[i + 1]), ptx::pack_bf16(v[i + 2], v[i + 3]),
+                           ptx::pack_bf16(v[i + 4], v[i + 5]), ptx::pack_bf16(v[i + 6], v[i + 7]));
     }
 }
 

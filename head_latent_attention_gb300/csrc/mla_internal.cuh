@@ -66,6 +66,7 @@ struct Epilogue {
     const float2 *rope_table = nullptr;
     const int32_t *rope_pos = nullptr;
     uint32_t *status = nullptr;  // device status word (index flags, timeouts)
+    bool out_f16 = false;        // tensor-core path: store fp16 instead of bfloat16
 };
 
 // Row-major 2-D view of a tensor: rows x cols elements, row stride ld.
@@ -141,6 +142,24 @@ struct DecodeTcArgs {
 int decode_tc_max_clusters();
 bool decode_tc_supported(int H, int r_kv, int d_rope);
 cudaError_t decode_tc(const DecodeTcArgs &a, cudaStream_t s);
+
+// Tensor-core causal prefill (prefill_tc.cu): bfloat16, (d_nope, d_rope, d_v)
+// in {(128, 64, 128), (64, 0, 64), (128, 0, 128)}.
+struct PrefillTcArgs {
+    int B, S, H, d_nope, d_rope, d_v, max_batch, max_seq;
+    int64_t kv_rows;
+    const void *q_nope, *q_rope;  // [B*S, H*d_nope], [B*S, H*d_rope]
+    const void *k, *v;            // fp16 workspace [B*kv_rows, H*d_nope], [B*kv_rows, H*d_v]
+    const void *rope;             // rope cache rows (decoupled, bfloat16)
+    int64_t rope_stride;
+    void *k_rope16;               // fp16 workspace copy of the rope keys [B*kv_rows, 64]
+    const int32_t *start_pos;     // device [B]
+    float scale_log2;
+    void *o;                      // [B, S, H, d_v]
+    uint32_t *status;
+};
+bool prefill_tc_supported(int d_nope, int d_rope, int d_v);
+cudaError_t prefill_tc(const PrefillTcArgs &a, cudaStream_t s);
 
 struct PrefillArgs {
     int dtype;

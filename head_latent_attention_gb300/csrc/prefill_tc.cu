@@ -1,0 +1,392 @@
+// Causal flash-style prefill attention on tcgen05 (fp16 operands, fp32 softmax).
+//
+// One CTA per (128-query tile, head, sequence); tiles with more keys launch
+// first.  Per 64-key tile:
+//   S = Q K^T        tcgen05.mma M=128 (queries), N=64 (keys), K=d_qk, into
+//                    one of two tensor-memory score buffers;
+//   softmax          4 warps, one query row per thread: scale, causal mask
+//                    (key j <= query position), online max with a lazy
+//                    rescale (only when the max grows by more than 8 in log2
+//                    units), exp2, fp16 P into a 128-byte-swizzled tile;
+//   O += P V         tcgen05.mma M=128, N=d_v, K=64 with V read as an
+//                    MN-major operand straight from its TMA tile.
+// Warp 0 streams K and V tiles with TMA into a 3-stage ring, warp 1 issues
+// the MMAs (the next tile's QK^T overlaps the current softmax).  For the
+// decoupled variant the key is [k_C ‖ k_R (shared by all heads)] and the
+// query [q_nope ‖ q_rope].
+// Both contractions run in fp16 (same tensor-core rate as bfloat16, 8x finer
+// rounding): K and V come from an fp16 workspace, the bfloat16 query tile is
+// converted to fp16 in shared memory after its load (exact for |q| in fp16's
+// normal range), and P is stored as fp16 (values in [0, 256]).
+#include "mla_internal.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                    int box_rows);
+
+namespace {
+
+constexpr int kQ = 128;
+constexpr int kBN = 64;
+constexpr int kStages = 3;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.f;
+
+template <int NQ, int NV>  // 64-column atoms of q/k (NQ) and of v (NV)
+struct PCfg {
+    static constexpr int kQBytes = NQ * kQ * 128;
+    static constexpr int kAtom = kBN * 128;
+    static constexpr int kStageBytes = (NQ + NV) * kAtom;
+    static constexpr int kPBytes = kQ * 128;
+    static constexpr int kOffKV = kQBytes;
+    static constexpr int kOffP = kOffKV + kStages * kStageBytes;
+    static constexpr int kOffBar = kOffP + kPBytes;
+    static constexpr int kSmem = kOffBar + 256 + 1024;
+    static constexpr int kOCols = NV * 64;
+    static constexpr int kSCol = 128;
+    static constexpr int kTmem = 256;
+};
+
+struct PreTcParams {
+    int B, S, H, max_seq, d_nope;
+    int64_t kv_rows;
+    bool rope;                 // decoupled: last q/k atom from q_rope / rope cache
+    const int32_t *start_pos;  // device [B]
+    float scale_log2;
+    bf16 *o;                   // [B, S, H, d_v]
+    int d_v;
+    uint32_t *status;
+};
+
+struct PBars {
+    uint64_t q_full, q_ready;
+    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t s_full[2], s_empty[2];
+    uint64_t p_full, pv_done;
+    int abort;
+    uint32_t tmem;
+};
+
+template <int NQ, int NV>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tQ, const __grid_constant__ CUtensorMap tQR,
+                      const __grid_constant__ CUtensorMap tK, const __grid_constant__ CUtensorMap tKR,
+                      const __grid_constant__ CUtensorMap tV, PreTcParams p)
+{
+    using C = PCfg<NQ, NV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sQ = smem;
+    uint8_t *sKV = smem + C::kOffKV;
+    uint8_t *sP = smem + C::kOffP;
+    PBars *bar = (PBars *)(smem + C::kOffBar);
+    volatile int *abort_flag = &bar->abort;
+
+    const int n_qt = (p.S + kQ - 1) / kQ;
+    const int qt = n_qt - 1 - (int)blockIdx.x;  // longest tiles first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * kQ;
+    const int nq = min(kQ, p.S - q0);
+    const int sp = p.start_pos[b];
+    const int last_key = sp + q0 + nq - 1;  // keys 0..last_key are visible to some row
+    const int n_kt = last_key / kBN + 1;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int nk_nope = p.rope ? NQ - 1 : NQ;  // q/k atoms from q_nope / the key workspace
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar->q_full, 1);
+        ptx::mbar_init(&bar->q_ready, kQ);
+        for (int i = 0; i < kStages; ++i) {
+            ptx::mbar_init(&bar->kv_full[i], 1);
+            ptx::mbar_init(&bar->kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&bar->s_full[i], 1);
+            ptx::mbar_init(&bar->s_empty[i], kQ);
+        }
+        ptx::mbar_init(&bar->p_full, kQ);
+        ptx::mbar_init(&bar->pv_done, 1);
+        bar->abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) ptx::tmem_alloc(&bar->tmem, C::kTmem);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bar->tmem;
+    bool ok = true;
+
+    if (warp == 0) {
+        if (ptx::elect_one()) {
+            ptx::prefetch_tmap(&tQ);
+            ptx::prefetch_tmap(&tK);
+            ptx::prefetch_tmap(&tV);
+            if (p.rope) {
+                ptx::prefetch_tmap(&tQR);
+                ptx::prefetch_tmap(&tKR);
+            }
+            const int qrow = b * p.S + q0;
+            ptx::mbar_expect_tx(&bar->q_full, NQ * kQ * 128);
+            for (int a = 0; a < nk_nope; ++a)
+                ptx::tma_load_2d(sQ + a * kQ * 128, &tQ, &bar->q_full, h * p.d_nope + a * 64, qrow);
+            if (p.rope) ptx::tma_load_2d(sQ + (NQ - 1) * kQ * 128, &tQR, &bar->q_full, h * 64, qrow);
+            int pending[kStages] = {-1, -1, -1};
+            for (int t = 0; t < n_kt; ++t) {
+                const int st = t % kStages;
+                const uint32_t ph = (t / kStages) & 1;
+                if (!ptx::mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
+                ptx::mbar_expect_tx(&bar->kv_full[st], C::kStageBytes);
+                uint8_t *dst = sKV + st * C::kStageBytes;
+                const int krow = (int)(b * p.kv_rows) + t * kBN;
+                for (int a = 0; a < nk_nope; ++a)
+                    ptx::tma_load_2d(dst + a * C::kAtom, &tK, &bar->kv_full[st], h * p.d_nope + a * 64, krow);
+                if (p.rope) ptx::tma_load_2d(dst + (NQ - 1) * C::kAtom, &tKR, &bar->kv_full[st], 0, krow);
+                for (int a = 0; a < NV; ++a)
+                    ptx::tma_load_2d(dst + (NQ + a) * C::kAtom, &tV, &bar->kv_full[st], h * p.d_v + a * 64, krow);
+                pending[st] = (int)ph;
+            }
+            if (!ok) *abort_flag = 1;
+            volatile int never = 0;
+            ptx::mbar_wait(&bar->q_full, 0, &never);
+            for (int i = 0; i < kStages; ++i)
+                if (pending[i] >= 0) ptx::mbar_wait(&bar->kv_full[i], (uint32_t)pending[i], &never);
+        }
+    } else if (warp == 1) {
+        if (ptx::elect_one()) {
+            constexpr uint32_t idesc_s = ptx::idesc_f16(kQ, kBN, false, false);
+            constexpr uint32_t idesc_o = ptx::idesc_f16(kQ, NV * 64, false, true);
+            const uint32_t q0a = ptx::smem_u32(sQ), kv0 = ptx::smem_u32(sKV), p0 = ptx::smem_u32(sP);
+            if (!ptx::mbar_wait(&bar->q_ready, 0, abort_flag)) ok = false;
+            for (int t = 0; ok && t <= n_kt; ++t) {
+                if (t < n_kt) {
+                    const int st = t % kStages, sb = t & 1;
+                    if (!ptx::mbar_wait(&bar->kv_full[st], (t / kStages) & 1, abort_flag) ||
+                        !ptx::mbar_wait(&bar->s_empty[sb], ((t >> 1) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t kb = kv0 + st * C::kStageBytes;
+                    for (int a = 0; a < NQ; ++a) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            ptx::mma_bf16(tmem + C::kSCol + sb * kBN,
+                                          ptx::sdesc_sw128(q0a + a * kQ * 128 + k * 32, 16, 1024),
+                                          ptx::sdesc_sw128(kb + a * C::kAtom + k * 32, 16, 1024), idesc_s,
+                                          (a | k) != 0);
+                    }
+                    ptx::mma_commit(&bar->s_full[sb]);
+                }
+                if (t > 0) {
+                    const int pt = t - 1, st = pt % kStages;
+                    if (!ptx::mbar_wait(&bar->p_full, pt & 1, abort_flag)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    const uint32_t vb = kv0 + st * C::kStageBytes + NQ * C::kAtom;
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; ++k)
+                        ptx::mma_bf16(tmem, ptx::sdesc_sw128(p0 + k * 32, 16, 1024),
+                                      ptx::sdesc_sw128(vb + k * 2048, C::kAtom, 1024), idesc_o,
+                                      (pt > 0 || k > 0) ? 1u : 0u);
+                    ptx::mma_commit(&bar->kv_empty[st]);
+                    ptx::mma_commit(&bar->pv_done);
+                }
+            }
+            if (!ok) *abort_flag = 1;
+        }
+    } else {
+        const int quad = warp % 4;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const int my_pos = sp + q0 + r;
+        uint8_t *prow = sP + r * 128;
+        float m_run = -INFINITY, l_run = 0.f;
+        // Query tile: bfloat16 -> fp16 in place (row r of every atom).
+        if (!ptx::mbar_wait(&bar->q_full, 0, abort_flag)) ok = false;
+        if (ok) {
+            for (int a = 0; a < NQ; ++a) {
+                uint4 *row = reinterpret_cast<uint4 *>(sQ + a * kQ * 128 + r * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 w = row[j];
+                    w.x = ptx::bf16x2_to_f16x2(w.x);
+                    w.y = ptx::bf16x2_to_f16x2(w.y);
+                    w.z = ptx::bf16x2_to_f16x2(w.z);
+                    w.w = ptx::bf16x2_to_f16x2(w.w);
+                    row[j] = w;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::mbar_arrive(&bar->q_ready);
+        }
+        for (int t = 0; ok && t < n_kt; ++t) {
+            const int sb = t & 1;
+            if (!ptx::mbar_wait(&bar->s_full[sb], (t >> 1) & 1, abort_flag)) { ok = false; break; }
+            ptx::tc_fence_after();
+            uint32_t r0[32], r1[32];
+            ptx::tmem_ld32(tmem + lane_off + C::kSCol + sb * kBN, r0);
+            ptx::tmem_ld32(tmem + lane_off + C::kSCol + sb * kBN + 32, r1);
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar->s_empty[sb]);
+            const int j0 = t * kBN;
+            const int lim = my_pos - j0;  // keys j0 + j with j <= lim are visible
+            float s[64];
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                s[j] = (j <= lim) ? __uint_as_float(r0[j]) * p.scale_log2 : -INFINITY;
+                s[32 + j] = (32 + j <= lim) ? __uint_as_float(r1[j]) * p.scale_log2 : -INFINITY;
+            }
+#pragma unroll
+            for (int j = 0; j < 64; ++j) mt = fmaxf(mt, s[j]);
+            const bool resc = mt > m_run + kRescaleThreshold;
+            const float m_new = resc ? mt : m_run;
+            // Rows past the sequence end (r >= nq) see no key in later tiles;
+            // keep their state finite.
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_use);
+            float psum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float a0 = exp2f(s[2 * j] - m_use), a1 = exp2f(s[2 * j + 1] - m_use);
+                psum += a0 + a1;
+                pk[j] = ptx::pack_f16(a0, a1);
+            }
+            l_run = l_run * corr + psum;
+            m_run = m_new;
+            if (t > 0 && !ptx::mbar_wait(&bar->pv_done, (t - 1) & 1, abort_flag)) { ok = false; break; }
+            if (resc && t > 0 && corr != 1.f) {
+                ptx::tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < C::kOCols; c += 32) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tmem + lane_off + c, o);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
+                    ptx::tmem_st32(tmem + lane_off + c, o);
+                }
+                ptx::tmem_st_wait();
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(prow + ((j ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar->p_full);
+        }
+        if (ok && ptx::mbar_wait(&bar->pv_done, (n_kt - 1) & 1, abort_flag)) {
+            ptx::tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+            for (int c = 0; c < C::kOCols; c += 32) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tmem + lane_off + c, o);
+                ptx::tmem_ld_wait();
+                if (r < nq) {
+                    bf16 *dst = p.o + (((int64_t)b * p.S + q0 + r) * p.H + h) * p.d_v + c;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 w;
+                        w.x = ptx::pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+                        w.y = ptx::pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+                        w.z = ptx::pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
+                        w.w = ptx::pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
+                        *reinterpret_cast<uint4 *>(dst + j) = w;
+                    }
+                }
+            }
+        } else {
+            ok = false;
+        }
+        if (!ok) *abort_flag = 1;
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::kTmem);
+    }
+    if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, kStatusTimeout);
+}
+
+// fp16 copy of the rope keys of rows [0, kv_rows) of every sequence.
+__global__ void __launch_bounds__(256) rope_to_f16_kernel(const uint16_t *rope, int64_t stride, int max_seq,
+                                                          int64_t kv_rows, int B, uint16_t *out)
+{
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // one 8-element chunk
+    const int64_t total = (int64_t)B * kv_rows * 8;
+    if (i >= total) return;
+    const int64_t row = i / 8, ch = i % 8;
+    const int64_t b = row / kv_rows, j = row % kv_rows;
+    const uint4 w = *reinterpret_cast<const uint4 *>(rope + (b * max_seq + j) * stride + ch * 8);
+    *reinterpret_cast<uint4 *>(out + row * 64 + ch * 8) =
+        make_uint4(ptx::bf16x2_to_f16x2(w.x), ptx::bf16x2_to_f16x2(w.y), ptx::bf16x2_to_f16x2(w.z),
+                   ptx::bf16x2_to_f16x2(w.w));
+}
+
+template <int NQ, int NV>
+cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
+{
+    using C = PCfg<NQ, NV>;
+    CUtensorMap tq, tqr, tk, tkr, tv;
+    const int64_t T = (int64_t)a.B * a.S;
+    const int64_t KR = (int64_t)a.B * a.kv_rows;
+    if (!make_tmap_bf16(&tq, a.q_nope, T, (int64_t)a.H * a.d_nope, (int64_t)a.H * a.d_nope, 64, kQ) ||
+        !make_tmap_bf16(&tk, a.k, KR, (int64_t)a.H * a.d_nope, (int64_t)a.H * a.d_nope, 64, kBN) ||
+        !make_tmap_bf16(&tv, a.v, KR, (int64_t)a.H * a.d_v, (int64_t)a.H * a.d_v, 64, kBN))
+        return cudaErrorInvalidValue;
+    if (a.d_rope) {
+        if (!make_tmap_bf16(&tqr, a.q_rope, T, (int64_t)a.H * 64, (int64_t)a.H * 64, 64, kQ) ||
+            !make_tmap_bf16(&tkr, a.k_rope16, KR, 64, 64, 64, kBN))
+            return cudaErrorInvalidValue;
+        rope_to_f16_kernel<<<dim3((unsigned)((KR * 64 / 8 + 255) / 256)), 256, 0, s>>>(
+            (const uint16_t *)a.rope, a.rope_stride, a.max_seq, a.kv_rows, a.B, (uint16_t *)a.k_rope16);
+        note_launch();
+    } else {
+        tqr = tq;
+        tkr = tk;
+    }
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<NQ, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmem);
+    if (e != cudaSuccess) return e;
+    PreTcParams p;
+    p.B = a.B; p.S = a.S; p.H = a.H; p.max_seq = a.max_seq; p.d_nope = a.d_nope;
+    p.kv_rows = a.kv_rows;
+    p.rope = a.d_rope != 0;
+    p.start_pos = a.start_pos;
+    p.scale_log2 = a.scale_log2;
+    p.o = (bf16 *)a.o;
+    p.d_v = a.d_v;
+    p.status = a.status;
+    dim3 grid((a.S + kQ - 1) / kQ, a.H, a.B);
+    profile_begin(MLA_PROFILE_PREFILL_ATTENTION, s);
+    prefill_tc_kernel<NQ, NV><<<grid, kThreads, C::kSmem, s>>>(tq, tqr, tk, tkr, tv, p);
+    profile_end(MLA_PROFILE_PREFILL_ATTENTION, s);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int d_nope, int d_rope, int d_v)
+{
+    return (d_nope == 128 && d_rope == 64 && d_v == 128) || (d_nope == 64 && d_rope == 0 && d_v == 64) ||
+           (d_nope == 128 && d_rope == 0 && d_v == 128);
+}
+
+cudaError_t prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
+{
+    if (a.B == 0 || a.S == 0) return cudaSuccess;
+    if (a.d_nope == 128 && a.d_rope == 64 && a.d_v == 128) return launch_prefill_tc<3, 2>(a, s);
+    if (a.d_nope == 64 && a.d_rope == 0 && a.d_v == 64) return launch_prefill_tc<1, 1>(a, s);
+    if (a.d_nope == 128 && a.d_rope == 0 && a.d_v == 128) return launch_prefill_tc<2, 2>(a, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace mla
