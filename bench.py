@@ -305,7 +305,7 @@ def run_prefill(args, lay_device):
     import torch
     import head_latent_attention_gb300 as mla
     hbm_peak, tf_peak, tf_sust, peak_src = peaks()
-    w = PREFILL
+    w = PREFILL if not args.prefill_batch else PREFILL.replace(batch=args.prefill_batch)
     B, S = w.batch, w.seq
     lay = build_layer(w, lay_device, B, S, B * S, S)
     xs, _ = syn.activations(w, B * S)
@@ -431,6 +431,10 @@ def main():
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill layer (profiling aid)")
+    ap.add_argument("--prefill-batch", type=int, default=0,
+                    help="sequences in the prefill workload (default 4)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -449,6 +453,13 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device(device))
+    if args.prefill_only:
+        from head_latent_attention_gb300 import _build
+        _build.build()
+        out = run_prefill(args, device)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        return
     out = run_ours(args, rank, world, device)
     if rank == 0:
         print(json.dumps(out), flush=True)

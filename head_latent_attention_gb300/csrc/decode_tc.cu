@@ -5,27 +5,31 @@
 // 512) and rope keys k_R,j (d_rope = 64): s_hj = q_abs,h . c_j + q_R,h . k_R,j,
 // softmax over j, o_lat,h = sum_j p_hj c_j.  The fp32 accumulator o_lat for
 // 128 heads x 512 latent columns is exactly one SM's tensor memory, so a
-// cluster of two CTAs splits the latent: CTA r owns columns [256 r, 256 r +
-// 256) (CTA 0 also the rope columns).  Each CTA
-//   - streams only its own columns of each 64-key tile (TMA, 128-byte swizzle);
+// cluster of two CTAs splits the columns: CTA r owns latent columns
+// [256 r, 256 r + 256) and rope columns [32 r, 32 r + 32).  Each CTA
+//   - streams only its own columns of each 64-key tile (TMA; 128-byte swizzle
+//     for the latent, 64-byte swizzle for the 32 rope columns);
 //   - computes a partial score tile S_r = Q_r K_r^T (M = 128 heads, N = 64
-//     keys) into tensor memory;
-//   - sends S_r to its peer through distributed shared memory and adds the
-//     peer's partial, so both CTAs hold the same fp32 scores and take the
-//     same online-softmax decisions;
-//   - accumulates O_r += P V_r (M = 128, N = 256, K = 64 keys) with the same
-//     shared-memory tile read as an MN-major operand.
-// Warp roles per CTA: warp 0 TMA producer, warp 1 MMA issuer, warps 2..5
-// softmax (one head row per thread).  The running max is only raised when
-// it grows by more than 8 (log2 units), so the O rescale is rare; the final
-// result is exact either way because the same stale max is used for P and
-// for the running sum.
+//     keys, K = 288) into tensor memory;
+//   - sends S_r to the peer with st.async, each store completing bytes on the
+//     peer's mbarrier (no per-thread fences), and adds the peer's partial in
+//     the same order on both sides, so both CTAs take bit-identical softmax
+//     decisions;
+//   - writes P (bfloat16) back into tensor memory over its scores and
+//     accumulates O_r += P V_r (A from tensor memory, V read as an MN-major
+//     operand from the same shared-memory tile; M = 128, N = 256, K = 64).
+// The softmax warps send tile t+1's partial before working on tile t, so the
+// exchange latency hides behind the exponentials.  Warp roles: warp 0 TMA
+// producer (3-stage ring), warp 1 MMA issuer (polls both queues, P.V first),
+// warps 2..5 softmax, one head row per thread.  The running max is raised only
+// when it grows by more than 8 (log2 units), so the O rescale is rare; the
+// result is exact either way because P and the running sum use the same max.
 //
 // Work: the concatenation of all sequences' keys is cut into one contiguous
-// range per cluster (a device-side scheduler computes the prefix sums of
-// the lengths); a cluster's range splits into one segment per sequence it
-// touches.  A segment that covers a whole sequence writes o_lat directly;
-// others write (O, m, l) partials that a combine kernel merges.
+// range per cluster (a device-side scheduler computes the prefix sums of the
+// lengths); a range splits into one segment per sequence it touches.  A
+// segment that covers a whole sequence writes o_lat directly; others write
+// (O, m, l) partials that a combine kernel merges.
 #include "mla_internal.cuh"
 #include "ptx.cuh"
 
@@ -38,28 +42,25 @@ namespace {
 
 constexpr int kH = 128;       // heads per CTA = MMA M
 constexpr int kBKV = 64;      // keys per tile
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kThreads = 192;
-constexpr int kXStride = 68;  // floats per exchange-buffer row (272 bytes: conflict-free v4 rows)
 constexpr float kRescaleThreshold = 8.f;
+constexpr int kLA = 4;        // 64-column latent atoms per CTA (r_kv = 512)
 
-template <int LA>  // latent atoms (64 columns) per CTA
-struct DCfg {
-    static constexpr int kQAtoms = LA + 1;
-    static constexpr int kQBytes = kQAtoms * kH * 128;
-    static constexpr int kAtomBytes = kBKV * 128;
-    static constexpr int kStageBytes = kQAtoms * kAtomBytes;
-    static constexpr int kPBytes = kH * 128;
-    static constexpr int kXBytes = kH * kXStride * 4;
-    static constexpr int kOffKV = kQBytes;
-    static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-    static constexpr int kOffX = kOffP + kPBytes;
-    static constexpr int kOffBar = kOffX + kXBytes;
-    static constexpr int kSmem = kOffBar + 256 + 1024;
-    static constexpr int kOCols = LA * 64;
-    static constexpr int kSCol = kOCols;
-    static constexpr int kRLat = 2 * LA * 64;
-};
+// Shared memory (per CTA)
+constexpr int kQLat = kLA * kH * 128;            // 4 latent atoms of the query, 64 KB
+constexpr int kQBytes = kQLat + kH * 64;         // + 32 rope columns (64-byte rows): 72 KB
+constexpr int kAtom = kBKV * 128;                // one 64x64 latent atom of a KV tile
+constexpr int kStageBytes = kLA * kAtom + kBKV * 64;  // + 32 rope columns: 36 KB
+constexpr int kXBytes = kH * 64 * 4;             // peer's partial scores, 32 KB
+constexpr int kOffKV = kQBytes;
+constexpr int kOffX = kOffKV + kStages * kStageBytes;
+constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kSmem = kOffBar + 256 + 1024;
+// Tensor memory: O in columns [0, 256), score / P buffers at 256 and 320.
+constexpr int kOCols = kLA * 64;
+constexpr int kSCol = 256;
+constexpr int kRLat = 2 * kLA * 64;
 
 struct DecTcParams {
     int B, H, max_seq;
@@ -75,9 +76,9 @@ struct DecTcParams {
 struct Bars {
     uint64_t q_full, q_empty;
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], s_empty[2];
+    uint64_t s_full[2];
     uint64_t p_full, pv_done, o_empty;
-    uint64_t x_full, peer_free;
+    uint64_t x_full, x_free;
     int abort;
     uint32_t tmem;
 };
@@ -123,6 +124,16 @@ __device__ __forceinline__ void arrive_remote(uint32_t remote_bar)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
 }
+// 16-byte store into the peer's shared memory that completes 16 bytes of the
+// transaction count of the peer's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     addr),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Segments of this cluster's key range [start, end) of the concatenated keys.
 struct SegIter {
@@ -193,26 +204,22 @@ struct TileCursor {
     }
 };
 
-template <int LA>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQR,
                      const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmR,
                      DecTcParams p)
 {
-    using C = DCfg<LA>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sQ = smem;
-    uint8_t *sKV = smem + C::kOffKV;
-    uint8_t *sP = smem + C::kOffP;
-    float *sX = (float *)(smem + C::kOffX);
-    Bars *bar = (Bars *)(smem + C::kOffBar);
+    uint8_t *sKV = smem + kOffKV;
+    uint8_t *sX = smem + kOffX;
+    Bars *bar = (Bars *)(smem + kOffBar);
     volatile int *abort_flag = &bar->abort;
 
     const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
     const int cid = (int)cluster_id();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int nq_atoms = LA + (rank == 0 ? 1 : 0);
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(&bar->q_full, 1);
@@ -221,22 +228,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&bar->kv_full[i], 1);
             ptx::mbar_init(&bar->kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&bar->s_full[i], 1);
-            ptx::mbar_init(&bar->s_empty[i], kH);
-        }
+        for (int i = 0; i < 2; ++i) ptx::mbar_init(&bar->s_full[i], 1);
         ptx::mbar_init(&bar->p_full, kH);
         ptx::mbar_init(&bar->pv_done, 1);
         ptx::mbar_init(&bar->o_empty, kH);
-        ptx::mbar_init(&bar->x_full, kH);
-        ptx::mbar_init(&bar->peer_free, kH);
+        ptx::mbar_init(&bar->x_full, 1);
+        ptx::mbar_init(&bar->x_free, 1);
         bar->abort = 0;
         ptx::fence_mbar_init();
+        ptx::mbar_expect_tx(&bar->x_full, kXBytes);  // arm the first exchange
     }
     if (warp == 1) ptx::tmem_alloc(&bar->tmem, 512);
     ptx::tc_fence_before();
     __syncthreads();
-    cluster_sync();  // the peer's barriers exist before any remote arrive
+    cluster_sync();  // the peer's barriers exist before any remote arrive or store
     ptx::tc_fence_after();
     const uint32_t tmem = bar->tmem;
     const int chunk = *p.chunk;
@@ -259,30 +264,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             int b, k0, k1;
             bool whole;
             int nseg = 0, g = 0;
-            int pending[kStages] = {-1, -1};
+            int pending[kStages] = {-1, -1, -1};
             int q_pending = -1;
             while (ok && it.next(b, k0, k1, whole)) {
                 if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) { fail(); break; }
-                ptx::mbar_expect_tx(&bar->q_full, nq_atoms * kH * 128);
-                for (int a = 0; a < LA; ++a)
-                    ptx::tma_load_2d_hint(sQ + a * kH * 128, &tmQ, &bar->q_full, (int)rank * LA * 64 + a * 64,
+                ptx::mbar_expect_tx(&bar->q_full, kQBytes);
+                for (int a = 0; a < kLA; ++a)
+                    ptx::tma_load_2d_hint(sQ + a * kH * 128, &tmQ, &bar->q_full, (int)rank * kLA * 64 + a * 64,
                                           b * p.H, keep);
-                if (rank == 0) ptx::tma_load_2d_hint(sQ + LA * kH * 128, &tmQR, &bar->q_full, 0, b * p.H, keep);
+                ptx::tma_load_2d_hint(sQ + kQLat, &tmQR, &bar->q_full, (int)rank * 32, b * p.H, keep);
                 q_pending = nseg & 1;
                 ++nseg;
                 const int ntiles = (k1 - k0 + kBKV - 1) / kBKV;
                 for (int t = 0; t < ntiles; ++t, ++g) {
-                    const int st = g & 1;
-                    if (!ptx::mbar_wait(&bar->kv_empty[st], ((g >> 1) & 1) ^ 1, abort_flag)) { fail(); break; }
-                    ptx::mbar_expect_tx(&bar->kv_full[st], nq_atoms * C::kAtomBytes);
+                    const int st = g % kStages;
+                    const uint32_t ph = (uint32_t)(g / kStages) & 1;
+                    if (!ptx::mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag)) { fail(); break; }
+                    ptx::mbar_expect_tx(&bar->kv_full[st], kStageBytes);
                     const int row = b * p.max_seq + k0 + t * kBKV;
-                    uint8_t *dst = sKV + st * C::kStageBytes;
-                    for (int a = 0; a < LA; ++a)
-                        ptx::tma_load_2d_hint(dst + a * C::kAtomBytes, &tmL, &bar->kv_full[st],
-                                              (int)rank * LA * 64 + a * 64, row, stream);
-                    if (rank == 0)
-                        ptx::tma_load_2d_hint(dst + LA * C::kAtomBytes, &tmR, &bar->kv_full[st], 0, row, stream);
-                    pending[st] = (g >> 1) & 1;
+                    uint8_t *dst = sKV + st * kStageBytes;
+                    for (int a = 0; a < kLA; ++a)
+                        ptx::tma_load_2d_hint(dst + a * kAtom, &tmL, &bar->kv_full[st], (int)rank * kLA * 64 + a * 64,
+                                              row, stream);
+                    ptx::tma_load_2d_hint(dst + kLA * kAtom, &tmR, &bar->kv_full[st], (int)rank * 32, row, stream);
+                    pending[st] = (int)ph;
                 }
             }
             volatile int never = 0;
@@ -293,11 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (ptx::elect_one()) {
             // Non-blocking issue: poll both queues and issue whichever MMA
-            // group is ready, P.V first (it frees a KV stage for the next
-            // load); a QK^T waiting on its tile never holds back a P.V.
+            // group is ready, P.V first (it frees a KV stage for the next load).
             constexpr uint32_t idesc_s = ptx::idesc_bf16(kH, kBKV, false, false);
-            constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, LA * 64, false, true);
-            const uint32_t q0 = ptx::smem_u32(sQ), kv0 = ptx::smem_u32(sKV), p0 = ptx::smem_u32(sP);
+            constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, kLA * 64, false, true);
+            const uint32_t q0 = ptx::smem_u32(sQ), kv0 = ptx::smem_u32(sKV);
             TileCursor qk, pv;
             qk.init(p.prefix, p.B, cid, chunk);
             pv.init(p.prefix, p.B, cid, chunk);
@@ -310,36 +314,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ready = ptx::mbar_try_wait(ptx::smem_u32(&bar->o_empty), (pv.nseg - 1) & 1);
                     if (ready) {
                         ptx::tc_fence_after();
-                        const int st = pv.g & 1;
-                        const uint32_t vb = kv0 + st * C::kStageBytes;
+                        const int st = pv.g % kStages;
+                        const uint32_t vb = kv0 + st * kStageBytes;
+                        const uint32_t pa = tmem + kSCol + (pv.g & 1) * kBKV;
 #pragma unroll
                         for (int k = 0; k < kBKV / 16; ++k)
-                            ptx::mma_bf16(tmem, ptx::sdesc_sw128(p0 + k * 32, 16, 1024),
-                                          ptx::sdesc_sw128(vb + k * 2048, C::kAtomBytes, 1024), idesc_o,
-                                          (pv.t == 0 && k == 0) ? 0u : 1u);
+                            ptx::mma_f16_tmem_a(tmem, pa + k * 8, ptx::sdesc_sw128(vb + k * 2048, kAtom, 1024),
+                                                idesc_o, (pv.t == 0 && k == 0) ? 0u : 1u);
                         ptx::mma_commit(&bar->kv_empty[st]);
                         ptx::mma_commit(&bar->pv_done);
                         pv.step();
                         progressed = true;
                     }
                 }
-                if (qk.valid) {
-                    const int st = qk.g & 1;
+                // QK^T of tile g overwrites the buffer that held P(g - 2):
+                // P.V(g - 2) must have been issued (the tensor pipe keeps order).
+                if (qk.valid && pv.g >= qk.g - 1) {
+                    const int st = qk.g % kStages;
                     bool ready = qk.t > 0 || ptx::mbar_try_wait(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
-                    ready = ready && ptx::mbar_try_wait(ptx::smem_u32(&bar->kv_full[st]), (qk.g >> 1) & 1) &&
-                            ptx::mbar_try_wait(ptx::smem_u32(&bar->s_empty[st]), ((qk.g >> 1) & 1) ^ 1);
+                    ready = ready && ptx::mbar_try_wait(ptx::smem_u32(&bar->kv_full[st]), (qk.g / kStages) & 1);
                     if (ready) {
                         ptx::tc_fence_after();
-                        const uint32_t kb = kv0 + st * C::kStageBytes;
-                        const uint32_t d = tmem + C::kSCol + st * kBKV;
-                        for (int a = 0; a < nq_atoms; ++a) {
+                        const uint32_t kb = kv0 + st * kStageBytes;
+                        const uint32_t d = tmem + kSCol + (qk.g & 1) * kBKV;
+#pragma unroll
+                        for (int a = 0; a < kLA; ++a) {
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 ptx::mma_bf16(d, ptx::sdesc_sw128(q0 + a * kH * 128 + k * 32, 16, 1024),
-                                              ptx::sdesc_sw128(kb + a * C::kAtomBytes + k * 32, 16, 1024),
-                                              idesc_s, (a | k) != 0);
+                                              ptx::sdesc_sw128(kb + a * kAtom + k * 32, 16, 1024), idesc_s,
+                                              (a | k) != 0);
                         }
-                        ptx::mma_commit(&bar->s_full[st]);
+#pragma unroll
+                        for (int k = 0; k < 2; ++k)
+                            ptx::mma_bf16(d, ptx::sdesc_sw64(q0 + kQLat + k * 32, 512),
+                                          ptx::sdesc_sw64(kb + kLA * kAtom + k * 32, 512), idesc_s, 1u);
+                        ptx::mma_commit(&bar->s_full[qk.g & 1]);
                         if (qk.t == qk.ntiles - 1) ptx::mma_commit(&bar->q_empty);
                         qk.step();
                         progressed = true;
@@ -353,50 +363,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp % 4;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const uint32_t peer_x = map_peer(sX + h * kXStride, peer);
+        const uint32_t peer_xrow = map_peer(sX + h * 256, peer);
         const uint32_t peer_xfull = map_peer(&bar->x_full, peer);
-        const uint32_t peer_free = map_peer(&bar->peer_free, peer);
-        float *my_x = sX + h * kXStride;
-        uint8_t *prow = sP + h * 128;
+        const uint32_t peer_xfree = map_peer(&bar->x_free, peer);
+        const uint8_t *my_xrow = sX + h * 256;
+        // Total tiles of this cluster (the exchange runs one tile ahead,
+        // across segment boundaries).
+        int n_tiles = 0;
+        {
+            SegIter it;
+            it.init(p.prefix, p.B, cid, chunk);
+            int b, k0, k1;
+            bool whole;
+            while (it.next(b, k0, k1, whole)) n_tiles += (k1 - k0 + kBKV - 1) / kBKV;
+        }
+        // Read this thread's score row of buffer g & 1 and send it to the
+        // peer (16-byte chunk c of row h goes to chunk c ^ (h & 15)).
+        auto send = [&](int g) -> bool {
+            if (!ptx::mbar_wait(&bar->s_full[g & 1], (g >> 1) & 1, abort_flag)) return false;
+            ptx::tc_fence_after();
+            if (!ptx::mbar_wait_cluster(&bar->x_free, (g & 1) ^ 1, abort_flag)) return false;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV + half * 32, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int cc = half * 8 + c;
+                    st_async_v4(peer_xrow + ((cc ^ (h & 15)) << 4), __uint_as_float(r[4 * c]),
+                                __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
+                                __uint_as_float(r[4 * c + 3]), peer_xfull);
+                }
+            }
+            return true;
+        };
+        if (n_tiles > 0 && !send(0)) fail();
         SegIter it;
         it.init(p.prefix, p.B, cid, chunk);
         int b, k0, k1;
         bool whole;
-        int g = 0, s_cnt = 0, x_cnt = 0, p_cnt = 0;
+        int g = 0;
         while (ok && it.next(b, k0, k1, whole)) {
             float m_run = -INFINITY, l_run = 0.f;
             const int len = k1 - k0;
             const int ntiles = (len + kBKV - 1) / kBKV;
             for (int t = 0; t < ntiles; ++t, ++g) {
                 const int valid = min(kBKV, len - t * kBKV);
-                const int sb = s_cnt & 1;
-                if (!ptx::mbar_wait(&bar->s_full[sb], (s_cnt >> 1) & 1, abort_flag)) { fail(); break; }
-                ptx::tc_fence_after();
-                uint32_t r0[32], r1[32];
-                ptx::tmem_ld32(tmem + lane_off + C::kSCol + sb * kBKV, r0);
-                ptx::tmem_ld32(tmem + lane_off + C::kSCol + sb * kBKV + 32, r1);
-                ptx::tmem_ld_wait();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(&bar->s_empty[sb]);
-                ++s_cnt;
+                // 1. Full scores of tile g: own partial (still in tensor
+                //    memory) plus the peer's, same operand order in both CTAs.
+                if (!ptx::mbar_wait_cluster(&bar->x_full, g & 1, abort_flag)) { fail(); break; }
                 float s[64];
+                {
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV, r0);
+                    ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV + 32, r1);
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) { s[j] = __uint_as_float(r0[j]); s[32 + j] = __uint_as_float(r1[j]); }
-                // Exchange partial scores with the peer CTA.
-                if (!ptx::mbar_wait_cluster(&bar->peer_free, (x_cnt & 1) ^ 1, abort_flag)) { fail(); break; }
-#pragma unroll
-                for (int j = 0; j < 64; j += 4) st_cluster_v4(peer_x + j * 4, s[j], s[j + 1], s[j + 2], s[j + 3]);
-                arrive_remote(peer_xfull);
-                if (!ptx::mbar_wait_cluster(&bar->x_full, x_cnt & 1, abort_flag)) { fail(); break; }
-#pragma unroll
-                for (int j = 0; j < 64; j += 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(my_x + j);
-                    // Same operand order in both CTAs: S_0 + S_1.
-                    if (rank == 0) { s[j] += v.x; s[j + 1] += v.y; s[j + 2] += v.z; s[j + 3] += v.w; }
-                    else { s[j] = v.x + s[j]; s[j + 1] = v.y + s[j + 1]; s[j + 2] = v.z + s[j + 2]; s[j + 3] = v.w + s[j + 3]; }
+                    for (int c = 0; c < 16; ++c) {
+                        const float4 v = *reinterpret_cast<const float4 *>(my_xrow + ((c ^ (h & 15)) << 4));
+                        const uint32_t *rr = c < 8 ? &r0[4 * c] : &r1[4 * (c - 8)];
+                        const float o0 = __uint_as_float(rr[0]), o1 = __uint_as_float(rr[1]);
+                        const float o2 = __uint_as_float(rr[2]), o3 = __uint_as_float(rr[3]);
+                        if (rank == 0) {
+                            s[4 * c] = o0 + v.x; s[4 * c + 1] = o1 + v.y; s[4 * c + 2] = o2 + v.z; s[4 * c + 3] = o3 + v.w;
+                        } else {
+                            s[4 * c] = v.x + o0; s[4 * c + 1] = v.y + o1; s[4 * c + 2] = v.z + o2; s[4 * c + 3] = v.w + o3;
+                        }
+                    }
                 }
-                arrive_remote(peer_free);
-                ++x_cnt;
+                softmax_bar();  // every row of the exchange buffer has been read
+                if (h == 0) {
+                    ptx::mbar_expect_tx(&bar->x_full, kXBytes);  // arm the next exchange
+                    arrive_remote(peer_xfree);                   // the peer may overwrite it
+                }
+                // 2. Send the next tile's partial before the exponentials.
+                if (g + 1 < n_tiles && !send(g + 1)) { fail(); break; }
+                // 3. Online softmax of tile g.
                 float mt = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < 64; ++j) {
@@ -416,12 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l_run = l_run * corr + psum;
                 m_run = m_new;
-                // The previous PV must be done before P is overwritten or O rescaled.
-                if (p_cnt > 0 && !ptx::mbar_wait(&bar->pv_done, (p_cnt - 1) & 1, abort_flag)) { fail(); break; }
+                // Wait for P.V(g - 1) every tile, so that the pv_done phases
+                // are observed in order (a parity wait is only valid one
+                // phase behind); it is long done by now.  O must also hold
+                // every earlier P.V before a rescale.
+                if (g > 0 && !ptx::mbar_wait(&bar->pv_done, (g - 1) & 1, abort_flag)) { fail(); break; }
                 if (resc && t > 0) {
                     ptx::tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < C::kOCols; c += 32) {
+                    for (int c = 0; c < kOCols; c += 32) {
                         uint32_t o[32];
                         ptx::tmem_ld32(tmem + lane_off + c, o);
                         ptx::tmem_ld_wait();
@@ -429,45 +475,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
                         ptx::tmem_st32(tmem + lane_off + c, o);
                     }
-                    ptx::tmem_st_wait();
                 }
-                // P row (K-major, 128-byte swizzle: 16-byte chunk j at j ^ (h & 7)).
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<uint4 *>(prow + ((j ^ (h & 7)) << 4)) =
-                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                // P over the scores of this tile (columns 0..31 of the buffer).
+                ptx::tmem_st32(tmem + lane_off + kSCol + (g & 1) * kBKV, pk);
+                ptx::tmem_st_wait();
                 if (valid < kBKV) {
                     // Rows past the segment may hold arbitrary cache contents;
                     // P is 0 there, but 0 * NaN is not 0: zero those rows.
-                    uint8_t *stg = sKV + (g & 1) * C::kStageBytes;
+                    uint8_t *stg = sKV + (g % kStages) * kStageBytes;
                     const int nrow = kBKV - valid;
-                    for (int i = h; i < LA * nrow * 8; i += kH) {
+                    for (int i = h; i < kLA * nrow * 8; i += kH) {
                         const int a = i / (nrow * 8), rr = (i / 8) % nrow, ch = i % 8;
-                        *reinterpret_cast<uint4 *>(stg + a * C::kAtomBytes + (valid + rr) * 128 + ch * 16) =
+                        *reinterpret_cast<uint4 *>(stg + a * kAtom + (valid + rr) * 128 + ch * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
+                    ptx::fence_proxy_async_smem();
                 }
-                ptx::fence_proxy_async_smem();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bar->p_full);
-                ++p_cnt;
             }
             if (!ok) break;
-            // Segment done: read the accumulator once its last PV completed.
-            if (!ptx::mbar_wait(&bar->pv_done, (p_cnt - 1) & 1, abort_flag)) { fail(); break; }
+            // Segment done: read the accumulator once its last P.V completed.
+            if (!ptx::mbar_wait(&bar->pv_done, (g - 1) & 1, abort_flag)) { fail(); break; }
             ptx::tc_fence_after();
             const bool row_ok = h < p.H;
             const int slot = cid + b;
 #pragma unroll 1
-            for (int c = 0; c < C::kOCols; c += 32) {
+            for (int c = 0; c < kOCols; c += 32) {
                 uint32_t o[32];
                 ptx::tmem_ld32(tmem + lane_off + c, o);
                 ptx::tmem_ld_wait();
                 if (!row_ok) continue;
-                const int col = (int)rank * C::kOCols + c;
+                const int col = (int)rank * kOCols + c;
                 if (whole) {
                     const float inv = 1.f / l_run;
-                    bf16 *dst = p.o_lat + ((int64_t)b * p.H + h) * C::kRLat + col;
+                    bf16 *dst = p.o_lat + ((int64_t)b * p.H + h) * kRLat + col;
 #pragma unroll
                     for (int j = 0; j < 32; j += 8) {
                         uint4 w;
@@ -478,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(dst + j) = w;
                     }
                 } else {
-                    float *dst = p.o_part + ((int64_t)slot * p.H + h) * C::kRLat + col;
+                    float *dst = p.o_part + ((int64_t)slot * p.H + h) * kRLat + col;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4 *>(dst + j) =
@@ -587,23 +629,22 @@ __global__ void __launch_bounds__(128) decode_combine_tc_kernel(const int *prefi
     }
 }
 
-template <int LA>
 cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
 {
-    using C = DCfg<LA>;
     CUtensorMap tq, tqr, tl, tr;
     const int64_t q_rows = (int64_t)a.B * a.H;
-    if (!make_tmap_bf16(&tq, a.q_abs, q_rows, 2 * LA * 64, 2 * LA * 64, 64, kH) ||
-        !make_tmap_bf16(&tqr, a.q_rope, q_rows, 64, 64, 64, kH) ||
-        !make_tmap_bf16(&tl, a.lat, (int64_t)a.max_batch * a.max_seq, 2 * LA * 64, a.lat_stride, 64, kBKV) ||
-        !make_tmap_bf16(&tr, a.rope, (int64_t)a.max_batch * a.max_seq, 64, a.rope_stride, 64, kBKV))
+    const int64_t c_rows = (int64_t)a.max_batch * a.max_seq;
+    if (!make_tmap_bf16(&tq, a.q_abs, q_rows, kRLat, kRLat, 64, kH) ||
+        !make_tmap_bf16(&tqr, a.q_rope, q_rows, 64, 64, 32, kH) ||
+        !make_tmap_bf16(&tl, a.lat, c_rows, kRLat, a.lat_stride, 64, kBKV) ||
+        !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV))
         return cudaErrorInvalidValue;
     decode_schedule_kernel<<<1, 1024, 0, s>>>(a.seq_lens, a.B, a.max_seq, a.n_clusters, a.prefix, a.chunk,
                                               a.status);
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_tc_kernel<LA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     DecTcParams p;
     p.B = a.B; p.H = a.H; p.max_seq = a.max_seq;
@@ -616,7 +657,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * a.n_clusters, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -626,11 +667,11 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     profile_begin(MLA_PROFILE_DECODE_ATTENTION, s);
-    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<LA>, tq, tqr, tl, tr, p);
+    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tq, tqr, tl, tr, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
     if (e != cudaSuccess) return e;
-    decode_combine_tc_kernel<<<dim3(a.H, a.B), 128, 0, s>>>(a.prefix, a.chunk, a.B, a.H, 2 * LA * 64, a.o_part,
+    decode_combine_tc_kernel<<<dim3(a.H, a.B), 128, 0, s>>>(a.prefix, a.chunk, a.B, a.H, kRLat, a.o_part,
                                                             a.ml_part, (bf16 *)a.o_lat);
     note_launch();
     return cudaGetLastError();
@@ -642,9 +683,7 @@ int decode_tc_max_clusters()
 {
     static int cached = -1;
     if (cached >= 0) return cached;
-    using C = DCfg<4>;
-    if (cudaFuncSetAttribute(decode_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) != cudaSuccess)
         return cached = 0;
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
@@ -652,7 +691,7 @@ int decode_tc_max_clusters()
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.dynamicSmemBytes = kSmem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -661,7 +700,7 @@ int decode_tc_max_clusters()
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<4>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel, &cfg) != cudaSuccess) n = 0;
     return cached = n;
 }
 
@@ -671,7 +710,7 @@ cudaError_t decode_tc(const DecodeTcArgs &a, cudaStream_t s)
 {
     if (a.B == 0) return cudaSuccess;
     if (!decode_tc_supported(a.H, a.r_kv, a.d_rope) || a.n_clusters < 1) return cudaErrorInvalidValue;
-    return launch_decode_tc<4>(a, s);
+    return launch_decode_tc(a, s);
 }
 
 }  // namespace mla

@@ -296,8 +296,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 }  // namespace
 
-// 2-D bfloat16 tensor map over a row-major view with a (64 x box_rows) box,
-// 128-byte swizzle, zero fill out of bounds.
+// 2-D 16-bit tensor map over a row-major view with a (box_cols x box_rows)
+// box, zero fill out of bounds; 128-byte swizzle for 64-column boxes, 64-byte
+// swizzle for 32-column boxes.
 bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
                     int box_rows)
 {
@@ -308,7 +309,8 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
     cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
