@@ -85,7 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mla_project_latent": (I, [P, P, P, L, P, P, P, P, P, P, S, P]),
         "mla_prefill": (I, [P, P, P, P, P, I, I, P, P, P, S, P]),
         "mla_decode": (I, [P, P, P, P, P, P, I, P, P, S, P]),
-        "mla_out_proj": (I, [P, P, P, L, P, P]),
+        "mla_out_proj": (I, [P, P, P, L, P, P, S, P]),
         "mla_get_device_status": (I, [P, P, P, ctypes.POINTER(ctypes.c_uint32)]),
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_launch_count": (ctypes.c_uint64, []),
@@ -217,9 +217,10 @@ def mla_decode(h: Handle, w: MlaWeights, q_nope: torch.Tensor, q_rope: Optional[
         B, _ptr(o), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
-def mla_out_proj(h: Handle, w: MlaWeights, o: torch.Tensor, y: torch.Tensor, stream=None) -> int:
+def mla_out_proj(h: Handle, w: MlaWeights, o: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
+                 stream=None) -> int:
     return load_library().mla_out_proj(h.ptr, ctypes.byref(w), _ptr(o), o.shape[0], _ptr(y),
-                                       _stream(stream))
+                                       _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
 def mla_get_device_status(h: Handle, ws: torch.Tensor, stream=None):
@@ -295,7 +296,7 @@ class MlaLayer:
     def out_proj(self, o, stream=None):
         o2 = o.reshape(o.shape[0] if o.dim() == 3 else -1, self.cfg.n_heads * self.cfg.d_v)
         y = torch.empty(o2.shape[0], self.cfg.d_model, dtype=o.dtype, device=o.device)
-        _check(mla_out_proj(self.h, self.w, o2, y, stream), "mla_out_proj")
+        _check(mla_out_proj(self.h, self.w, o2, y, self.ws, stream), "mla_out_proj")
         return y
 
     def device_status(self, stream=None):

@@ -54,16 +54,77 @@ int heads_per_block_of(const mla_config &c) { return c.n_heads / c.n_latent_head
 int decode_splits(const mla_config &c) { return (c.max_seq + kDecodeChunk - 1) / kDecodeChunk; }
 
 // Workspace regions, each 256-byte aligned, after the status header.
-struct ProjectWs { size_t cq, end; };
+struct ProjectWs { size_t cq, split, end; };
+struct OutProjWs { size_t split, end; };
 struct DecodeWs { size_t q_abs, o_lat, o_part, ml_part, prefix, end; };
 struct PrefillWs { size_t start_pos, k, v, kr, end; };
 
-ProjectWs project_ws(const mla_config &c, int64_t T)
+// The projection GEMMs of one call, in the shapes mla_project_latent runs
+// them (used both to size and to launch; the pointers are filled in later).
+struct ProjGemms {
+    GemmArgs g[5];
+    int n = 0;
+};
+
+ProjGemms project_gemms(const mla_config &c, int64_t T)
 {
+    ProjGemms r;
+    const int M = (int)T, H = c.n_heads;
+    auto lin = [&](int N, int K) {
+        GemmArgs g;
+        g.A = Mat2D{nullptr, M, K, K};
+        g.B = Mat2D{nullptr, N, K, K};
+        g.M = M; g.N = N; g.K = K;
+        return g;
+    };
+    r.g[r.n++] = lin(c.r_kv, c.d_model);
+    if (c.variant == MLA_VARIANT_DECOUPLED) {
+        r.g[r.n++] = lin(c.d_rope, c.d_model);
+        r.g[r.n++] = lin(c.r_q, c.d_model);
+        r.g[r.n++] = lin(H * c.d_nope, c.r_q);
+        r.g[r.n++] = lin(H * c.d_rope, c.r_q);
+    } else {
+        r.g[r.n++] = lin(H * c.d_nope, c.d_model);
+    }
+    return r;
+}
+
+size_t split_bytes(const mla_handle *h, const GemmArgs &g)
+{
+    return h->cfg.dtype == MLA_DTYPE_BF16 ? gemm_tc_workspace(g, h->num_sms) : 0;
+}
+
+ProjectWs project_ws(const mla_handle *h, int64_t T)
+{
+    const mla_config &c = h->cfg;
     ProjectWs w;
     w.cq = kWsHeader;
     size_t n = c.variant == MLA_VARIANT_DECOUPLED ? (size_t)T * c.r_q * esize(c) : 0;
-    w.end = round_up(w.cq + n, 256);
+    w.split = round_up(w.cq + n, 256);
+    size_t sb = 0;
+    if (T > 0 && T <= INT32_MAX) {
+        ProjGemms pg = project_gemms(c, T);
+        for (int i = 0; i < pg.n; ++i) sb = std::max(sb, split_bytes(h, pg.g[i]));
+    }
+    w.end = round_up(w.split + sb, 256);
+    return w;
+}
+
+OutProjWs out_proj_ws(const mla_handle *h, int64_t T)
+{
+    const mla_config &c = h->cfg;
+    OutProjWs w;
+    w.split = kWsHeader;
+    size_t sb = 0;
+    if (T > 0 && T <= INT32_MAX) {
+        const int K = c.n_heads * c.d_v;
+        GemmArgs g;
+        g.A = Mat2D{nullptr, T, K, K};
+        g.B = Mat2D{nullptr, c.d_model, K, K};
+        g.M = (int)T; g.N = c.d_model; g.K = K;
+        sb = split_bytes(h, g);
+    }
+    w.end = round_up(w.split + sb, 256);
     return w;
 }
 
@@ -133,9 +194,10 @@ GemmArgs linear_args(const void *x, int64_t ldx, const void *W, int64_t ldw, int
 }
 
 // bfloat16 runs on the tensor cores, float32 on the CUDA cores.
-mla_status run_gemm(const mla_handle *h, GemmArgs g, uint32_t *status, cudaStream_t s)
+mla_status run_gemm(const mla_handle *h, GemmArgs g, uint32_t *status, cudaStream_t s, float *split = nullptr)
 {
     if (!g.epi.status) g.epi.status = status;
+    g.split_ws = split;
     if (h->cfg.dtype == MLA_DTYPE_BF16) {
         if (!gemm_tc_supported(g)) return MLA_ERR_UNSUPPORTED;
         return cuda_status(gemm_tc(g, h->num_sms, s));
@@ -253,7 +315,8 @@ size_t mla_workspace_size(const mla_handle *h, int batch, int max_len, int64_t n
     if (!h || batch < 0 || max_len < 0 || n_tokens < 0) return 0;
     const mla_config &c = h->cfg;
     size_t need = kWsHeader;
-    need = std::max(need, project_ws(c, n_tokens).end);
+    need = std::max(need, project_ws(h, n_tokens).end);
+    need = std::max(need, out_proj_ws(h, n_tokens).end);
     if (c.variant != MLA_VARIANT_SMALL) need = std::max(need, decode_ws(h, batch).end);
     need = std::max(need, prefill_ws(c, batch, max_len).end);
     return need;
@@ -279,19 +342,20 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
     if (!align_ok(c, {x, q_nope, q_rope, cache->lat, cache->rope, w->W_DQ, w->W_UQ, w->W_QR, w->W_DKV,
                       w->W_KR, w->W_Q, ws}))
         return MLA_ERR_INVALID_ARG;
-    ProjectWs L = project_ws(c, T);
+    ProjectWs L = project_ws(h, T);
     if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t *status = (uint32_t *)ws;
     const int M = (int)T, H = c.n_heads;
     char *wsb = (char *)ws;
+    float *split = (float *)(wsb + L.split);
 
     // Latent and (decoupled) rope key, written straight into the caches.
     GemmArgs g = linear_args(x, c.d_model, w->W_DKV, c.d_model, M, c.r_kv, c.d_model, cache->lat,
                              cache->lat_stride);
     g.epi.row_seq = seq_idx; g.epi.row_pos = pos; g.epi.seq_rows = c.max_seq;
     g.epi.max_batch = c.max_batch; g.epi.max_seq = c.max_seq;
-    MLA_TRY(run_gemm(h, g, status, s));
+    MLA_TRY(run_gemm(h, g, status, s, split));
     if (dec) {
         GemmArgs r = g;
         r.B = Mat2D{w->W_KR, c.d_rope, c.d_model, c.d_model};
@@ -299,20 +363,20 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
         r.epi.out = cache->rope; r.epi.ldc = cache->rope_stride;
         r.epi.rope_mode = kRopeInterleaved; r.epi.rope_dim = c.d_rope;
         r.epi.rope_table = h->rope_table; r.epi.rope_pos = pos;
-        MLA_TRY(run_gemm(h, r, status, s));
+        MLA_TRY(run_gemm(h, r, status, s, split));
 
         void *cq = wsb + L.cq;
         GemmArgs a = linear_args(x, c.d_model, w->W_DQ, c.d_model, M, c.r_q, c.d_model, cq, c.r_q);
-        MLA_TRY(run_gemm(h, a, status, s));
+        MLA_TRY(run_gemm(h, a, status, s, split));
         GemmArgs qn = linear_args(cq, c.r_q, w->W_UQ, c.r_q, M, H * c.d_nope, c.r_q, q_nope,
                                   (int64_t)H * c.d_nope);
-        MLA_TRY(run_gemm(h, qn, status, s));
+        MLA_TRY(run_gemm(h, qn, status, s, split));
         GemmArgs qr = linear_args(cq, c.r_q, w->W_QR, c.r_q, M, H * c.d_rope, c.r_q, q_rope,
                                   (int64_t)H * c.d_rope);
         qr.epi.rope_mode = kRopeInterleaved; qr.epi.rope_dim = c.d_rope;
         qr.epi.rope_table = h->rope_table; qr.epi.rope_pos = pos;
         qr.epi.max_seq = c.max_seq;
-        MLA_TRY(run_gemm(h, qr, status, s));
+        MLA_TRY(run_gemm(h, qr, status, s, split));
     } else {
         GemmArgs q = linear_args(x, c.d_model, w->W_Q, c.d_model, M, H * c.d_nope, c.d_model, q_nope,
                                  (int64_t)H * c.d_nope);
@@ -321,7 +385,7 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
             q.epi.rope_table = h->rope_table; q.epi.rope_pos = pos;
             q.epi.max_seq = c.max_seq;
         }
-        MLA_TRY(run_gemm(h, q, status, s));
+        MLA_TRY(run_gemm(h, q, status, s, split));
     }
     return MLA_OK;
 }
@@ -515,17 +579,19 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     return MLA_OK;
 }
 
-mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int64_t T, void *y,
-                        void *stream)
+mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int64_t T, void *y, void *ws,
+                        size_t ws_bytes, void *stream)
 {
     if (!h || !w || T < 0) return MLA_ERR_INVALID_ARG;
     if (T == 0) return MLA_OK;
     const mla_config &c = h->cfg;
-    if (!o || !y || !w->W_O || T > INT32_MAX) return MLA_ERR_INVALID_ARG;
-    if (!align_ok(c, {o, y, w->W_O})) return MLA_ERR_INVALID_ARG;
+    if (!o || !y || !w->W_O || !ws || T > INT32_MAX) return MLA_ERR_INVALID_ARG;
+    if (!align_ok(c, {o, y, w->W_O, ws})) return MLA_ERR_INVALID_ARG;
+    OutProjWs L = out_proj_ws(h, T);
+    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
     const int K = c.n_heads * c.d_v;
     GemmArgs g = linear_args(o, K, w->W_O, K, (int)T, c.d_model, K, y, c.d_model);
-    return run_gemm(h, g, h->status, (cudaStream_t)stream);
+    return run_gemm(h, g, (uint32_t *)ws, (cudaStream_t)stream, (float *)((char *)ws + L.split));
 }
 
 mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t *bits)

@@ -297,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         if (ptx::elect_one()) {
-            // Non-blocking issue: poll both queues and issue whichever MMA
-            // group is ready, P.V first (it frees a KV stage for the next load).
+            // Non-blocking issue (test_wait, never try_wait, which may suspend
+            // the thread): poll both queues and issue whichever MMA group is
+            // ready, P.V first (it frees a KV stage for the next load).
             constexpr uint32_t idesc_s = ptx::idesc_bf16(kH, kBKV, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, kLA * 64, false, true);
             const uint32_t q0 = ptx::smem_u32(sQ), kv0 = ptx::smem_u32(sKV);
@@ -309,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok && pv.valid) {
                 bool progressed = false;
                 if (pv.g < qk.g) {
-                    bool ready = ptx::mbar_try_wait(ptx::smem_u32(&bar->p_full), pv.g & 1);
+                    bool ready = ptx::mbar_test(ptx::smem_u32(&bar->p_full), pv.g & 1);
                     if (ready && pv.t == 0 && pv.nseg > 0)
-                        ready = ptx::mbar_try_wait(ptx::smem_u32(&bar->o_empty), (pv.nseg - 1) & 1);
+                        ready = ptx::mbar_test(ptx::smem_u32(&bar->o_empty), (pv.nseg - 1) & 1);
                     if (ready) {
                         ptx::tc_fence_after();
                         const int st = pv.g % kStages;
@@ -331,8 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // P.V(g - 2) must have been issued (the tensor pipe keeps order).
                 if (qk.valid && pv.g >= qk.g - 1) {
                     const int st = qk.g % kStages;
-                    bool ready = qk.t > 0 || ptx::mbar_try_wait(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
-                    ready = ready && ptx::mbar_try_wait(ptx::smem_u32(&bar->kv_full[st]), (qk.g / kStages) & 1);
+                    bool ready = qk.t > 0 || ptx::mbar_test(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
+                    ready = ready && ptx::mbar_test(ptx::smem_u32(&bar->kv_full[st]), (qk.g / kStages) & 1);
                     if (ready) {
                         ptx::tc_fence_after();
                         const uint32_t kb = kv0 + st * kStageBytes;

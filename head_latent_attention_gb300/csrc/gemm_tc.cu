@@ -14,6 +14,8 @@
 // timeout bit, stops issuing, drains its own copies and frees tensor memory.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "mla_internal.cuh"
 #include "ptx.cuh"
 
@@ -29,6 +31,8 @@ struct TcGemmParams {
     int M, N, K, batch;
     int64_t a_row_batch, a_col_batch, b_row_batch, b_col_batch;
     int tiles_m, tiles_n;
+    int splits, kb_per_split;  // split-K: unit u = (tile u % tiles, K slice u / tiles)
+    float *partial;            // split-K partial sums [splits, M, N] (fp32), or null
     Epilogue epi;
     uint32_t *status;
 };
@@ -154,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int num_tiles = p.tiles_m * p.tiles_n * p.batch;
+    const int num_units = num_tiles * p.splits;
     const int nk = (p.K + kBK - 1) / kBK;
     bool ok = true;
 
@@ -166,11 +171,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pending[S];
 #pragma unroll
             for (int i = 0; i < S; ++i) pending[i] = -1;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
                 int z, mt, nt;
-                tile_coords(t, p.tiles_m, p.tiles_n, z, mt, nt);
+                tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
+                const int ks = u / num_tiles;
+                const int kb0 = ks * p.kb_per_split, kb1 = min(nk, kb0 + p.kb_per_split);
                 const int ax = (int)(z * p.a_col_batch), ay = (int)(z * p.a_row_batch) + mt * kBM;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
                     ptx::mbar_expect_tx(&full[stage], C::kStageBytes);
                     ptx::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], ax + kb * kBK, ay);
@@ -202,11 +209,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                const int ks = u / num_tiles;
+                const int kb0 = ks * p.kb_per_split, kb1 = min(nk, kb0 + p.kb_per_split);
                 if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + acc * BN;
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t a0 = ptx::smem_u32(sA + stage * C::kABytes);
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t ad = ptx::sdesc_sw128(a0 + k * 32, 16, 1024);
                         const uint64_t bd = kBMN ? ptx::sdesc_sw128(b0 + k * 2048, kBK * 128, 1024)
                                                  : ptx::sdesc_sw128(b0 + k * 32, 16, 1024);
-                        ptx::mma_bf16(d, ad, bd, idesc, (kb | k) != 0);
+                        ptx::mma_bf16(d, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
                     }
                     ptx::mma_commit(&empty[stage]);
                     if (++stage == S) { stage = 0; phase ^= 1; }
@@ -233,14 +242,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         const bool half_rope = p.epi.rope_mode == kRopeHalf;
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             int z, mt, nt;
-            tile_coords(t, p.tiles_m, p.tiles_n, z, mt, nt);
+            tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
+            const int ks = u / num_tiles;
             if (!ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag)) { ok = false; break; }
             ptx::tc_fence_after();
             const int m = mt * kBM + quad * 32 + lane;
             const uint32_t tbase = tmem + acc * BN + ((uint32_t)(quad * 32) << 16);
-            if (half_rope) {
+            if (p.partial) {
+                // Split-K: raw fp32 partial sums; the reduce kernel applies the epilogue.
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r0[32];
+                    ptx::tmem_ld32(tbase + c, r0);
+                    ptx::tmem_ld_wait();
+                    const int n0 = nt * BN + c;
+                    if (m < p.M && n0 < p.N) {
+                        float *dst = p.partial + ((int64_t)ks * p.M + m) * p.N + n0;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(dst + i) =
+                                make_float4(__uint_as_float(r0[i]), __uint_as_float(r0[i + 1]),
+                                            __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
+                    }
+                }
+            } else if (half_rope) {
                 for (int c = 0; c < BN; c += 64) {
                     uint32_t r0[32], r1[32];
                     ptx::tmem_ld32(tbase + c, r0);
@@ -278,6 +304,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_dealloc(tmem, C::kTmemCols);
     }
     if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, kStatusTimeout);
+}
+
+// Sum of the split-K partials of one NC-column chunk of one row, then the
+// usual epilogue (RoPE, cache scatter, conversion).
+template <int NC>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(TcGemmParams p)
+{
+    const int chunks = p.N / NC;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)p.M * chunks) return;
+    const int m = (int)(i / chunks), n0 = (int)(i % chunks) * NC;
+    float v[64];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) v[j] = 0.f;
+    for (int ks = 0; ks < p.splits; ++ks) {
+        const float4 *src = reinterpret_cast<const float4 *>(p.partial + ((int64_t)ks * p.M + m) * p.N + n0);
+#pragma unroll
+        for (int j = 0; j < NC / 4; ++j) {
+            const float4 w = src[j];
+            v[4 * j] += w.x;
+            v[4 * j + 1] += w.y;
+            v[4 * j + 2] += w.z;
+            v[4 * j + 3] += w.w;
+        }
+    }
+    store_chunk<NC>(p, 0, m, n0, v);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
@@ -327,8 +379,56 @@ bool gemm_tc_supported(const GemmArgs &a)
     return true;
 }
 
+// Tile width and K split: large GEMMs take the widest tile that still gives
+// every SM a tile; skinny ones (few output tiles, e.g. one decode token per
+// sequence) split K so that the work units fill whole waves of SMs.
+GemmPlan gemm_tc_plan(const GemmArgs &a, int num_sms)
+{
+    auto tiles = [&](int bn) { return ((a.M + kBM - 1) / kBM) * ((a.N + bn - 1) / bn) * a.batch; };
+    GemmPlan pl;
+    pl.bn = 64;
+    if (a.N % 256 == 0 && tiles(256) >= num_sms) pl.bn = 256;
+    else if (a.N % 128 == 0 && tiles(128) >= num_sms) pl.bn = 128;
+    pl.splits = 1;
+    const int nk = (a.K + kBK - 1) / kBK;
+    const int t64 = tiles(64);
+    if (t64 < num_sms && a.batch == 1 && a.epi.batch_stride == 0 && nk >= 2 && !a.trans_b) {
+        // Estimated time ~ bytes moved (weights, plus the fp32 partials written
+        // and read back) / fraction of the SMs kept busy over whole waves.
+        const double wbytes = 2.0 * a.N * a.K + 2.0 * a.M * a.K;
+        auto cost = [&](int units, int sp) {
+            const int waves = (units + num_sms - 1) / num_sms;
+            const double eff = (double)units / ((double)waves * num_sms);
+            return (wbytes + (sp > 1 ? 8.0 * sp * a.M * a.N : 0.0)) / eff;
+        };
+        double best = cost(tiles(pl.bn), 1);
+        for (int bn : {128, 64}) {
+            if (bn == 128 && a.N % 128) continue;
+            const int t = tiles(bn);
+            for (int sp = 2; sp <= std::min(nk, 64); ++sp) {
+                const int kbps = (nk + sp - 1) / sp;
+                const int real = (nk + kbps - 1) / kbps;
+                const double c = cost(t * real, real);
+                if (c < 0.95 * best) {
+                    best = c;
+                    pl.bn = bn;
+                    pl.splits = real;
+                }
+            }
+        }
+    }
+    pl.kb_per_split = (nk + pl.splits - 1) / pl.splits;
+    return pl;
+}
+
+size_t gemm_tc_workspace(const GemmArgs &a, int num_sms)
+{
+    GemmPlan pl = gemm_tc_plan(a, num_sms);
+    return pl.splits > 1 ? (size_t)pl.splits * a.M * a.N * sizeof(float) : 0;
+}
+
 template <int BN, bool kBMN>
-static cudaError_t launch(const GemmArgs &a, int num_sms, cudaStream_t s)
+static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cudaStream_t s)
 {
     using C = Cfg<BN>;
     CUtensorMap ta, tb;
@@ -344,33 +444,44 @@ static cudaError_t launch(const GemmArgs &a, int num_sms, cudaStream_t s)
     p.b_row_batch = a.b_row_batch; p.b_col_batch = a.b_col_batch;
     p.tiles_m = (a.M + kBM - 1) / kBM;
     p.tiles_n = (a.N + BN - 1) / BN;
+    p.splits = pl.splits;
+    p.kb_per_split = pl.kb_per_split;
+    p.partial = pl.splits > 1 ? a.split_ws : nullptr;
     p.epi = a.epi;
     p.status = a.epi.status;
-    const int tiles = p.tiles_m * p.tiles_n * a.batch;
+    if (pl.splits > 1 && !a.split_ws) return cudaErrorInvalidValue;
+    const int units = p.tiles_m * p.tiles_n * a.batch * p.splits;
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmem);
     if (e != cudaSuccess) return e;
-    gemm_tc_kernel<BN, kBMN><<<std::min(tiles, num_sms), kThreads, C::kSmem, s>>>(ta, tb, p);
+    gemm_tc_kernel<BN, kBMN><<<std::min(units, num_sms), kThreads, C::kSmem, s>>>(ta, tb, p);
     note_launch();
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (pl.splits > 1) {
+        const int nc = a.epi.rope_mode == kRopeHalf ? 64 : 32;
+        const int64_t threads = (int64_t)a.M * (a.N / nc);
+        const unsigned blocks = (unsigned)((threads + 255) / 256);
+        if (nc == 64) splitk_reduce_kernel<64><<<blocks, 256, 0, s>>>(p);
+        else splitk_reduce_kernel<32><<<blocks, 256, 0, s>>>(p);
+        note_launch();
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 cudaError_t gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t s)
 {
     if (a.M == 0 || a.N == 0 || a.batch == 0) return cudaSuccess;
     if (!gemm_tc_supported(a)) return cudaErrorInvalidValue;
-    auto tiles = [&](int bn) { return ((a.M + kBM - 1) / kBM) * ((a.N + bn - 1) / bn) * a.batch; };
-    int bn = 64;
-    if (a.N % 256 == 0 && tiles(256) >= num_sms) bn = 256;
-    else if (a.N % 128 == 0 && tiles(128) >= num_sms) bn = 128;
+    const GemmPlan pl = gemm_tc_plan(a, num_sms);
     if (a.trans_b) {
-        if (bn == 256) return launch<256, true>(a, num_sms, s);
-        if (bn == 128) return launch<128, true>(a, num_sms, s);
-        return launch<64, true>(a, num_sms, s);
+        if (pl.bn == 256) return launch<256, true>(a, pl, num_sms, s);
+        if (pl.bn == 128) return launch<128, true>(a, pl, num_sms, s);
+        return launch<64, true>(a, pl, num_sms, s);
     }
-    if (bn == 256) return launch<256, false>(a, num_sms, s);
-    if (bn == 128) return launch<128, false>(a, num_sms, s);
-    return launch<64, false>(a, num_sms, s);
+    if (pl.bn == 256) return launch<256, false>(a, pl, num_sms, s);
+    if (pl.bn == 128) return launch<128, false>(a, pl, num_sms, s);
+    return launch<64, false>(a, pl, num_sms, s);
 }
 
 }  // namespace mla

@@ -88,6 +88,11 @@ struct GemmArgs {
     bool trans_b = false;
     int M = 0, N = 0, K = 0, batch = 1;
     Epilogue epi;
+    float *split_ws = nullptr;  // tensor-core split-K partials (gemm_tc_workspace bytes)
+};
+
+struct GemmPlan {
+    int bn, splits, kb_per_split;
 };
 
 // CUDA-core kernels (the float32 path).
@@ -97,6 +102,8 @@ cudaError_t gemm_simt(int dtype, const GemmArgs &a, cudaStream_t s);
 // gemm_tc_supported(): 16-byte aligned views and row strides, N % 32 == 0,
 // batch offsets on 16-byte boundaries, output rows 16-byte aligned.
 bool gemm_tc_supported(const GemmArgs &a);
+GemmPlan gemm_tc_plan(const GemmArgs &a, int num_sms);
+size_t gemm_tc_workspace(const GemmArgs &a, int num_sms);  // split-K scratch bytes (0: none)
 cudaError_t gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t s);
 
 struct DecodeArgs {

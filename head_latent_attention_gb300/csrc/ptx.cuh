@@ -78,6 +78,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of a phase (try_wait may suspend the thread for a while,
+// which a loop polling several barriers must not do).
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity)
 {
     uint32_t ok;

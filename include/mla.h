@@ -184,9 +184,10 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope,
                       size_t ws_bytes, void *stream);
 
 /* Output projection y = W_O [o_1 ‖ ... ‖ o_H] (deepseek-mla output_proj;
- * out_proj in mla_attn / mlra_attn).  o [T, H*d_v], y [T, d_model]. */
+ * out_proj in mla_attn / mlra_attn).  o [T, H*d_v], y [T, d_model].  The
+ * workspace holds split-K partial sums when T is small (decode). */
 mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int64_t T,
-                        void *y, void *stream);
+                        void *y, void *ws, size_t ws_bytes, void *stream);
 
 /* Synchronise `stream`, read and clear the status words of the workspace
  * (ws may be NULL) and of the handle (used by calls without a workspace).

@@ -109,7 +109,7 @@ def test_null_handle_paths(lib):
                          None) == lib.MLA_ERR_INVALID_ARG
     assert L.mla_decode(None, None, None, None, None, None, 1, None, None, 0,
                         None) == lib.MLA_ERR_INVALID_ARG
-    assert L.mla_out_proj(None, None, None, 1, None, None) == lib.MLA_ERR_INVALID_ARG
+    assert L.mla_out_proj(None, None, None, 1, None, None, 0, None) == lib.MLA_ERR_INVALID_ARG
     L.mla_destroy(None)
 
 
