@@ -19,15 +19,25 @@ static cudaEvent_t g_prof_end[MLA_PROFILE_COUNT] = {};
 
 void note_launch(int n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
 
-void profile_begin(int which, cudaStream_t s)
+// Inside stream capture the record is made external, so that it becomes an
+// event-record node of the graph the caller can time; outside capture it is a
+// plain record.  A failed diagnostic record must not surface as the error of
+// the next launch, so its error state is cleared.
+static void profile_record(cudaEvent_t ev, cudaStream_t s)
 {
-    if (g_prof_begin[which]) cudaEventRecord(g_prof_begin[which], s);
+    if (!ev) return;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        e = cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    else
+        e = cudaEventRecord(ev, s);
+    if (e != cudaSuccess) (void)cudaGetLastError();
 }
 
-void profile_end(int which, cudaStream_t s)
-{
-    if (g_prof_end[which]) cudaEventRecord(g_prof_end[which], s);
-}
+void profile_begin(int which, cudaStream_t s) { profile_record(g_prof_begin[which], s); }
+
+void profile_end(int which, cudaStream_t s) { profile_record(g_prof_end[which], s); }
 
 }  // namespace mla
 

@@ -7,23 +7,25 @@
 // 128 heads x 512 latent columns is exactly one SM's tensor memory, so a
 // cluster of two CTAs splits the columns: CTA r owns latent columns
 // [256 r, 256 r + 256) and rope columns [32 r, 32 r + 32).  Each CTA
-//   - streams only its own columns of each 64-key tile (TMA; 128-byte swizzle
-//     for the latent, 64-byte swizzle for the 32 rope columns);
-//   - computes a partial score tile S_r = Q_r K_r^T (M = 128 heads, N = 64
+//   - keeps its 288 query columns in tensor memory (the A operand of QK^T),
+//     leaving shared memory to a 6-stage ring of 48-key tiles of its own
+//     cache columns (TMA; 128-byte swizzle for the latent, 64-byte for rope);
+//   - computes a partial score tile S_r = Q_r K_r^T (M = 128 heads, N = 48
 //     keys, K = 288) into tensor memory;
 //   - sends S_r to the peer with st.async, each store completing bytes on the
-//     peer's mbarrier (no per-thread fences), and adds the peer's partial in
-//     the same order on both sides, so both CTAs take bit-identical softmax
-//     decisions;
-//   - writes P (bfloat16) back into tensor memory over its scores and
-//     accumulates O_r += P V_r (A from tensor memory, V read as an MN-major
-//     operand from the same shared-memory tile; M = 128, N = 256, K = 64).
-// The softmax warps send tile t+1's partial before working on tile t, so the
-// exchange latency hides behind the exponentials.  Warp roles: warp 0 TMA
-// producer (3-stage ring), warp 1 MMA issuer (polls both queues, P.V first),
-// warps 2..5 softmax, one head row per thread.  The running max is raised only
-// when it grows by more than 8 (log2 units), so the O rescale is rare; the
-// result is exact either way because P and the running sum use the same max.
+//     peer's mbarrier (double-buffered, so a send never waits for the peer to
+//     finish the previous tile), and adds the peer's partial in the same
+//     order on both sides, so both CTAs take bit-identical softmax decisions;
+//   - writes P (bfloat16) over its scores in tensor memory and accumulates
+//     O_r += P V_r (A from tensor memory, V read as an MN-major operand from
+//     the same shared-memory tile; M = 128, N = 256, K = 48).
+// The softmax warps send tile t+1's partial before the exponentials of tile
+// t, so the exchange latency hides behind them.  Warp roles: warp 0 TMA
+// producer, warp 1 MMA issuer (non-blocking polling of both queues, P.V
+// first), warps 2..5 softmax and query loads, one head row per thread.  The
+// running max is raised only when it grows by more than 8 (log2 units), so
+// the O rescale is rare; the result is exact either way because P and the
+// running sum use the same max.
 //
 // Work: the concatenation of all sequences' keys is cut into one contiguous
 // range per cluster (a device-side scheduler computes the prefix sums of the
@@ -41,25 +43,26 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
 namespace {
 
 constexpr int kH = 128;       // heads per CTA = MMA M
-constexpr int kBKV = 64;      // keys per tile
-constexpr int kStages = 3;
+constexpr int kBKV = 48;      // keys per tile
+constexpr int kStages = 6;
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kLA = 4;        // 64-column latent atoms per CTA (r_kv = 512)
 
-// Shared memory (per CTA)
-constexpr int kQLat = kLA * kH * 128;            // 4 latent atoms of the query, 64 KB
-constexpr int kQBytes = kQLat + kH * 64;         // + 32 rope columns (64-byte rows): 72 KB
-constexpr int kAtom = kBKV * 128;                // one 64x64 latent atom of a KV tile
-constexpr int kStageBytes = kLA * kAtom + kBKV * 64;  // + 32 rope columns: 36 KB
-constexpr int kXBytes = kH * 64 * 4;             // peer's partial scores, 32 KB
-constexpr int kOffKV = kQBytes;
-constexpr int kOffX = kOffKV + kStages * kStageBytes;
-constexpr int kOffBar = kOffX + kXBytes;
+// Shared memory (per CTA): the KV ring and two exchange buffers.
+constexpr int kAtom = kBKV * 128;                     // one 48x64 latent atom of a KV tile
+constexpr int kStageBytes = kLA * kAtom + kBKV * 64;  // + 32 rope columns (64-byte rows)
+constexpr int kXStride = 52;                          // floats per exchange row (conflict-free v4 rows)
+constexpr int kXBytes = kH * kXStride * 4;
+constexpr uint32_t kXTx = kH * kBKV * 4;              // bytes one exchange delivers
+constexpr int kOffX = kStages * kStageBytes;
+constexpr int kOffBar = kOffX + 2 * kXBytes;
 constexpr int kSmem = kOffBar + 256 + 1024;
-// Tensor memory: O in columns [0, 256), score / P buffers at 256 and 320.
+// Tensor memory: O in [0, 256), the query (288 bf16 = 144 columns) in
+// [256, 400), score / P buffers at 400 and 448.
 constexpr int kOCols = kLA * 64;
-constexpr int kSCol = 256;
+constexpr int kQCol = 256;
+constexpr int kSCol = 400;
 constexpr int kRLat = 2 * kLA * 64;
 
 struct DecTcParams {
@@ -78,7 +81,7 @@ struct Bars {
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[2];
     uint64_t p_full, pv_done, o_empty;
-    uint64_t x_full, x_free;
+    uint64_t x_full[2], x_free[2];
     int abort;
     uint32_t tmem;
 };
@@ -205,15 +208,13 @@ struct TileCursor {
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQR,
-                     const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmR,
-                     DecTcParams p)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmR,
+                     const bf16 *__restrict__ q_abs, const bf16 *__restrict__ q_rope, DecTcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sQ = smem;
-    uint8_t *sKV = smem + kOffKV;
-    uint8_t *sX = smem + kOffX;
+    uint8_t *sKV = smem;
+    float *sX = (float *)(smem + kOffX);
     Bars *bar = (Bars *)(smem + kOffBar);
     volatile int *abort_flag = &bar->abort;
 
@@ -222,21 +223,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar->q_full, 1);
+        ptx::mbar_init(&bar->q_full, kH);
         ptx::mbar_init(&bar->q_empty, 1);
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&bar->kv_full[i], 1);
             ptx::mbar_init(&bar->kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) ptx::mbar_init(&bar->s_full[i], 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&bar->s_full[i], 1);
+            ptx::mbar_init(&bar->x_full[i], 1);
+            ptx::mbar_init(&bar->x_free[i], 1);
+        }
         ptx::mbar_init(&bar->p_full, kH);
         ptx::mbar_init(&bar->pv_done, 1);
         ptx::mbar_init(&bar->o_empty, kH);
-        ptx::mbar_init(&bar->x_full, 1);
-        ptx::mbar_init(&bar->x_free, 1);
         bar->abort = 0;
         ptx::fence_mbar_init();
-        ptx::mbar_expect_tx(&bar->x_full, kXBytes);  // arm the first exchange
+        for (int i = 0; i < 2; ++i) ptx::mbar_expect_tx(&bar->x_full[i], kXTx);  // arm both buffers
     }
     if (warp == 1) ptx::tmem_alloc(&bar->tmem, 512);
     ptx::tc_fence_before();
@@ -254,27 +257,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (ptx::elect_one()) {
-            ptx::prefetch_tmap(&tmQ);
-            ptx::prefetch_tmap(&tmQR);
             ptx::prefetch_tmap(&tmL);
             ptx::prefetch_tmap(&tmR);
-            const uint64_t keep = ptx::policy_evict_last(), stream = ptx::policy_evict_first();
+            const uint64_t stream = ptx::policy_evict_first();
             SegIter it;
             it.init(p.prefix, p.B, cid, chunk);
             int b, k0, k1;
             bool whole;
-            int nseg = 0, g = 0;
-            int pending[kStages] = {-1, -1, -1};
-            int q_pending = -1;
+            int g = 0;
+            int pending[kStages];
+#pragma unroll
+            for (int i = 0; i < kStages; ++i) pending[i] = -1;
             while (ok && it.next(b, k0, k1, whole)) {
-                if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) { fail(); break; }
-                ptx::mbar_expect_tx(&bar->q_full, kQBytes);
-                for (int a = 0; a < kLA; ++a)
-                    ptx::tma_load_2d_hint(sQ + a * kH * 128, &tmQ, &bar->q_full, (int)rank * kLA * 64 + a * 64,
-                                          b * p.H, keep);
-                ptx::tma_load_2d_hint(sQ + kQLat, &tmQR, &bar->q_full, (int)rank * 32, b * p.H, keep);
-                q_pending = nseg & 1;
-                ++nseg;
                 const int ntiles = (k1 - k0 + kBKV - 1) / kBKV;
                 for (int t = 0; t < ntiles; ++t, ++g) {
                     const int st = g % kStages;
@@ -291,7 +285,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             volatile int never = 0;
-            if (q_pending >= 0) ptx::mbar_wait(&bar->q_full, (uint32_t)q_pending, &never);
             for (int i = 0; i < kStages; ++i)
                 if (pending[i] >= 0) ptx::mbar_wait(&bar->kv_full[i], (uint32_t)pending[i], &never);
         }
@@ -302,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ready, P.V first (it frees a KV stage for the next load).
             constexpr uint32_t idesc_s = ptx::idesc_bf16(kH, kBKV, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, kLA * 64, false, true);
-            const uint32_t q0 = ptx::smem_u32(sQ), kv0 = ptx::smem_u32(sKV);
+            const uint32_t kv0 = ptx::smem_u32(sKV);
             TileCursor qk, pv;
             qk.init(p.prefix, p.B, cid, chunk);
             pv.init(p.prefix, p.B, cid, chunk);
@@ -338,18 +331,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_fence_after();
                         const uint32_t kb = kv0 + st * kStageBytes;
                         const uint32_t d = tmem + kSCol + (qk.g & 1) * kBKV;
+                        // K steps 0..15: latent atoms (128-byte swizzle); 16..17: rope (64-byte).
 #pragma unroll
-                        for (int a = 0; a < kLA; ++a) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                ptx::mma_bf16(d, ptx::sdesc_sw128(q0 + a * kH * 128 + k * 32, 16, 1024),
-                                              ptx::sdesc_sw128(kb + a * kAtom + k * 32, 16, 1024), idesc_s,
-                                              (a | k) != 0);
-                        }
+                        for (int k = 0; k < 16; ++k)
+                            ptx::mma_f16_tmem_a(d, tmem + kQCol + k * 8,
+                                                ptx::sdesc_sw128(kb + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
+                                                idesc_s, k != 0);
 #pragma unroll
                         for (int k = 0; k < 2; ++k)
-                            ptx::mma_bf16(d, ptx::sdesc_sw64(q0 + kQLat + k * 32, 512),
-                                          ptx::sdesc_sw64(kb + kLA * kAtom + k * 32, 512), idesc_s, 1u);
+                            ptx::mma_f16_tmem_a(d, tmem + kQCol + (16 + k) * 8,
+                                                ptx::sdesc_sw64(kb + kLA * kAtom + k * 32, 512), idesc_s, 1u);
                         ptx::mma_commit(&bar->s_full[qk.g & 1]);
                         if (qk.t == qk.ntiles - 1) ptx::mma_commit(&bar->q_empty);
                         qk.step();
@@ -364,42 +355,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp % 4;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const uint32_t peer_xrow = map_peer(sX + h * 256, peer);
-        const uint32_t peer_xfull = map_peer(&bar->x_full, peer);
-        const uint32_t peer_xfree = map_peer(&bar->x_free, peer);
-        const uint8_t *my_xrow = sX + h * 256;
-        // Total tiles of this cluster (the exchange runs one tile ahead,
-        // across segment boundaries).
-        int n_tiles = 0;
-        {
-            SegIter it;
-            it.init(p.prefix, p.B, cid, chunk);
-            int b, k0, k1;
-            bool whole;
-            while (it.next(b, k0, k1, whole)) n_tiles += (k1 - k0 + kBKV - 1) / kBKV;
+        uint32_t peer_xrow[2], peer_xfull[2], peer_xfree[2];
+        for (int i = 0; i < 2; ++i) {
+            peer_xrow[i] = map_peer((const uint8_t *)sX + i * kXBytes + h * kXStride * 4, peer);
+            peer_xfull[i] = map_peer(&bar->x_full[i], peer);
+            peer_xfree[i] = map_peer(&bar->x_free[i], peer);
         }
-        // Read this thread's score row of buffer g & 1 and send it to the
-        // peer (16-byte chunk c of row h goes to chunk c ^ (h & 15)).
-        auto send = [&](int g) -> bool {
-            if (!ptx::mbar_wait(&bar->s_full[g & 1], (g >> 1) & 1, abort_flag)) return false;
+        // This CTA's 288 query columns of row h into tensor memory (lanes =
+        // heads, bf16 pairs per 32-bit column, lower column in the low half,
+        // which is how consecutive bf16 values sit in memory).
+        auto load_q = [&](int b, int nseg) -> bool {
+            if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) return false;
             ptx::tc_fence_after();
-            if (!ptx::mbar_wait_cluster(&bar->x_free, (g & 1) ^ 1, abort_flag)) return false;
+            const bool row_ok = h < p.H;
+            const uint4 *src = reinterpret_cast<const uint4 *>(q_abs + ((int64_t)b * p.H + h) * kRLat + rank * kOCols);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV + half * 32, r);
-                ptx::tmem_ld_wait();
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[32];
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int cc = half * 8 + c;
-                    st_async_v4(peer_xrow + ((cc ^ (h & 15)) << 4), __uint_as_float(r[4 * c]),
-                                __uint_as_float(r[4 * c + 1]), __uint_as_float(r[4 * c + 2]),
-                                __uint_as_float(r[4 * c + 3]), peer_xfull);
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 v = row_ok ? src[c * 8 + i] : make_uint4(0, 0, 0, 0);
+                    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
                 }
+                ptx::tmem_st32(tmem + lane_off + kQCol + c * 32, w);
             }
+            const uint4 *rs = reinterpret_cast<const uint4 *>(q_rope + ((int64_t)b * p.H + h) * 64 + rank * 32);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 v = row_ok ? rs[i] : make_uint4(0, 0, 0, 0);
+                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+            }
+            ptx::tmem_st16(tmem + lane_off + kQCol + 128, w);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar->q_full);
             return true;
         };
-        if (n_tiles > 0 && !send(0)) fail();
+        // Read this thread's score row of buffer g & 1 and send it into the
+        // peer's exchange buffer g & 1.
+        auto send = [&](int g) -> bool {
+            if (!ptx::mbar_wait(&bar->s_full[g & 1], (g >> 1) & 1, abort_flag)) return false;
+            if (!ptx::mbar_wait_cluster(&bar->x_free[g & 1], ((g >> 1) & 1) ^ 1, abort_flag)) return false;
+            ptx::tc_fence_after();
+            uint32_t r0[32], r1[16];
+            ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV, r0);
+            ptx::tmem_ld16(tmem + lane_off + kSCol + (g & 1) * kBKV + 32, r1);
+            ptx::tmem_ld_wait();
+            const uint32_t dst = peer_xrow[g & 1], xb = peer_xfull[g & 1];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                st_async_v4(dst + c * 16, __uint_as_float(r0[4 * c]), __uint_as_float(r0[4 * c + 1]),
+                            __uint_as_float(r0[4 * c + 2]), __uint_as_float(r0[4 * c + 3]), xb);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                st_async_v4(dst + (8 + c) * 16, __uint_as_float(r1[4 * c]), __uint_as_float(r1[4 * c + 1]),
+                            __uint_as_float(r1[4 * c + 2]), __uint_as_float(r1[4 * c + 3]), xb);
+            return true;
+        };
+        TileCursor nx;  // the tile after the current one (the send runs one tile ahead)
+        nx.init(p.prefix, p.B, cid, chunk);
+        if (nx.valid) {
+            if (!load_q(nx.b, 0) || !send(0)) fail();
+            nx.step();
+        }
         SegIter it;
         it.init(p.prefix, p.B, cid, chunk);
         int b, k0, k1;
@@ -411,18 +430,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ntiles = (len + kBKV - 1) / kBKV;
             for (int t = 0; t < ntiles; ++t, ++g) {
                 const int valid = min(kBKV, len - t * kBKV);
+                const int xb = g & 1;
                 // 1. Full scores of tile g: own partial (still in tensor
                 //    memory) plus the peer's, same operand order in both CTAs.
-                if (!ptx::mbar_wait_cluster(&bar->x_full, g & 1, abort_flag)) { fail(); break; }
-                float s[64];
+                if (!ptx::mbar_wait_cluster(&bar->x_full[xb], (g >> 1) & 1, abort_flag)) { fail(); break; }
+                float s[kBKV];
                 {
-                    uint32_t r0[32], r1[32];
-                    ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV, r0);
-                    ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV + 32, r1);
+                    uint32_t r0[32], r1[16];
+                    ptx::tmem_ld32(tmem + lane_off + kSCol + xb * kBKV, r0);
+                    ptx::tmem_ld16(tmem + lane_off + kSCol + xb * kBKV + 32, r1);
                     ptx::tmem_ld_wait();
+                    const float *xr = sX + xb * (kXBytes / 4) + h * kXStride;
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const float4 v = *reinterpret_cast<const float4 *>(my_xrow + ((c ^ (h & 15)) << 4));
+                    for (int c = 0; c < kBKV / 4; ++c) {
+                        const float4 v = *reinterpret_cast<const float4 *>(xr + 4 * c);
                         const uint32_t *rr = c < 8 ? &r0[4 * c] : &r1[4 * (c - 8)];
                         const float o0 = __uint_as_float(rr[0]), o1 = __uint_as_float(rr[1]);
                         const float o2 = __uint_as_float(rr[2]), o3 = __uint_as_float(rr[3]);
@@ -433,17 +454,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                softmax_bar();  // every row of the exchange buffer has been read
+                softmax_bar();  // every row of exchange buffer xb has been read
                 if (h == 0) {
-                    ptx::mbar_expect_tx(&bar->x_full, kXBytes);  // arm the next exchange
-                    arrive_remote(peer_xfree);                   // the peer may overwrite it
+                    ptx::mbar_expect_tx(&bar->x_full[xb], kXTx);  // arm its next use (tile g + 2)
+                    arrive_remote(peer_xfree[xb]);                // the peer may overwrite it
                 }
-                // 2. Send the next tile's partial before the exponentials.
-                if (g + 1 < n_tiles && !send(g + 1)) { fail(); break; }
+                // 2. The next tile: its query (at a segment boundary) and its partial.
+                if (nx.valid) {
+                    if (nx.t == 0 && !load_q(nx.b, nx.nseg)) { fail(); break; }
+                    if (!send(g + 1)) { fail(); break; }
+                    nx.step();
+                }
                 // 3. Online softmax of tile g.
                 float mt = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
+                for (int j = 0; j < kBKV; ++j) {
                     s[j] = (j < valid) ? s[j] * p.scale_log2 : -INFINITY;
                     mt = fmaxf(mt, s[j]);
                 }
@@ -451,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_new = resc ? mt : m_run;
                 const float corr = exp2f(m_run - m_new);
                 float psum = 0.f;
-                uint32_t pk[32];
+                uint32_t pk[kBKV / 2];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < kBKV / 2; ++j) {
                     const float a0 = exp2f(s[2 * j] - m_new), a1 = exp2f(s[2 * j + 1] - m_new);
                     psum += a0 + a1;
                     pk[j] = ptx::pack_bf16(a0, a1);
@@ -477,8 +502,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_st32(tmem + lane_off + c, o);
                     }
                 }
-                // P over the scores of this tile (columns 0..31 of the buffer).
-                ptx::tmem_st32(tmem + lane_off + kSCol + (g & 1) * kBKV, pk);
+                // P over the scores of this tile (columns 0..23 of the buffer).
+                ptx::tmem_st16(tmem + lane_off + kSCol + xb * kBKV, pk);
+                ptx::tmem_st8(tmem + lane_off + kSCol + xb * kBKV + 16, pk + 16);
                 ptx::tmem_st_wait();
                 if (valid < kBKV) {
                     // Rows past the segment may hold arbitrary cache contents;
@@ -632,12 +658,9 @@ __global__ void __launch_bounds__(128) decode_combine_tc_kernel(const int *prefi
 
 cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
 {
-    CUtensorMap tq, tqr, tl, tr;
-    const int64_t q_rows = (int64_t)a.B * a.H;
+    CUtensorMap tl, tr;
     const int64_t c_rows = (int64_t)a.max_batch * a.max_seq;
-    if (!make_tmap_bf16(&tq, a.q_abs, q_rows, kRLat, kRLat, 64, kH) ||
-        !make_tmap_bf16(&tqr, a.q_rope, q_rows, 64, 64, 32, kH) ||
-        !make_tmap_bf16(&tl, a.lat, c_rows, kRLat, a.lat_stride, 64, kBKV) ||
+    if (!make_tmap_bf16(&tl, a.lat, c_rows, kRLat, a.lat_stride, 64, kBKV) ||
         !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV))
         return cudaErrorInvalidValue;
     decode_schedule_kernel<<<1, 1024, 0, s>>>(a.seq_lens, a.B, a.max_seq, a.n_clusters, a.prefix, a.chunk,
@@ -645,7 +668,8 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     note_launch();
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    static int smem_dev = -1;
+    e = smem_limit_once(smem_dev, (const void *)decode_tc_kernel, kSmem);
     if (e != cudaSuccess) return e;
     DecTcParams p;
     p.B = a.B; p.H = a.H; p.max_seq = a.max_seq;
@@ -668,7 +692,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     profile_begin(MLA_PROFILE_DECODE_ATTENTION, s);
-    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tq, tqr, tl, tr, p);
+    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tl, tr, (const bf16 *)a.q_abs, (const bf16 *)a.q_rope, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
     if (e != cudaSuccess) return e;

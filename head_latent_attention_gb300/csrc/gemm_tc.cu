@@ -451,8 +451,8 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     p.status = a.epi.status;
     if (pl.splits > 1 && !a.split_ws) return cudaErrorInvalidValue;
     const int units = p.tiles_m * p.tiles_n * a.batch * p.splits;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<BN, kBMN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+    static int smem_dev = -1;
+    cudaError_t e = smem_limit_once(smem_dev, (const void *)gemm_tc_kernel<BN, kBMN>, C::kSmem);
     if (e != cudaSuccess) return e;
     gemm_tc_kernel<BN, kBMN><<<std::min(units, num_sms), kThreads, C::kSmem, s>>>(ta, tb, p);
     note_launch();

@@ -24,6 +24,20 @@ void note_launch(int n = 1);
 void profile_begin(int which, cudaStream_t s);
 void profile_end(int which, cudaStream_t s);
 
+// Raise a kernel's dynamic shared-memory limit once per device (call site
+// keeps `set_on_device`, initially -1): the attribute need not be set per
+// launch, and setting it only once keeps launches cheap and capturable.
+inline cudaError_t smem_limit_once(int &set_on_device, const void *func, int bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (set_on_device == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) set_on_device = dev;
+    return e;
+}
+
 // Workspace status bits (mirrors the values documented in mla.h).
 constexpr uint32_t kStatusPos = 1u;
 constexpr uint32_t kStatusSeq = 2u;

@@ -1,23 +1,26 @@
 // Causal flash-style prefill attention on tcgen05 (fp16 operands, fp32 softmax).
 //
-// One CTA per (128-query tile, head, sequence); tiles with more keys launch
-// first.  Per 64-key tile:
-//   S = Q K^T        tcgen05.mma M=128 (queries), N=64 (keys), K=d_qk, into
-//                    one of two tensor-memory score buffers;
-//   softmax          4 warps, one query row per thread: scale, causal mask
-//                    (key j <= query position), online max with a lazy
-//                    rescale (only when the max grows by more than 8 in log2
-//                    units), exp2, fp16 P into a 128-byte-swizzled tile;
-//   O += P V         tcgen05.mma M=128, N=d_v, K=64 with V read as an
-//                    MN-major operand straight from its TMA tile.
-// Warp 0 streams K and V tiles with TMA into a 3-stage ring, warp 1 issues
-// the MMAs (the next tile's QK^T overlaps the current softmax).  For the
-// decoupled variant the key is [k_C ‖ k_R (shared by all heads)] and the
-// query [q_nope ‖ q_rope].
+// One CTA per (pair of adjacent 128-query tiles, head, sequence); pairs with
+// more keys launch first.  The two query tiles share every 64-key K/V tile
+// (3-stage TMA ring) and have their own softmax warpgroup, so while one
+// warpgroup turns scores into probabilities the tensor pipe runs the other
+// tile's QK^T or P.V.  Per query tile q and key tile j:
+//   S_q = Q_q K_j^T   tcgen05.mma M=128, N=64, K=d_qk into one of two
+//                     tensor-memory score buffers of tile q;
+//   softmax           one query row per thread: scale, causal mask (key <=
+//                     query position), online max with a lazy rescale (only
+//                     when the max grows by more than 8 in log2 units), exp2;
+//                     P (fp16) is written back over its scores in tensor memory;
+//   O_q += P V_j      tcgen05.mma with A = P from tensor memory and V read as
+//                     an MN-major operand from its TMA tile (M=128, N=d_v).
+// Warp 0 is the TMA producer, warp 1 issues the MMAs (non-blocking polling of
+// both tiles' queues), warps 2..5 and 6..9 are the two softmax warpgroups.
+// For the decoupled variant the key is [k_C ‖ k_R (shared by all heads)] and
+// the query [q_nope ‖ q_rope].
 // Both contractions run in fp16 (same tensor-core rate as bfloat16, 8x finer
-// rounding): K and V come from an fp16 workspace, the bfloat16 query tile is
-// converted to fp16 in shared memory after its load (exact for |q| in fp16's
-// normal range), and P is stored as fp16 (values in [0, 256]).
+// rounding): K and V come from an fp16 workspace, the bfloat16 query tiles are
+// converted to fp16 in shared memory after their load (exact for |q| in fp16's
+// normal range), and P is fp16 (values in [0, 256]).
 #include "mla_internal.cuh"
 #include "ptx.cuh"
 
@@ -31,28 +34,27 @@ namespace {
 constexpr int kQ = 128;
 constexpr int kBN = 64;
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.f;
 
 template <int NQ, int NV>  // 64-column atoms of q/k (NQ) and of v (NV)
 struct PCfg {
-    static constexpr int kQBytes = NQ * kQ * 128;
+    static constexpr int kQBytes = NQ * kQ * 128;  // one query tile
     static constexpr int kAtom = kBN * 128;
     static constexpr int kStageBytes = (NQ + NV) * kAtom;
-    static constexpr int kPBytes = kQ * 128;
-    static constexpr int kOffKV = kQBytes;
-    static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
-    static constexpr int kSmem = kOffBar + 256 + 1024;
-    static constexpr int kOCols = NV * 64;
-    static constexpr int kSCol = 128;
-    static constexpr int kTmem = 256;
+    static constexpr int kOffKV = 2 * kQBytes;
+    static constexpr int kOffBar = kOffKV + kStages * kStageBytes;
+    static constexpr int kSmem = kOffBar + 512 + 1024;
+    // Tensor memory: O_0 at 0, O_1 at 128, score/P buffers (tile q, buffer i)
+    // at 256 + 64 (2q + i).
+    static constexpr int kOCol = 128;
+    static constexpr int kSCol = 256;
 };
 
 struct PreTcParams {
     int B, S, H, max_seq, d_nope;
     int64_t kv_rows;
-    bool rope;                 // decoupled: last q/k atom from q_rope / rope cache
+    bool rope;                 // decoupled: last q/k atom from q_rope / rope keys
     const int32_t *start_pos;  // device [B]
     float scale_log2;
     bf16 *o;                   // [B, S, H, d_v]
@@ -61,10 +63,10 @@ struct PreTcParams {
 };
 
 struct PBars {
-    uint64_t q_full, q_ready;
+    uint64_t q_full[2], q_ready[2];
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2], s_empty[2];
-    uint64_t p_full, pv_done;
+    uint64_t s_full[2][2];
+    uint64_t p_full[2], pv_done[2];
     int abort;
     uint32_t tmem;
 };
@@ -78,40 +80,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = PCfg<NQ, NV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sQ = smem;
     uint8_t *sKV = smem + C::kOffKV;
-    uint8_t *sP = smem + C::kOffP;
     PBars *bar = (PBars *)(smem + C::kOffBar);
     volatile int *abort_flag = &bar->abort;
 
     const int n_qt = (p.S + kQ - 1) / kQ;
-    const int qt = n_qt - 1 - (int)blockIdx.x;  // longest tiles first
+    const int n_pairs = (n_qt + 1) / 2;
+    const int pi = n_pairs - 1 - (int)blockIdx.x;  // longest pairs first
     const int h = blockIdx.y, b = blockIdx.z;
-    const int q0 = qt * kQ;
-    const int nq = min(kQ, p.S - q0);
     const int sp = p.start_pos[b];
-    const int last_key = sp + q0 + nq - 1;  // keys 0..last_key are visible to some row
-    const int n_kt = last_key / kBN + 1;
+    // Query tile q of this CTA covers rows [q0[q], q0[q] + nq[q]); nq = 0 if absent.
+    int q0[2], nq[2], n_kt[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        q0[q] = (2 * pi + q) * kQ;
+        nq[q] = max(0, min(kQ, p.S - q0[q]));
+        n_kt[q] = nq[q] > 0 ? (sp + q0[q] + nq[q] - 1) / kBN + 1 : 0;
+    }
+    const int n_kt_all = max(n_kt[0], n_kt[1]);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int nk_nope = p.rope ? NQ - 1 : NQ;  // q/k atoms from q_nope / the key workspace
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar->q_full, 1);
-        ptx::mbar_init(&bar->q_ready, kQ);
+        for (int q = 0; q < 2; ++q) {
+            ptx::mbar_init(&bar->q_full[q], 1);
+            ptx::mbar_init(&bar->q_ready[q], kQ);
+            ptx::mbar_init(&bar->p_full[q], kQ);
+            ptx::mbar_init(&bar->pv_done[q], 1);
+            for (int i = 0; i < 2; ++i) ptx::mbar_init(&bar->s_full[q][i], 1);
+        }
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&bar->kv_full[i], 1);
             ptx::mbar_init(&bar->kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&bar->s_full[i], 1);
-            ptx::mbar_init(&bar->s_empty[i], kQ);
-        }
-        ptx::mbar_init(&bar->p_full, kQ);
-        ptx::mbar_init(&bar->pv_done, 1);
         bar->abort = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 1) ptx::tmem_alloc(&bar->tmem, C::kTmem);
+    if (warp == 1) ptx::tmem_alloc(&bar->tmem, 512);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -127,13 +132,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::prefetch_tmap(&tQR);
                 ptx::prefetch_tmap(&tKR);
             }
-            const int qrow = b * p.S + q0;
-            ptx::mbar_expect_tx(&bar->q_full, NQ * kQ * 128);
-            for (int a = 0; a < nk_nope; ++a)
-                ptx::tma_load_2d(sQ + a * kQ * 128, &tQ, &bar->q_full, h * p.d_nope + a * 64, qrow);
-            if (p.rope) ptx::tma_load_2d(sQ + (NQ - 1) * kQ * 128, &tQR, &bar->q_full, h * 64, qrow);
+            bool q_pending[2] = {false, false};
+            for (int q = 0; q < 2; ++q) {
+                if (nq[q] == 0) continue;
+                uint8_t *dq = smem + q * C::kQBytes;
+                const int qrow = b * p.S + q0[q];
+                ptx::mbar_expect_tx(&bar->q_full[q], C::kQBytes);
+                for (int a = 0; a < nk_nope; ++a)
+                    ptx::tma_load_2d(dq + a * kQ * 128, &tQ, &bar->q_full[q], h * p.d_nope + a * 64, qrow);
+                if (p.rope) ptx::tma_load_2d(dq + (NQ - 1) * kQ * 128, &tQR, &bar->q_full[q], h * 64, qrow);
+                q_pending[q] = true;
+            }
             int pending[kStages] = {-1, -1, -1};
-            for (int t = 0; t < n_kt; ++t) {
+            for (int t = 0; t < n_kt_all; ++t) {
                 const int st = t % kStages;
                 const uint32_t ph = (t / kStages) & 1;
                 if (!ptx::mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag)) { ok = false; break; }
@@ -149,89 +160,115 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) *abort_flag = 1;
             volatile int never = 0;
-            ptx::mbar_wait(&bar->q_full, 0, &never);
+            for (int q = 0; q < 2; ++q)
+                if (q_pending[q]) ptx::mbar_wait(&bar->q_full[q], 0, &never);
             for (int i = 0; i < kStages; ++i)
                 if (pending[i] >= 0) ptx::mbar_wait(&bar->kv_full[i], (uint32_t)pending[i], &never);
         }
     } else if (warp == 1) {
         if (ptx::elect_one()) {
+            // Four queues: QK^T and P.V of each query tile, issued as soon as
+            // ready (test_wait polling, P.V first).  QK^T(q, j) overwrites the
+            // buffer of P(q, j - 2): P.V(q, j - 2) must have been issued (the
+            // tensor pipe keeps order).  The key tile's stage is released with
+            // the last P.V that reads it (tile 1 reads every key tile tile 0 does).
             constexpr uint32_t idesc_s = ptx::idesc_f16(kQ, kBN, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_f16(kQ, NV * 64, false, true);
-            const uint32_t q0a = ptx::smem_u32(sQ), kv0 = ptx::smem_u32(sKV), p0 = ptx::smem_u32(sP);
-            if (!ptx::mbar_wait(&bar->q_ready, 0, abort_flag)) ok = false;
-            for (int t = 0; ok && t <= n_kt; ++t) {
-                if (t < n_kt) {
-                    const int st = t % kStages, sb = t & 1;
-                    if (!ptx::mbar_wait(&bar->kv_full[st], (t / kStages) & 1, abort_flag) ||
-                        !ptx::mbar_wait(&bar->s_empty[sb], ((t >> 1) & 1) ^ 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+            const uint32_t kv0 = ptx::smem_u32(sKV);
+            int qk[2] = {0, 0}, pv[2] = {0, 0};
+            bool qready[2] = {nq[0] == 0, nq[1] == 0};
+            long long last = clock64();
+            while (ok && (pv[0] < n_kt[0] || pv[1] < n_kt[1])) {
+                bool progressed = false;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int j = pv[q];
+                    if (j >= n_kt[q] || j >= qk[q]) continue;
+                    // The stage is released by tile 1's P.V; it must come after tile 0's.
+                    if (q == 1 && j < n_kt[0] && pv[0] <= j) continue;
+                    if (!ptx::mbar_test(ptx::smem_u32(&bar->p_full[q]), j & 1)) continue;
                     ptx::tc_fence_after();
+                    const int st = j % kStages;
+                    const uint32_t vb = kv0 + st * C::kStageBytes + NQ * C::kAtom;
+                    const uint32_t pa = tmem + C::kSCol + (2 * q + (j & 1)) * kBN;
+#pragma unroll
+                    for (int k = 0; k < kBN / 16; ++k)
+                        ptx::mma_f16_tmem_a(tmem + q * C::kOCol, pa + k * 8,
+                                            ptx::sdesc_sw128(vb + k * 2048, C::kAtom, 1024), idesc_o,
+                                            (j > 0 || k > 0) ? 1u : 0u);
+                    ptx::mma_commit(&bar->pv_done[q]);
+                    const bool last_reader = (q == 1) || (j >= n_kt[1]);
+                    if (last_reader) ptx::mma_commit(&bar->kv_empty[st]);
+                    ++pv[q];
+                    progressed = true;
+                }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int j = qk[q];
+                    if (j >= n_kt[q] || pv[q] < j - 1) continue;
+                    if (!qready[q]) {
+                        if (!ptx::mbar_test(ptx::smem_u32(&bar->q_ready[q]), 0)) continue;
+                        qready[q] = true;
+                    }
+                    const int st = j % kStages;
+                    if (!ptx::mbar_test(ptx::smem_u32(&bar->kv_full[st]), (j / kStages) & 1)) continue;
+                    ptx::tc_fence_after();
+                    const uint32_t qa = ptx::smem_u32(smem + q * C::kQBytes);
                     const uint32_t kb = kv0 + st * C::kStageBytes;
+                    const uint32_t d = tmem + C::kSCol + (2 * q + (j & 1)) * kBN;
                     for (int a = 0; a < NQ; ++a) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            ptx::mma_bf16(tmem + C::kSCol + sb * kBN,
-                                          ptx::sdesc_sw128(q0a + a * kQ * 128 + k * 32, 16, 1024),
+                            ptx::mma_bf16(d, ptx::sdesc_sw128(qa + a * kQ * 128 + k * 32, 16, 1024),
                                           ptx::sdesc_sw128(kb + a * C::kAtom + k * 32, 16, 1024), idesc_s,
                                           (a | k) != 0);
                     }
-                    ptx::mma_commit(&bar->s_full[sb]);
+                    ptx::mma_commit(&bar->s_full[q][j & 1]);
+                    ++qk[q];
+                    progressed = true;
                 }
-                if (t > 0) {
-                    const int pt = t - 1, st = pt % kStages;
-                    if (!ptx::mbar_wait(&bar->p_full, pt & 1, abort_flag)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                    const uint32_t vb = kv0 + st * C::kStageBytes + NQ * C::kAtom;
-#pragma unroll
-                    for (int k = 0; k < kBN / 16; ++k)
-                        ptx::mma_bf16(tmem, ptx::sdesc_sw128(p0 + k * 32, 16, 1024),
-                                      ptx::sdesc_sw128(vb + k * 2048, C::kAtom, 1024), idesc_o,
-                                      (pt > 0 || k > 0) ? 1u : 0u);
-                    ptx::mma_commit(&bar->kv_empty[st]);
-                    ptx::mma_commit(&bar->pv_done);
-                }
+                if (progressed) last = clock64();
+                else if (*abort_flag || clock64() - last > ptx::kWaitCycles) ok = false;
             }
             if (!ok) *abort_flag = 1;
         }
     } else {
+        const int q = (warp - 2) / 4;  // query tile of this softmax warpgroup
         const int quad = warp % 4;
         const int r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        const int my_pos = sp + q0 + r;
-        uint8_t *prow = sP + r * 128;
+        const int my_pos = sp + q0[q] + r;
+        uint8_t *sQ = smem + q * C::kQBytes;
         float m_run = -INFINITY, l_run = 0.f;
-        // Query tile: bfloat16 -> fp16 in place (row r of every atom).
-        if (!ptx::mbar_wait(&bar->q_full, 0, abort_flag)) ok = false;
-        if (ok) {
-            for (int a = 0; a < NQ; ++a) {
-                uint4 *row = reinterpret_cast<uint4 *>(sQ + a * kQ * 128 + r * 128);
+        if (nq[q] > 0) {
+            // Query tile: bfloat16 -> fp16 in place (row r of every atom).
+            if (!ptx::mbar_wait(&bar->q_full[q], 0, abort_flag)) ok = false;
+            if (ok) {
+                for (int a = 0; a < NQ; ++a) {
+                    uint4 *row = reinterpret_cast<uint4 *>(sQ + a * kQ * 128 + r * 128);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint4 w = row[j];
-                    w.x = ptx::bf16x2_to_f16x2(w.x);
-                    w.y = ptx::bf16x2_to_f16x2(w.y);
-                    w.z = ptx::bf16x2_to_f16x2(w.z);
-                    w.w = ptx::bf16x2_to_f16x2(w.w);
-                    row[j] = w;
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 w = row[j];
+                        w.x = ptx::bf16x2_to_f16x2(w.x);
+                        w.y = ptx::bf16x2_to_f16x2(w.y);
+                        w.z = ptx::bf16x2_to_f16x2(w.z);
+                        w.w = ptx::bf16x2_to_f16x2(w.w);
+                        row[j] = w;
+                    }
                 }
+                ptx::fence_proxy_async_smem();
+                ptx::mbar_arrive(&bar->q_ready[q]);
             }
-            ptx::fence_proxy_async_smem();
-            ptx::mbar_arrive(&bar->q_ready);
         }
-        for (int t = 0; ok && t < n_kt; ++t) {
-            const int sb = t & 1;
-            if (!ptx::mbar_wait(&bar->s_full[sb], (t >> 1) & 1, abort_flag)) { ok = false; break; }
+        for (int t = 0; ok && t < n_kt[q]; ++t) {
+            const uint32_t sbuf = C::kSCol + (2 * q + (t & 1)) * kBN;
+            if (!ptx::mbar_wait(&bar->s_full[q][t & 1], (t >> 1) & 1, abort_flag)) { ok = false; break; }
             ptx::tc_fence_after();
             uint32_t r0[32], r1[32];
-            ptx::tmem_ld32(tmem + lane_off + C::kSCol + sb * kBN, r0);
-            ptx::tmem_ld32(tmem + lane_off + C::kSCol + sb * kBN + 32, r1);
+            ptx::tmem_ld32(tmem + lane_off + sbuf, r0);
+            ptx::tmem_ld32(tmem + lane_off + sbuf + 32, r1);
             ptx::tmem_ld_wait();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(&bar->s_empty[sb]);
-            const int j0 = t * kBN;
-            const int lim = my_pos - j0;  // keys j0 + j with j <= lim are visible
+            const int lim = my_pos - t * kBN;  // keys t*64 + j with j <= lim are visible
             float s[64];
             float mt = -INFINITY;
 #pragma unroll
@@ -243,8 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < 64; ++j) mt = fmaxf(mt, s[j]);
             const bool resc = mt > m_run + kRescaleThreshold;
             const float m_new = resc ? mt : m_run;
-            // Rows past the sequence end (r >= nq) see no key in later tiles;
-            // keep their state finite.
+            // Rows past the sequence end see no key; keep their state finite.
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_use);
             float psum = 0.f;
@@ -257,51 +293,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             l_run = l_run * corr + psum;
             m_run = m_new;
-            if (t > 0 && !ptx::mbar_wait(&bar->pv_done, (t - 1) & 1, abort_flag)) { ok = false; break; }
+            // P.V(t - 1) every tile: keeps the pv_done phases observed in
+            // order, and O must hold it before a rescale.
+            if (t > 0 && !ptx::mbar_wait(&bar->pv_done[q], (t - 1) & 1, abort_flag)) { ok = false; break; }
             if (resc && t > 0 && corr != 1.f) {
                 ptx::tc_fence_after();
 #pragma unroll 1
-                for (int c = 0; c < C::kOCols; c += 32) {
+                for (int c = 0; c < NV * 64; c += 32) {
                     uint32_t o[32];
-                    ptx::tmem_ld32(tmem + lane_off + c, o);
+                    ptx::tmem_ld32(tmem + lane_off + q * C::kOCol + c, o);
                     ptx::tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
-                    ptx::tmem_st32(tmem + lane_off + c, o);
+                    ptx::tmem_st32(tmem + lane_off + q * C::kOCol + c, o);
                 }
-                ptx::tmem_st_wait();
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4 *>(prow + ((j ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            ptx::fence_proxy_async_smem();
+            ptx::tmem_st32(tmem + lane_off + sbuf, pk);
+            ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bar->p_full);
+            ptx::mbar_arrive(&bar->p_full[q]);
         }
-        if (ok && ptx::mbar_wait(&bar->pv_done, (n_kt - 1) & 1, abort_flag)) {
-            ptx::tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        if (ok && n_kt[q] > 0) {
+            if (ptx::mbar_wait(&bar->pv_done[q], (n_kt[q] - 1) & 1, abort_flag)) {
+                ptx::tc_fence_after();
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
-            for (int c = 0; c < C::kOCols; c += 32) {
-                uint32_t o[32];
-                ptx::tmem_ld32(tmem + lane_off + c, o);
-                ptx::tmem_ld_wait();
-                if (r < nq) {
-                    bf16 *dst = p.o + (((int64_t)b * p.S + q0 + r) * p.H + h) * p.d_v + c;
+                for (int c = 0; c < NV * 64; c += 32) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tmem + lane_off + q * C::kOCol + c, o);
+                    ptx::tmem_ld_wait();
+                    if (r < nq[q]) {
+                        bf16 *dst = p.o + (((int64_t)b * p.S + q0[q] + r) * p.H + h) * p.d_v + c;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 w;
-                        w.x = ptx::pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
-                        w.y = ptx::pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-                        w.z = ptx::pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
-                        w.w = ptx::pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + j) = w;
+                        for (int j = 0; j < 32; j += 8) {
+                            uint4 w;
+                            w.x = ptx::pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
+                            w.y = ptx::pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
+                            w.z = ptx::pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
+                            w.w = ptx::pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(dst + j) = w;
+                        }
                     }
                 }
+            } else {
+                ok = false;
             }
-        } else {
-            ok = false;
         }
         if (!ok) *abort_flag = 1;
     }
@@ -310,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, C::kTmem);
+        ptx::tmem_dealloc(tmem, 512);
     }
     if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, kStatusTimeout);
 }
@@ -352,8 +388,8 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
         tqr = tq;
         tkr = tk;
     }
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<NQ, NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+    static int smem_dev = -1;
+    cudaError_t e = smem_limit_once(smem_dev, (const void *)prefill_tc_kernel<NQ, NV>, C::kSmem);
     if (e != cudaSuccess) return e;
     PreTcParams p;
     p.B = a.B; p.S = a.S; p.H = a.H; p.max_seq = a.max_seq; p.d_nope = a.d_nope;
@@ -364,7 +400,7 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
     p.o = (bf16 *)a.o;
     p.d_v = a.d_v;
     p.status = a.status;
-    dim3 grid((a.S + kQ - 1) / kQ, a.H, a.B);
+    dim3 grid(((a.S + kQ - 1) / kQ + 1) / 2, a.H, a.B);
     profile_begin(MLA_PROFILE_PREFILL_ATTENTION, s);
     prefill_tc_kernel<NQ, NV><<<grid, kThreads, C::kSmem, s>>>(tq, tqr, tk, tkr, tv, p);
     profile_end(MLA_PROFILE_PREFILL_ATTENTION, s);

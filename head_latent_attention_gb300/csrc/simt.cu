@@ -346,8 +346,11 @@ template <typename T, int HG>
 cudaError_t launch_decode_hg(const DecodeArgs &a, cudaStream_t s)
 {
     size_t smem = sizeof(float) * (size_t)HG * (a.r_lat + a.d_rope + a.chunk);
-    cudaError_t e = cudaFuncSetAttribute(decode_partial_kernel<T, HG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static int smem_dev = -1;
+    static int smem_set = 0;
+    if ((int)smem > smem_set) smem_dev = -1;  // the chunk size can grow the request
+    cudaError_t e = smem_limit_once(smem_dev, (const void *)decode_partial_kernel<T, HG>, (int)smem);
+    if (e == cudaSuccess && (int)smem > smem_set) smem_set = (int)smem;
     if (e != cudaSuccess) return e;
     dim3 grid(a.n_split, a.B, a.H / HG);
     profile_begin(MLA_PROFILE_DECODE_ATTENTION, s);
@@ -376,8 +379,11 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s)
     int dq = a.d_qk_nope + a.d_rope;
     size_t smem = sizeof(float) * ((size_t)kPQ * dq + (size_t)kPK * dq + (size_t)kPK * a.d_v +
                                    (size_t)kPQ * (kPK + 1));
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    static int smem_dev = -1;
+    static int smem_set = 0;
+    if ((int)smem > smem_set) smem_dev = -1;  // the head widths can grow the request
+    cudaError_t e = smem_limit_once(smem_dev, (const void *)prefill_kernel<T>, (int)smem);
+    if (e == cudaSuccess && (int)smem > smem_set) smem_set = (int)smem;
     if (e != cudaSuccess) return e;
     dim3 grid((a.S + kPQ - 1) / kPQ, a.H, a.B);
     profile_begin(MLA_PROFILE_PREFILL_ATTENTION, s);

@@ -212,8 +212,9 @@ typedef enum {
 } mla_profile_point;
 
 /* Process-wide timing hook: while set, every launch of the kernel named by
- * `which` is bracketed by cudaEventRecord(begin) / cudaEventRecord(end) on the
- * stream of the call that launches it.  begin/end are cudaEvent_t handles
+ * `which` is bracketed by records of `begin` and `end` on the stream of the
+ * call that launches it (inside stream capture they are recorded as external
+ * events, i.e. event-record nodes of the graph the caller can time).  begin/end are cudaEvent_t handles
  * owned by the caller; NULL clears the hook.  Not thread-safe: set it only
  * while no other thread is calling into the library. */
 mla_status mla_set_profile_events(int which, void *begin, void *end);
