@@ -35,7 +35,7 @@ TORCH_DTYPE = {DTYPE_F32: torch.float32, DTYPE_BF16: torch.bfloat16}
 EXPORTS = ("mla_check_config", "mla_create", "mla_destroy", "mla_workspace_size",
            "mla_project_latent", "mla_prefill", "mla_decode", "mla_out_proj",
            "mla_get_device_status", "mla_status_string", "mla_launch_count",
-           "mla_set_profile_events")
+           "mla_set_profile_events", "mla_out_proj_static")
 MLA_PROFILE_DECODE_ATTENTION = 0
 MLA_PROFILE_PREFILL_ATTENTION = 1
 
@@ -86,6 +86,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mla_prefill": (I, [P, P, P, P, P, I, I, P, P, P, S, P]),
         "mla_decode": (I, [P, P, P, P, P, P, I, P, P, S, P]),
         "mla_out_proj": (I, [P, P, P, L, P, P, S, P]),
+        "mla_out_proj_static": (I, [P, P, P, L, P, P]),
         "mla_get_device_status": (I, [P, P, P, ctypes.POINTER(ctypes.c_uint32)]),
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_launch_count": (ctypes.c_uint64, []),
@@ -223,7 +224,16 @@ def mla_out_proj(h: Handle, w: MlaWeights, o: torch.Tensor, y: torch.Tensor, ws:
                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
-def mla_get_device_status(h: Handle, ws: torch.Tensor, stream=None):
+def mla_out_proj_static(h: Handle, w: MlaWeights, o: torch.Tensor, y: torch.Tensor,
+                        stream=None) -> int:
+    """mla_out_proj without a workspace: for callers that cannot allocate
+    device memory (the scratch is a fixed buffer owned by the library; see
+    include/mla.h for its size limit and sharing rules)."""
+    return load_library().mla_out_proj_static(h.ptr, ctypes.byref(w), _ptr(o), o.shape[0], _ptr(y),
+                                              _stream(stream))
+
+
+def mla_get_device_status(h: Handle, ws: Optional[torch.Tensor], stream=None):
     bits = ctypes.c_uint32(0)
     st = load_library().mla_get_device_status(h.ptr, _ptr(ws), _stream(stream), ctypes.byref(bits))
     return st, bits.value

@@ -197,6 +197,30 @@ mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int6
  * was set, MLA_ERR_TIMEOUT when bit 8 was, MLA_ERR_DEVICE_DATA otherwise. */
 mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t *bits);
 
+/* Output projection that allocates nothing: the same y = W_O [o_1 ‖ ... ‖ o_H]
+ * as mla_out_proj (same arguments minus the workspace), for callers that can
+ * neither allocate device memory nor hand the library a workspace — e.g. a
+ * plugin inside an inference runtime that has reserved all device memory for
+ * its own pool, or a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not acceptable.  The pages have no counterpart: this is
+ * a deployment convenience, not part of the method.
+ *  - Scratch (the split-K partial sums of small token counts) lives in one
+ *    32 MiB buffer owned by the library (a static device array, held by every
+ *    GPU that loads the library until the process exits).  A call whose
+ *    partial sums would exceed it returns MLA_ERR_WORKSPACE; use mla_out_proj
+ *    with a workspace then.
+ *  - The first call on each device looks the buffer's device address up
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture on the device.
+ *  - All calls on a device share the buffer, which keeps the previous call's
+ *    contents (each call overwrites what it reads, so nothing needs clearing):
+ *    calls whose executions overlap on the GPU (other streams or threads) race
+ *    on it, and the caller must serialise them.
+ *  - Device-side flags (timeouts) go to the handle's status word, read with
+ *    mla_get_device_status(h, NULL, stream, &bits). */
+mla_status mla_out_proj_static(mla_handle *h, const mla_weights *w, const void *o, int64_t T,
+                               void *y, void *stream);
+
 /* Static English text for a status code. */
 const char *mla_status_string(mla_status s);
 

@@ -110,6 +110,7 @@ def test_null_handle_paths(lib):
     assert L.mla_decode(None, None, None, None, None, None, 1, None, None, 0,
                         None) == lib.MLA_ERR_INVALID_ARG
     assert L.mla_out_proj(None, None, None, 1, None, None, 0, None) == lib.MLA_ERR_INVALID_ARG
+    assert L.mla_out_proj_static(None, None, None, 1, None, None) == lib.MLA_ERR_INVALID_ARG
     L.mla_destroy(None)
 
 
