@@ -7,24 +7,27 @@
 // 128 heads x 512 latent columns is exactly one SM's tensor memory, so a
 // cluster of two CTAs splits the columns: CTA r owns latent columns
 // [256 r, 256 r + 256) and rope columns [32 r, 32 r + 32).  Each CTA
-//   - keeps its 288 query columns in tensor memory (the A operand of QK^T),
-//     leaving shared memory to a 6-stage ring of 48-key tiles of its own
-//     cache columns (TMA; 128-byte swizzle for the latent, 64-byte for rope);
+//   - keeps its 256 latent query columns in shared memory (TMA, 128-byte
+//     swizzle) and its 32 rope query columns in tensor memory: both are the
+//     A operand of Q K^T;
+//   - streams 48-key tiles of its own cache columns through a 4-stage ring
+//     (TMA; 128-byte swizzle for the latent, 64-byte for rope);
 //   - computes a partial score tile S_r = Q_r K_r^T (M = 128 heads, N = 48
-//     keys, K = 288) into tensor memory;
+//     keys, K = 288) into one of four score buffers in tensor memory, so the
+//     tensor pipe runs up to three tiles ahead of the softmax;
 //   - sends S_r to the peer with st.async, each store completing bytes on the
 //     peer's mbarrier (double-buffered, so a send never waits for the peer to
 //     finish the previous tile), and adds the peer's partial in the same
 //     order on both sides, so both CTAs take bit-identical softmax decisions;
-//   - writes P (bfloat16) over its scores in tensor memory and accumulates
-//     O_r += P V_r (A from tensor memory, V read as an MN-major operand from
-//     the same shared-memory tile; M = 128, N = 256, K = 48).
+//   - writes P (bfloat16) into one of two P buffers in tensor memory and
+//     accumulates O_r += P V_r (A from tensor memory, V read as an MN-major
+//     operand from the same shared-memory tile; M = 128, N = 256, K = 48).
 // The softmax warps send tile t+1's partial before the exponentials of tile
 // t, so the exchange latency hides behind them.  Warp roles: warp 0 TMA
 // producer, warp 1 MMA issuer (non-blocking polling of both queues, P.V
-// first), warps 2..5 softmax and query loads, one head row per thread.  The
-// running max is raised only when it grows by more than 8 (log2 units), so
-// the O rescale is rare; the result is exact either way because P and the
+// first), warps 2..5 softmax and rope-query loads, one head row per thread.
+// The running max is raised only when it grows by more than 8 (log2 units),
+// so the O rescale is rare; the result is exact either way because P and the
 // running sum use the same max.
 //
 // Work: the concatenation of all sequences' keys is cut into one contiguous
@@ -44,26 +47,34 @@ namespace {
 
 constexpr int kH = 128;       // heads per CTA = MMA M
 constexpr int kBKV = 48;      // keys per tile
-constexpr int kStages = 6;
+constexpr int kStages = 4;    // KV ring
+constexpr int kSBuf = 4;      // score buffers in tensor memory
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kLA = 4;        // 64-column latent atoms per CTA (r_kv = 512)
 
-// Shared memory (per CTA): the KV ring and two exchange buffers.
+// Shared memory (per CTA): the KV ring, the latent query, two exchange buffers.
 constexpr int kAtom = kBKV * 128;                     // one 48x64 latent atom of a KV tile
 constexpr int kStageBytes = kLA * kAtom + kBKV * 64;  // + 32 rope columns (64-byte rows)
-constexpr int kXStride = 52;                          // floats per exchange row (conflict-free v4 rows)
+constexpr int kQAtom = kH * 128;                      // one 128x64 latent atom of the query
+constexpr int kXStride = 28;                          // words per exchange row (conflict-free v4 rows)
 constexpr int kXBytes = kH * kXStride * 4;
-constexpr uint32_t kXTx = kH * kBKV * 4;              // bytes one exchange delivers
-constexpr int kOffX = kStages * kStageBytes;
+constexpr uint32_t kXTx = kH * kBKV * 2;              // bytes one exchange delivers (fp16 scores)
+constexpr int kOffQ = kStages * kStageBytes;
+constexpr int kOffX = kOffQ + kLA * kQAtom;
 constexpr int kOffBar = kOffX + 2 * kXBytes;
 constexpr int kSmem = kOffBar + 256 + 1024;
-// Tensor memory: O in [0, 256), the query (288 bf16 = 144 columns) in
-// [256, 400), score / P buffers at 400 and 448.
+static_assert(kOffQ % 1024 == 0, "query atoms need 1024-byte alignment");
+static_assert(kSmem <= 232448, "shared memory per CTA");
+// Tensor memory: O in [0, 256), four 48-column score buffers in [256, 448),
+// two 24-column P buffers (bf16 pairs) in [448, 496), the rope query (32
+// bf16 = 16 columns) in [496, 512).
 constexpr int kOCols = kLA * 64;
-constexpr int kQCol = 256;
-constexpr int kSCol = 400;
+constexpr int kSCol = 256;
+constexpr int kPCol = kSCol + kSBuf * kBKV;
+constexpr int kQRCol = kPCol + 2 * (kBKV / 2);
 constexpr int kRLat = 2 * kLA * 64;
+static_assert(kQRCol + 16 <= 512, "tensor memory columns");
 
 struct DecTcParams {
     int B, H, max_seq;
@@ -77,14 +88,16 @@ struct DecTcParams {
 };
 
 struct Bars {
-    uint64_t q_full, q_empty;
+    uint64_t q_full, qr_full, q_empty;  // latent query (TMA), rope query (softmax warps), both consumed
     uint64_t kv_full[kStages], kv_empty[kStages];
-    uint64_t s_full[2];
-    uint64_t p_full, pv_done, o_empty;
+    uint64_t s_full[kSBuf], s_free[kSBuf];
+    uint64_t p_full[2], pv_done[2];
+    uint64_t o_empty;
     uint64_t x_full[2], x_free[2];
     int abort;
     uint32_t tmem;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -137,6 +150,38 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                  : "memory");
 }
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Arrive on the peer's mbarrier without ordering earlier memory operations
+// (a release at cluster scope waits for this thread's outstanding remote
+// stores, which costs thousands of cycles); callers order what they must
+// with a barrier first.
+__device__ __forceinline__ void arrive_remote_relaxed(uint32_t remote_bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+// Two fp32 values to fp16 (round to nearest even, saturating at the largest
+// finite value), the lower one in the low half.
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ float2 unpack_f16(uint32_t w)
+{
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+// One CTA's partial score row, scaled to log2 units and rounded to fp16:
+// the form both CTAs add, so that they hold bit-identical scores.
+__device__ __forceinline__ void pack_partial(const uint32_t (&r0)[32], const uint32_t (&r1)[16], float scale,
+                                             uint32_t (&w)[kBKV / 2])
+{
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        w[j] = pack_f16_sat(__uint_as_float(r0[2 * j]) * scale, __uint_as_float(r0[2 * j + 1]) * scale);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        w[16 + j] = pack_f16_sat(__uint_as_float(r1[2 * j]) * scale, __uint_as_float(r1[2 * j + 1]) * scale);
+}
 
 // Segments of this cluster's key range [start, end) of the concatenated keys.
 struct SegIter {
@@ -209,11 +254,12 @@ struct TileCursor {
 
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmR,
-                     const bf16 *__restrict__ q_abs, const bf16 *__restrict__ q_rope, DecTcParams p)
+                     const __grid_constant__ CUtensorMap tmQ, const bf16 *__restrict__ q_rope, DecTcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sKV = smem;
+    uint8_t *sQ = smem + kOffQ;
     float *sX = (float *)(smem + kOffX);
     Bars *bar = (Bars *)(smem + kOffBar);
     volatile int *abort_flag = &bar->abort;
@@ -223,19 +269,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar->q_full, kH);
+        ptx::mbar_init(&bar->q_full, 1);
+        ptx::mbar_init(&bar->qr_full, kH);
         ptx::mbar_init(&bar->q_empty, 1);
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&bar->kv_full[i], 1);
             ptx::mbar_init(&bar->kv_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSBuf; ++i) {
             ptx::mbar_init(&bar->s_full[i], 1);
+            ptx::mbar_init(&bar->s_free[i], kH);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&bar->p_full[i], kH);
+            ptx::mbar_init(&bar->pv_done[i], 1);
             ptx::mbar_init(&bar->x_full[i], 1);
             ptx::mbar_init(&bar->x_free[i], 1);
         }
-        ptx::mbar_init(&bar->p_full, kH);
-        ptx::mbar_init(&bar->pv_done, 1);
         ptx::mbar_init(&bar->o_empty, kH);
         bar->abort = 0;
         ptx::fence_mbar_init();
@@ -259,16 +309,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ptx::elect_one()) {
             ptx::prefetch_tmap(&tmL);
             ptx::prefetch_tmap(&tmR);
+            ptx::prefetch_tmap(&tmQ);
             const uint64_t stream = ptx::policy_evict_first();
             SegIter it;
             it.init(p.prefix, p.B, cid, chunk);
             int b, k0, k1;
             bool whole;
-            int g = 0;
+            int g = 0, nseg = 0;
             int pending[kStages];
 #pragma unroll
             for (int i = 0; i < kStages; ++i) pending[i] = -1;
+            int q_pending = -1;
             while (ok && it.next(b, k0, k1, whole)) {
+                // The segment's latent query, once every Q K^T of the
+                // previous segment has completed.
+                if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) { fail(); break; }
+                ptx::mbar_expect_tx(&bar->q_full, kLA * kQAtom);
+                for (int a = 0; a < kLA; ++a)
+                    ptx::tma_load_2d(sQ + a * kQAtom, &tmQ, &bar->q_full, (int)rank * kLA * 64 + a * 64, b * p.H);
+                q_pending = nseg & 1;
+                ++nseg;
                 const int ntiles = (k1 - k0 + kBKV - 1) / kBKV;
                 for (int t = 0; t < ntiles; ++t, ++g) {
                     const int st = g % kStages;
@@ -284,9 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pending[st] = (int)ph;
                 }
             }
+            // Copies still in flight land before the CTA may exit.
             volatile int never = 0;
             for (int i = 0; i < kStages; ++i)
                 if (pending[i] >= 0) ptx::mbar_wait(&bar->kv_full[i], (uint32_t)pending[i], &never);
+            if (q_pending >= 0) ptx::mbar_wait(&bar->q_full, (uint32_t)q_pending, &never);
         }
     } else if (warp == 1) {
         if (ptx::elect_one()) {
@@ -295,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ready, P.V first (it frees a KV stage for the next load).
             constexpr uint32_t idesc_s = ptx::idesc_bf16(kH, kBKV, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, kLA * 64, false, true);
-            const uint32_t kv0 = ptx::smem_u32(sKV);
+            const uint32_t kv0 = ptx::smem_u32(sKV), q0 = ptx::smem_u32(sQ);
             TileCursor qk, pv;
             qk.init(p.prefix, p.B, cid, chunk);
             pv.init(p.prefix, p.B, cid, chunk);
@@ -303,45 +365,49 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (ok && pv.valid) {
                 bool progressed = false;
                 if (pv.g < qk.g) {
-                    bool ready = ptx::mbar_test(ptx::smem_u32(&bar->p_full), pv.g & 1);
+                    bool ready = ptx::mbar_test(ptx::smem_u32(&bar->p_full[pv.g & 1]), (pv.g >> 1) & 1);
                     if (ready && pv.t == 0 && pv.nseg > 0)
                         ready = ptx::mbar_test(ptx::smem_u32(&bar->o_empty), (pv.nseg - 1) & 1);
                     if (ready) {
                         ptx::tc_fence_after();
                         const int st = pv.g % kStages;
                         const uint32_t vb = kv0 + st * kStageBytes;
-                        const uint32_t pa = tmem + kSCol + (pv.g & 1) * kBKV;
+                        const uint32_t pa = tmem + kPCol + (pv.g & 1) * (kBKV / 2);
 #pragma unroll
                         for (int k = 0; k < kBKV / 16; ++k)
                             ptx::mma_f16_tmem_a(tmem, pa + k * 8, ptx::sdesc_sw128(vb + k * 2048, kAtom, 1024),
                                                 idesc_o, (pv.t == 0 && k == 0) ? 0u : 1u);
                         ptx::mma_commit(&bar->kv_empty[st]);
-                        ptx::mma_commit(&bar->pv_done);
+                        ptx::mma_commit(&bar->pv_done[pv.g & 1]);
                         pv.step();
                         progressed = true;
                     }
                 }
-                // QK^T of tile g overwrites the buffer that held P(g - 2):
-                // P.V(g - 2) must have been issued (the tensor pipe keeps order).
-                if (qk.valid && pv.g >= qk.g - 1) {
-                    const int st = qk.g % kStages;
-                    bool ready = qk.t > 0 || ptx::mbar_test(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
+                if (qk.valid) {
+                    const int st = qk.g % kStages, sb = qk.g % kSBuf;
+                    bool ready = qk.t > 0 || (ptx::mbar_test(ptx::smem_u32(&bar->q_full), qk.nseg & 1) &&
+                                              ptx::mbar_test(ptx::smem_u32(&bar->qr_full), qk.nseg & 1));
                     ready = ready && ptx::mbar_test(ptx::smem_u32(&bar->kv_full[st]), (qk.g / kStages) & 1);
+                    // Score buffer sb held tile g - 4: the softmax must have read it.
+                    ready = ready && (qk.g < kSBuf ||
+                                      ptx::mbar_test(ptx::smem_u32(&bar->s_free[sb]), ((qk.g / kSBuf) - 1) & 1));
                     if (ready) {
                         ptx::tc_fence_after();
                         const uint32_t kb = kv0 + st * kStageBytes;
-                        const uint32_t d = tmem + kSCol + (qk.g & 1) * kBKV;
-                        // K steps 0..15: latent atoms (128-byte swizzle); 16..17: rope (64-byte).
+                        const uint32_t d = tmem + kSCol + sb * kBKV;
+                        // K steps 0..15: latent (query and keys in 128-byte
+                        // swizzled atoms); 16..17: rope (query in tensor
+                        // memory, keys 64-byte swizzled).
 #pragma unroll
                         for (int k = 0; k < 16; ++k)
-                            ptx::mma_f16_tmem_a(d, tmem + kQCol + k * 8,
-                                                ptx::sdesc_sw128(kb + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
-                                                idesc_s, k != 0);
+                            ptx::mma_bf16(d, ptx::sdesc_sw128(q0 + (k >> 2) * kQAtom + (k & 3) * 32, 16, 1024),
+                                          ptx::sdesc_sw128(kb + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024), idesc_s,
+                                          k != 0);
 #pragma unroll
                         for (int k = 0; k < 2; ++k)
-                            ptx::mma_f16_tmem_a(d, tmem + kQCol + (16 + k) * 8,
+                            ptx::mma_f16_tmem_a(d, tmem + kQRCol + k * 8,
                                                 ptx::sdesc_sw64(kb + kLA * kAtom + k * 32, 512), idesc_s, 1u);
-                        ptx::mma_commit(&bar->s_full[qk.g & 1]);
+                        ptx::mma_commit(&bar->s_full[sb]);
                         if (qk.t == qk.ntiles - 1) ptx::mma_commit(&bar->q_empty);
                         qk.step();
                         progressed = true;
@@ -361,24 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             peer_xfull[i] = map_peer(&bar->x_full[i], peer);
             peer_xfree[i] = map_peer(&bar->x_free[i], peer);
         }
-        // This CTA's 288 query columns of row h into tensor memory (lanes =
-        // heads, bf16 pairs per 32-bit column, lower column in the low half,
-        // which is how consecutive bf16 values sit in memory).
-        auto load_q = [&](int b, int nseg) -> bool {
+        // This CTA's 32 rope query columns of row h into tensor memory (lanes
+        // = heads, bf16 pairs per 32-bit column, lower column in the low
+        // half, which is how consecutive bf16 values sit in memory).
+        auto load_qr = [&](int b, int nseg) -> bool {
             if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) return false;
             ptx::tc_fence_after();
             const bool row_ok = h < p.H;
-            const uint4 *src = reinterpret_cast<const uint4 *>(q_abs + ((int64_t)b * p.H + h) * kRLat + rank * kOCols);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t w[32];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 v = row_ok ? src[c * 8 + i] : make_uint4(0, 0, 0, 0);
-                    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-                }
-                ptx::tmem_st32(tmem + lane_off + kQCol + c * 32, w);
-            }
             const uint4 *rs = reinterpret_cast<const uint4 *>(q_rope + ((int64_t)b * p.H + h) * 64 + rank * 32);
             uint32_t w[16];
 #pragma unroll
@@ -386,37 +441,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 v = row_ok ? rs[i] : make_uint4(0, 0, 0, 0);
                 w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
             }
-            ptx::tmem_st16(tmem + lane_off + kQCol + 128, w);
+            ptx::tmem_st16(tmem + lane_off + kQRCol, w);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bar->q_full);
+            ptx::mbar_arrive(&bar->qr_full);
             return true;
         };
-        // Read this thread's score row of buffer g & 1 and send it into the
-        // peer's exchange buffer g & 1.
+        // Read this thread's score row of tile g and send it into the peer's
+        // exchange buffer g & 1.
         auto send = [&](int g) -> bool {
-            if (!ptx::mbar_wait(&bar->s_full[g & 1], (g >> 1) & 1, abort_flag)) return false;
+            const int sb = g % kSBuf;
+            if (!ptx::mbar_wait(&bar->s_full[sb], (g / kSBuf) & 1, abort_flag)) return false;
             if (!ptx::mbar_wait_cluster(&bar->x_free[g & 1], ((g >> 1) & 1) ^ 1, abort_flag)) return false;
             ptx::tc_fence_after();
             uint32_t r0[32], r1[16];
-            ptx::tmem_ld32(tmem + lane_off + kSCol + (g & 1) * kBKV, r0);
-            ptx::tmem_ld16(tmem + lane_off + kSCol + (g & 1) * kBKV + 32, r1);
+            ptx::tmem_ld32(tmem + lane_off + kSCol + sb * kBKV, r0);
+            ptx::tmem_ld16(tmem + lane_off + kSCol + sb * kBKV + 32, r1);
             ptx::tmem_ld_wait();
+            uint32_t w[kBKV / 2];
+            pack_partial(r0, r1, p.scale_log2, w);
             const uint32_t dst = peer_xrow[g & 1], xb = peer_xfull[g & 1];
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                st_async_v4(dst + c * 16, __uint_as_float(r0[4 * c]), __uint_as_float(r0[4 * c + 1]),
-                            __uint_as_float(r0[4 * c + 2]), __uint_as_float(r0[4 * c + 3]), xb);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                st_async_v4(dst + (8 + c) * 16, __uint_as_float(r1[4 * c]), __uint_as_float(r1[4 * c + 1]),
-                            __uint_as_float(r1[4 * c + 2]), __uint_as_float(r1[4 * c + 3]), xb);
+            for (int c = 0; c < kBKV / 8; ++c)
+                st_async_v4(dst + c * 16, __uint_as_float(w[4 * c]), __uint_as_float(w[4 * c + 1]),
+                            __uint_as_float(w[4 * c + 2]), __uint_as_float(w[4 * c + 3]), xb);
             return true;
         };
         TileCursor nx;  // the tile after the current one (the send runs one tile ahead)
         nx.init(p.prefix, p.B, cid, chunk);
         if (nx.valid) {
-            if (!load_q(nx.b, 0) || !send(0)) fail();
+            if (!load_qr(nx.b, 0) || !send(0)) fail();
             nx.step();
         }
         SegIter it;
@@ -430,38 +484,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ntiles = (len + kBKV - 1) / kBKV;
             for (int t = 0; t < ntiles; ++t, ++g) {
                 const int valid = min(kBKV, len - t * kBKV);
-                const int xb = g & 1;
+                const int xb = g & 1, sb = g % kSBuf;
                 // 1. Full scores of tile g: own partial (still in tensor
                 //    memory) plus the peer's, same operand order in both CTAs.
                 if (!ptx::mbar_wait_cluster(&bar->x_full[xb], (g >> 1) & 1, abort_flag)) { fail(); break; }
                 float s[kBKV];
                 {
                     uint32_t r0[32], r1[16];
-                    ptx::tmem_ld32(tmem + lane_off + kSCol + xb * kBKV, r0);
-                    ptx::tmem_ld16(tmem + lane_off + kSCol + xb * kBKV + 32, r1);
+                    ptx::tmem_ld32(tmem + lane_off + kSCol + sb * kBKV, r0);
+                    ptx::tmem_ld16(tmem + lane_off + kSCol + sb * kBKV + 32, r1);
                     ptx::tmem_ld_wait();
-                    const float *xr = sX + xb * (kXBytes / 4) + h * kXStride;
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(&bar->s_free[sb]);  // score buffer sb may take tile g + 4
+                    uint32_t w[kBKV / 2];
+                    pack_partial(r0, r1, p.scale_log2, w);
+                    const uint32_t *xr = reinterpret_cast<const uint32_t *>(sX) + xb * (kXBytes / 4) + h * kXStride;
 #pragma unroll
-                    for (int c = 0; c < kBKV / 4; ++c) {
-                        const float4 v = *reinterpret_cast<const float4 *>(xr + 4 * c);
-                        const uint32_t *rr = c < 8 ? &r0[4 * c] : &r1[4 * (c - 8)];
-                        const float o0 = __uint_as_float(rr[0]), o1 = __uint_as_float(rr[1]);
-                        const float o2 = __uint_as_float(rr[2]), o3 = __uint_as_float(rr[3]);
-                        if (rank == 0) {
-                            s[4 * c] = o0 + v.x; s[4 * c + 1] = o1 + v.y; s[4 * c + 2] = o2 + v.z; s[4 * c + 3] = o3 + v.w;
-                        } else {
-                            s[4 * c] = v.x + o0; s[4 * c + 1] = v.y + o1; s[4 * c + 2] = v.z + o2; s[4 * c + 3] = v.w + o3;
+                    for (int c = 0; c < kBKV / 8; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(xr + 4 * c);
+                        const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 a = unpack_f16(w[4 * c + i]), b = unpack_f16(pw[i]);
+                            s[8 * c + 2 * i] = a.x + b.x;
+                            s[8 * c + 2 * i + 1] = a.y + b.y;
                         }
                     }
                 }
                 softmax_bar();  // every row of exchange buffer xb has been read
                 if (h == 0) {
                     ptx::mbar_expect_tx(&bar->x_full[xb], kXTx);  // arm its next use (tile g + 2)
-                    arrive_remote(peer_xfree[xb]);                // the peer may overwrite it
+                    arrive_remote_relaxed(peer_xfree[xb]);        // the peer may overwrite it
                 }
-                // 2. The next tile: its query (at a segment boundary) and its partial.
+                // 2. The next tile: its rope query (at a segment boundary) and its partial.
                 if (nx.valid) {
-                    if (nx.t == 0 && !load_q(nx.b, nx.nseg)) { fail(); break; }
+                    if (nx.t == 0 && !load_qr(nx.b, nx.nseg)) { fail(); break; }
                     if (!send(g + 1)) { fail(); break; }
                     nx.step();
                 }
@@ -469,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float mt = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < kBKV; ++j) {
-                    s[j] = (j < valid) ? s[j] * p.scale_log2 : -INFINITY;
+                    s[j] = (j < valid) ? s[j] : -INFINITY;
                     mt = fmaxf(mt, s[j]);
                 }
                 const bool resc = mt > m_run + kRescaleThreshold;
@@ -485,12 +542,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l_run = l_run * corr + psum;
                 m_run = m_new;
-                // Wait for P.V(g - 1) every tile, so that the pv_done phases
-                // are observed in order (a parity wait is only valid one
-                // phase behind); it is long done by now.  O must also hold
-                // every earlier P.V before a rescale.
-                if (g > 0 && !ptx::mbar_wait(&bar->pv_done, (g - 1) & 1, abort_flag)) { fail(); break; }
+                // P buffer g & 1 held P(g - 2): wait for P.V(g - 2).  Each
+                // pv_done barrier is waited on phase by phase, never two
+                // phases behind (P.V(g) cannot finish before P(g) exists).
+                if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[xb], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
                 if (resc && t > 0) {
+                    // O must hold every earlier P.V before it is rescaled.
+                    if (!ptx::mbar_wait(&bar->pv_done[xb ^ 1], ((g - 1) >> 1) & 1, abort_flag)) { fail(); break; }
                     ptx::tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < kOCols; c += 32) {
@@ -502,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tmem_st32(tmem + lane_off + c, o);
                     }
                 }
-                // P over the scores of this tile (columns 0..23 of the buffer).
-                ptx::tmem_st16(tmem + lane_off + kSCol + xb * kBKV, pk);
-                ptx::tmem_st8(tmem + lane_off + kSCol + xb * kBKV + 16, pk + 16);
+                ptx::tc_fence_after();
+                ptx::tmem_st16(tmem + lane_off + kPCol + xb * (kBKV / 2), pk);
+                ptx::tmem_st8(tmem + lane_off + kPCol + xb * (kBKV / 2) + 16, pk + 16);
                 ptx::tmem_st_wait();
                 if (valid < kBKV) {
                     // Rows past the segment may hold arbitrary cache contents;
@@ -519,11 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::fence_proxy_async_smem();
                 }
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(&bar->p_full);
+                ptx::mbar_arrive(&bar->p_full[xb]);
             }
             if (!ok) break;
             // Segment done: read the accumulator once its last P.V completed.
-            if (!ptx::mbar_wait(&bar->pv_done, (g - 1) & 1, abort_flag)) { fail(); break; }
+            if (!ptx::mbar_wait(&bar->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag)) { fail(); break; }
             ptx::tc_fence_after();
             const bool row_ok = h < p.H;
             const int slot = cid + b;
@@ -660,8 +718,10 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
 {
     CUtensorMap tl, tr;
     const int64_t c_rows = (int64_t)a.max_batch * a.max_seq;
+    CUtensorMap tq;
     if (!make_tmap_bf16(&tl, a.lat, c_rows, kRLat, a.lat_stride, 64, kBKV) ||
-        !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV))
+        !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV) ||
+        !make_tmap_bf16(&tq, a.q_abs, (int64_t)a.B * a.H, kRLat, kRLat, 64, kH))
         return cudaErrorInvalidValue;
     decode_schedule_kernel<<<1, 1024, 0, s>>>(a.seq_lens, a.B, a.max_seq, a.n_clusters, a.prefix, a.chunk,
                                               a.status);
@@ -692,7 +752,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     profile_begin(MLA_PROFILE_DECODE_ATTENTION, s);
-    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tl, tr, (const bf16 *)a.q_abs, (const bf16 *)a.q_rope, p);
+    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tl, tr, tq, (const bf16 *)a.q_rope, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
     if (e != cudaSuccess) return e;
