@@ -59,10 +59,11 @@ constexpr int kStageBytes = kLA * kAtom + kBKV * 64;  // + 32 rope columns (64-b
 constexpr int kQAtom = kH * 128;                      // one 128x64 latent atom of the query
 constexpr int kXStride = 28;                          // words per exchange row (conflict-free v4 rows)
 constexpr int kXBytes = kH * kXStride * 4;
-constexpr uint32_t kXTx = kH * kBKV * 2;              // bytes one exchange delivers (fp16 scores)
+constexpr uint32_t kXTx = kXBytes;                    // one exchange = one bulk copy of a whole buffer
 constexpr int kOffQ = kStages * kStageBytes;
 constexpr int kOffX = kOffQ + kLA * kQAtom;
-constexpr int kOffBar = kOffX + 2 * kXBytes;
+constexpr int kOffStage = kOffX + 2 * kXBytes;       // outgoing partial, copied to the peer in bulk
+constexpr int kOffBar = kOffStage + kXBytes;
 constexpr int kSmem = kOffBar + 256 + 1024;
 static_assert(kOffQ % 1024 == 0, "query atoms need 1024-byte alignment");
 static_assert(kSmem <= 232448, "shared memory per CTA");
@@ -150,6 +151,20 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
                  : "memory");
 }
 __device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void stage_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// Bulk copy of `bytes` from this CTA's shared memory into the peer's, completing
+// the bytes on the peer's mbarrier (both peer addresses already mapped).
+__device__ __forceinline__ void bulk_to_peer(uint32_t peer_dst, const void *src, uint32_t bytes, uint32_t peer_bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t"
+        "cp.async.bulk.commit_group;" ::"r"(peer_dst),
+        "r"(ptx::smem_u32(src)), "r"(bytes), "r"(peer_bar)
+        : "memory");
+}
+// The bulk copies this thread issued have finished reading their source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Arrive on the peer's mbarrier without ordering earlier memory operations
 // (a release at cluster scope waits for this thread's outstanding remote
 // stores, which costs thousands of cycles); callers order what they must
@@ -421,9 +436,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp % 4;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        uint32_t peer_xrow[2], peer_xfull[2], peer_xfree[2];
+        uint32_t peer_xbuf[2], peer_xfull[2], peer_xfree[2];
+        uint32_t *my_stage = reinterpret_cast<uint32_t *>(smem + kOffStage) + h * kXStride;
         for (int i = 0; i < 2; ++i) {
-            peer_xrow[i] = map_peer((const uint8_t *)sX + i * kXBytes + h * kXStride * 4, peer);
+            peer_xbuf[i] = map_peer((const uint8_t *)sX + i * kXBytes, peer);
             peer_xfull[i] = map_peer(&bar->x_full[i], peer);
             peer_xfree[i] = map_peer(&bar->x_free[i], peer);
         }
@@ -460,11 +476,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld_wait();
             uint32_t w[kBKV / 2];
             pack_partial(r0, r1, p.scale_log2, w);
-            const uint32_t dst = peer_xrow[g & 1], xb = peer_xfull[g & 1];
+            // Stage the row locally (the previous bulk copy has finished
+            // reading the staging buffer: its issuer waited before the last
+            // softmax barrier); one thread then copies all rows to the peer.
 #pragma unroll
             for (int c = 0; c < kBKV / 8; ++c)
-                st_async_v4(dst + c * 16, __uint_as_float(w[4 * c]), __uint_as_float(w[4 * c + 1]),
-                            __uint_as_float(w[4 * c + 2]), __uint_as_float(w[4 * c + 3]), xb);
+                *reinterpret_cast<uint4 *>(my_stage + 4 * c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            ptx::fence_proxy_async_smem();
+            stage_bar();
+            if (h == 0) bulk_to_peer(peer_xbuf[g & 1], smem + kOffStage, kXBytes, peer_xfull[g & 1]);
             return true;
         };
         TileCursor nx;  // the tile after the current one (the send runs one tile ahead)
@@ -511,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                if (h == 0) bulk_wait_read();  // the staging buffer may be rewritten
                 softmax_bar();  // every row of exchange buffer xb has been read
                 if (h == 0) {
                     ptx::mbar_expect_tx(&bar->x_full[xb], kXTx);  // arm its next use (tile g + 2)
@@ -622,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // copies into the peer have landed
     ptx::tc_fence_before();
     __syncthreads();
     cluster_sync();  // no CTA leaves while its peer may still touch its shared memory
