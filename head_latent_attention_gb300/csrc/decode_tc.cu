@@ -7,28 +7,27 @@
 // 128 heads x 512 latent columns is exactly one SM's tensor memory, so a
 // cluster of two CTAs splits the columns: CTA r owns latent columns
 // [256 r, 256 r + 256) and rope columns [32 r, 32 r + 32).  Each CTA
-//   - keeps its 256 latent query columns in shared memory (TMA, 128-byte
-//     swizzle) and its 32 rope query columns in tensor memory: both are the
-//     A operand of Q K^T;
-//   - streams 48-key tiles of its own cache columns through a 4-stage ring
+//   - keeps O (256 columns), its 288 query columns (the A operand of Q K^T)
+//     and two 48-column score buffers in tensor memory;
+//   - streams 48-key tiles of its own cache columns through a 5-stage ring
 //     (TMA; 128-byte swizzle for the latent, 64-byte for rope);
 //   - computes a partial score tile S_r = Q_r K_r^T (M = 128 heads, N = 48
-//     keys, K = 288) into one of four score buffers in tensor memory, so the
-//     tensor pipe runs up to three tiles ahead of the softmax;
-//   - sends S_r to the peer with st.async, each store completing bytes on the
-//     peer's mbarrier (double-buffered, so a send never waits for the peer to
-//     finish the previous tile), and adds the peer's partial in the same
-//     order on both sides, so both CTAs take bit-identical softmax decisions;
-//   - writes P (bfloat16) into one of two P buffers in tensor memory and
-//     accumulates O_r += P V_r (A from tensor memory, V read as an MN-major
-//     operand from the same shared-memory tile; M = 128, N = 256, K = 48).
-// The softmax warps send tile t+1's partial before the exponentials of tile
-// t, so the exchange latency hides behind them.  Warp roles: warp 0 TMA
-// producer, warp 1 MMA issuer (non-blocking polling of both queues, P.V
-// first), warps 2..5 softmax and rope-query loads, one head row per thread.
-// The running max is raised only when it grows by more than 8 (log2 units),
-// so the O rescale is rare; the result is exact either way because P and the
-// running sum use the same max.
+//     keys, K = 288);
+//   - scales S_r to log2 units, rounds it to fp16 and sends it to the peer
+//     two tiles ahead of the softmax, one bulk copy per warp (distributed
+//     shared memory moves ~12 bytes per clock per SM, so the exchange is
+//     the scarce resource); both CTAs add the same two rounded partials and
+//     so take bit-identical softmax decisions;
+//   - writes P (bfloat16) to shared memory (K-major, no swizzle) and
+//     accumulates O_r += P V_r (M = 128, N = 256, K = 48), V read as an
+//     MN-major operand from the same shared-memory tile.
+// Warp roles: warp 0 TMA producer (the first loads go out before the setup
+// syncs), warp 1 MMA issuer (non-blocking polling of both queues), warps
+// 2..9 softmax in two groups that take alternate tiles (two tiles in
+// flight), one head row per thread.  The running reference max is raised
+// only when a tile exceeds it by more than 8 (log2 units), so O is rarely
+// rescaled; the groups hand it to each other tile by tile.  The result is
+// exact either way because P and the row sums use the same reference.
 //
 // Work: the concatenation of all sequences' keys is cut into one contiguous
 // range per cluster (a device-side scheduler computes the prefix sums of the
@@ -47,33 +46,43 @@ namespace {
 
 constexpr int kH = 128;       // heads per CTA = MMA M
 constexpr int kBKV = 48;      // keys per tile
-constexpr int kStages = 4;    // KV ring
-constexpr int kSBuf = 4;      // score buffers in tensor memory
-constexpr int kThreads = 192;
+constexpr int kStages = 5;    // KV ring
+constexpr int kSBuf = 2;      // score buffers in tensor memory
+constexpr int kSoftmaxThreads = 256;  // warps 2..9
+constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr float kRescaleThreshold = 8.f;
 constexpr int kLA = 4;        // 64-column latent atoms per CTA (r_kv = 512)
 
 // Shared memory (per CTA): the KV ring, the latent query, two exchange buffers.
 constexpr int kAtom = kBKV * 128;                     // one 48x64 latent atom of a KV tile
 constexpr int kStageBytes = kLA * kAtom + kBKV * 64;  // + 32 rope columns (64-byte rows)
-constexpr int kQAtom = kH * 128;                      // one 128x64 latent atom of the query
-constexpr int kXStride = 28;                          // words per exchange row (conflict-free v4 rows)
-constexpr int kXBytes = kH * kXStride * 4;
+constexpr int kXBuf = 2;                              // exchange buffers (partials travel two tiles ahead)
+// Exchange buffer (fp16 scores): [head][48 keys], so each softmax warp's 32
+// head rows are one contiguous block that the warp copies to the peer itself.
+constexpr int kXRowBytes = kBKV * 2;
+constexpr int kXWarpBytes = 32 * kXRowBytes;
+constexpr int kXBytes = kH * kXRowBytes;
 constexpr uint32_t kXTx = kXBytes;                    // one exchange = one bulk copy of a whole buffer
-constexpr int kOffQ = kStages * kStageBytes;
-constexpr int kOffX = kOffQ + kLA * kQAtom;
-constexpr int kOffStage = kOffX + 2 * kXBytes;       // outgoing partial, copied to the peer in bulk
-constexpr int kOffBar = kOffStage + kXBytes;
-constexpr int kSmem = kOffBar + 256 + 1024;
-static_assert(kOffQ % 1024 == 0, "query atoms need 1024-byte alignment");
+constexpr int kOffX = kStages * kStageBytes;
+constexpr int kOffStage = kOffX + kXBuf * kXBytes;   // outgoing partials (one buffer per softmax group)
+// P (bf16, 128 heads x 48 keys) as the A operand of P.V: K-major without
+// swizzle, 8-row x 16-byte core matrices, the six core matrices of an 8-row
+// group adjacent (128 bytes apart), 8-row groups 768 bytes apart.
+constexpr int kPBytes = kH * kBKV * 2;
+constexpr int kPGroup = (kBKV / 8) * 128;
+constexpr int kOffP = kOffStage + 2 * kXBytes;
+constexpr int kOffRed = kOffP + 2 * kPBytes;          // reference maxima, segment-end (max, sum)
+constexpr int kOffBar = kOffRed + 6 * kH * 4;
+constexpr int kSmem = kOffBar + 512 + 1024;
+static_assert(kOffP % 16 == 0, "P operand alignment");
 static_assert(kSmem <= 232448, "shared memory per CTA");
-// Tensor memory: O in [0, 256), four 48-column score buffers in [256, 448),
-// two 24-column P buffers (bf16 pairs) in [448, 496), the rope query (32
-// bf16 = 16 columns) in [496, 512).
+// Tensor memory: O in [0, 256), the query (256 latent + 32 rope bf16 = 144
+// columns) in [256, 400), two 48-column score buffers in [400, 496).
 constexpr int kOCols = kLA * 64;
-constexpr int kSCol = 256;
-constexpr int kPCol = kSCol + kSBuf * kBKV;
-constexpr int kQRCol = kPCol + 2 * (kBKV / 2);
+constexpr int kQCol = 256;
+constexpr int kQRCol = kQCol + kOCols / 2;
+constexpr int kSCol = kQRCol + 16;
+static_assert(kSCol + kSBuf * kBKV <= 512, "tensor memory columns");
 constexpr int kRLat = 2 * kLA * 64;
 static_assert(kQRCol + 16 <= 512, "tensor memory columns");
 
@@ -89,16 +98,20 @@ struct DecTcParams {
 };
 
 struct Bars {
-    uint64_t q_full, qr_full, q_empty;  // latent query (TMA), rope query (softmax warps), both consumed
+    uint64_t q_full, q_empty;  // query written to tensor memory by the softmax warps; consumed
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[kSBuf], s_free[kSBuf];
     uint64_t p_full[2], pv_done[2];
     uint64_t o_empty;
-    uint64_t x_full[2], x_free[2];
+    uint64_t x_full[kXBuf], x_free[kXBuf];
+    // Softmax groups: reference-max handoff from group i, per lane quarter
+    // (one arrival per thread of the producing warp), and the segment-end
+    // meeting of the two warps of a lane quarter.
+    uint64_t hand[2][4], seg[4];
     int abort;
     uint32_t tmem;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -112,12 +125,6 @@ __device__ __forceinline__ uint32_t cluster_id()
     asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
     return r;
 }
-__device__ __forceinline__ uint32_t cluster_count()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
 __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -128,30 +135,23 @@ __device__ __forceinline__ uint32_t map_peer(const void *p, uint32_t peer)
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(ptx::smem_u32(p)), "r"(peer));
     return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d)
-{
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
-}
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v)
 {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void arrive_remote(uint32_t remote_bar)
+// Shared-memory matrix descriptor without swizzle: 8-row x 16-byte core
+// matrices, `lbo` bytes between core matrices along K, `sbo` bytes between
+// 8-row groups.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, uint32_t sbo)
 {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version; layout type 0 = no swizzle
+    return d;
 }
-// 16-byte store into the peer's shared memory that completes 16 bytes of the
-// transaction count of the peer's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar)
-{
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     addr),
-                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
-                 : "memory");
-}
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ void stage_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
 // Bulk copy of `bytes` from this CTA's shared memory into the peer's, completing
 // the bytes on the peer's mbarrier (both peer addresses already mapped).
 __device__ __forceinline__ void bulk_to_peer(uint32_t peer_dst, const void *src, uint32_t bytes, uint32_t peer_bar)
@@ -184,18 +184,6 @@ __device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi)
 __device__ __forceinline__ float2 unpack_f16(uint32_t w)
 {
     return __half22float2(*reinterpret_cast<const __half2 *>(&w));
-}
-// One CTA's partial score row, scaled to log2 units and rounded to fp16:
-// the form both CTAs add, so that they hold bit-identical scores.
-__device__ __forceinline__ void pack_partial(const uint32_t (&r0)[32], const uint32_t (&r1)[16], float scale,
-                                             uint32_t (&w)[kBKV / 2])
-{
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-        w[j] = pack_f16_sat(__uint_as_float(r0[2 * j]) * scale, __uint_as_float(r0[2 * j + 1]) * scale);
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        w[16 + j] = pack_f16_sat(__uint_as_float(r1[2 * j]) * scale, __uint_as_float(r1[2 * j + 1]) * scale);
 }
 
 // Segments of this cluster's key range [start, end) of the concatenated keys.
@@ -269,13 +257,11 @@ struct TileCursor {
 
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmR,
-                     const __grid_constant__ CUtensorMap tmQ, const bf16 *__restrict__ q_rope, DecTcParams p)
+                     const bf16 *__restrict__ q_abs, const bf16 *__restrict__ q_rope, DecTcParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sKV = smem;
-    uint8_t *sQ = smem + kOffQ;
-    float *sX = (float *)(smem + kOffX);
     Bars *bar = (Bars *)(smem + kOffBar);
     volatile int *abort_flag = &bar->abort;
 
@@ -283,9 +269,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cid = (int)cluster_id();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
+    // KV loads are issued by thread 0: the first kStages right after the
+    // barriers exist (before the CTA and cluster syncs, so the first HBM
+    // round trip overlaps the setup), the rest from the producer loop.
+    TileCursor ld;
+    int pending[kStages];
+    uint64_t evict_first = 0;
+    auto issue_load = [&]() -> bool {
+        const int st = ld.g % kStages;
+        const uint32_t ph = (uint32_t)(ld.g / kStages) & 1;
+        if (!ptx::mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag)) return false;
+        ptx::mbar_expect_tx(&bar->kv_full[st], kStageBytes);
+        const int row = ld.b * p.max_seq + ld.k0 + ld.t * kBKV;
+        uint8_t *dst = sKV + st * kStageBytes;
+        for (int a = 0; a < kLA; ++a)
+            ptx::tma_load_2d_hint(dst + a * kAtom, &tmL, &bar->kv_full[st], (int)rank * kLA * 64 + a * 64, row,
+                                  evict_first);
+        ptx::tma_load_2d_hint(dst + kLA * kAtom, &tmR, &bar->kv_full[st], (int)rank * 32, row, evict_first);
+        pending[st] = (int)ph;
+        ld.step();
+        return true;
+    };
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar->q_full, 1);
-        ptx::mbar_init(&bar->qr_full, kH);
+        ptx::mbar_init(&bar->q_full, kSoftmaxThreads / 2);  // the group that sends a segment's first tile
         ptx::mbar_init(&bar->q_empty, 1);
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&bar->kv_full[i], 1);
@@ -293,18 +299,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kSBuf; ++i) {
             ptx::mbar_init(&bar->s_full[i], 1);
-            ptx::mbar_init(&bar->s_free[i], kH);
+            ptx::mbar_init(&bar->s_free[i], kSoftmaxThreads / 2);  // one softmax group per buffer
         }
         for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(&bar->p_full[i], kH);
+            ptx::mbar_init(&bar->p_full[i], kSoftmaxThreads / 2);
             ptx::mbar_init(&bar->pv_done[i], 1);
-            ptx::mbar_init(&bar->x_full[i], 1);
-            ptx::mbar_init(&bar->x_free[i], 1);
         }
-        ptx::mbar_init(&bar->o_empty, kH);
+        for (int i = 0; i < kXBuf; ++i) {
+            ptx::mbar_init(&bar->x_full[i], 1);
+            ptx::mbar_init(&bar->x_free[i], kSoftmaxThreads / 64);  // one arrival per warp of a peer group
+        }
+        ptx::mbar_init(&bar->o_empty, kSoftmaxThreads);
+        for (int q = 0; q < 4; ++q) {
+            ptx::mbar_init(&bar->hand[0][q], 32);
+            ptx::mbar_init(&bar->hand[1][q], 32);
+            ptx::mbar_init(&bar->seg[q], 64);
+        }
         bar->abort = 0;
         ptx::fence_mbar_init();
-        for (int i = 0; i < 2; ++i) ptx::mbar_expect_tx(&bar->x_full[i], kXTx);  // arm both buffers
+        for (int i = 0; i < kXBuf; ++i) ptx::mbar_expect_tx(&bar->x_full[i], kXTx);  // arm every buffer
+        ptx::prefetch_tmap(&tmL);
+        ptx::prefetch_tmap(&tmR);
+        evict_first = ptx::policy_evict_first();
+#pragma unroll
+        for (int i = 0; i < kStages; ++i) pending[i] = -1;
+        ld.init(p.prefix, p.B, cid, *p.chunk);
+        for (int i = 0; i < kStages && ld.valid; ++i) issue_load();  // fresh ring: no waits
     }
     if (warp == 1) ptx::tmem_alloc(&bar->tmem, 512);
     ptx::tc_fence_before();
@@ -321,49 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp == 0) {
-        if (ptx::elect_one()) {
-            ptx::prefetch_tmap(&tmL);
-            ptx::prefetch_tmap(&tmR);
-            ptx::prefetch_tmap(&tmQ);
-            const uint64_t stream = ptx::policy_evict_first();
-            SegIter it;
-            it.init(p.prefix, p.B, cid, chunk);
-            int b, k0, k1;
-            bool whole;
-            int g = 0, nseg = 0;
-            int pending[kStages];
-#pragma unroll
-            for (int i = 0; i < kStages; ++i) pending[i] = -1;
-            int q_pending = -1;
-            while (ok && it.next(b, k0, k1, whole)) {
-                // The segment's latent query, once every Q K^T of the
-                // previous segment has completed.
-                if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) { fail(); break; }
-                ptx::mbar_expect_tx(&bar->q_full, kLA * kQAtom);
-                for (int a = 0; a < kLA; ++a)
-                    ptx::tma_load_2d(sQ + a * kQAtom, &tmQ, &bar->q_full, (int)rank * kLA * 64 + a * 64, b * p.H);
-                q_pending = nseg & 1;
-                ++nseg;
-                const int ntiles = (k1 - k0 + kBKV - 1) / kBKV;
-                for (int t = 0; t < ntiles; ++t, ++g) {
-                    const int st = g % kStages;
-                    const uint32_t ph = (uint32_t)(g / kStages) & 1;
-                    if (!ptx::mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag)) { fail(); break; }
-                    ptx::mbar_expect_tx(&bar->kv_full[st], kStageBytes);
-                    const int row = b * p.max_seq + k0 + t * kBKV;
-                    uint8_t *dst = sKV + st * kStageBytes;
-                    for (int a = 0; a < kLA; ++a)
-                        ptx::tma_load_2d_hint(dst + a * kAtom, &tmL, &bar->kv_full[st], (int)rank * kLA * 64 + a * 64,
-                                              row, stream);
-                    ptx::tma_load_2d_hint(dst + kLA * kAtom, &tmR, &bar->kv_full[st], (int)rank * 32, row, stream);
-                    pending[st] = (int)ph;
-                }
-            }
+        if (threadIdx.x == 0) {
+            while (ok && ld.valid)
+                if (!issue_load()) { fail(); break; }
             // Copies still in flight land before the CTA may exit.
             volatile int never = 0;
             for (int i = 0; i < kStages; ++i)
                 if (pending[i] >= 0) ptx::mbar_wait(&bar->kv_full[i], (uint32_t)pending[i], &never);
-            if (q_pending >= 0) ptx::mbar_wait(&bar->q_full, (uint32_t)q_pending, &never);
         }
     } else if (warp == 1) {
         if (ptx::elect_one()) {
@@ -372,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ready, P.V first (it frees a KV stage for the next load).
             constexpr uint32_t idesc_s = ptx::idesc_bf16(kH, kBKV, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, kLA * 64, false, true);
-            const uint32_t kv0 = ptx::smem_u32(sKV), q0 = ptx::smem_u32(sQ);
+            const uint32_t kv0 = ptx::smem_u32(sKV), p0 = ptx::smem_u32(smem + kOffP);
             TileCursor qk, pv;
             qk.init(p.prefix, p.B, cid, chunk);
             pv.init(p.prefix, p.B, cid, chunk);
@@ -387,11 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_fence_after();
                         const int st = pv.g % kStages;
                         const uint32_t vb = kv0 + st * kStageBytes;
-                        const uint32_t pa = tmem + kPCol + (pv.g & 1) * (kBKV / 2);
+                        const uint32_t pa = p0 + (pv.g & 1) * kPBytes;
 #pragma unroll
                         for (int k = 0; k < kBKV / 16; ++k)
-                            ptx::mma_f16_tmem_a(tmem, pa + k * 8, ptx::sdesc_sw128(vb + k * 2048, kAtom, 1024),
-                                                idesc_o, (pv.t == 0 && k == 0) ? 0u : 1u);
+                            ptx::mma_bf16(tmem, sdesc_plain(pa + k * 256, 128, kPGroup),
+                                          ptx::sdesc_sw128(vb + k * 2048, kAtom, 1024), idesc_o,
+                                          (pv.t == 0 && k == 0) ? 0u : 1u);
                         ptx::mma_commit(&bar->kv_empty[st]);
                         ptx::mma_commit(&bar->pv_done[pv.g & 1]);
                         pv.step();
@@ -400,24 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (qk.valid) {
                     const int st = qk.g % kStages, sb = qk.g % kSBuf;
-                    bool ready = qk.t > 0 || (ptx::mbar_test(ptx::smem_u32(&bar->q_full), qk.nseg & 1) &&
-                                              ptx::mbar_test(ptx::smem_u32(&bar->qr_full), qk.nseg & 1));
+                    bool ready = qk.t > 0 || ptx::mbar_test(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
                     ready = ready && ptx::mbar_test(ptx::smem_u32(&bar->kv_full[st]), (qk.g / kStages) & 1);
-                    // Score buffer sb held tile g - 4: the softmax must have read it.
+                    // Score buffer sb held tile g - 2: the softmax must have read it.
                     ready = ready && (qk.g < kSBuf ||
                                       ptx::mbar_test(ptx::smem_u32(&bar->s_free[sb]), ((qk.g / kSBuf) - 1) & 1));
                     if (ready) {
                         ptx::tc_fence_after();
                         const uint32_t kb = kv0 + st * kStageBytes;
                         const uint32_t d = tmem + kSCol + sb * kBKV;
-                        // K steps 0..15: latent (query and keys in 128-byte
-                        // swizzled atoms); 16..17: rope (query in tensor
-                        // memory, keys 64-byte swizzled).
+                        // K steps 0..15: latent (keys in 128-byte swizzled
+                        // atoms); 16..17: rope (keys 64-byte swizzled); the
+                        // query is read from tensor memory.
 #pragma unroll
                         for (int k = 0; k < 16; ++k)
-                            ptx::mma_bf16(d, ptx::sdesc_sw128(q0 + (k >> 2) * kQAtom + (k & 3) * 32, 16, 1024),
-                                          ptx::sdesc_sw128(kb + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024), idesc_s,
-                                          k != 0);
+                            ptx::mma_f16_tmem_a(d, tmem + kQCol + k * 8,
+                                                ptx::sdesc_sw128(kb + (k >> 2) * kAtom + (k & 3) * 32, 16, 1024),
+                                                idesc_s, k != 0);
 #pragma unroll
                         for (int k = 0; k < 2; ++k)
                             ptx::mma_f16_tmem_a(d, tmem + kQRCol + k * 8,
@@ -433,65 +417,117 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        const int quad = warp % 4;
+        // Softmax warps 2..9: warp w serves the tensor-memory lane quarter
+        // w % 4 (head rows 32 (w % 4) + lane); warps 2..5 take the even tiles
+        // and warps 6..9 the odd ones, each thread the whole row of its tile,
+        // so two tiles are in flight.  The running reference max passes
+        // from one group to the other tile by tile through shared memory,
+        // ordered by a producer/consumer named barrier per lane quarter.
+        const int quad = warp % 4, grp = (warp - 2) / 4;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-        uint32_t peer_xbuf[2], peer_xfull[2], peer_xfree[2];
-        uint32_t *my_stage = reinterpret_cast<uint32_t *>(smem + kOffStage) + h * kXStride;
-        for (int i = 0; i < 2; ++i) {
-            peer_xbuf[i] = map_peer((const uint8_t *)sX + i * kXBytes, peer);
-            peer_xfull[i] = map_peer(&bar->x_full[i], peer);
-            peer_xfree[i] = map_peer(&bar->x_free[i], peer);
-        }
-        // This CTA's 32 rope query columns of row h into tensor memory (lanes
-        // = heads, bf16 pairs per 32-bit column, lower column in the low
-        // half, which is how consecutive bf16 values sit in memory).
-        auto load_qr = [&](int b, int nseg) -> bool {
+        float *mslot = reinterpret_cast<float *>(smem + kOffRed);  // [2][kH] reference max after tile g (slot g & 1)
+        uint32_t hand_in = 0, nseg_done = 0;                       // handoffs received, segments finished
+        float *eslot = mslot + 2 * kH;                             // [2 groups][2][kH] (max, sum) at a segment end
+        const int xblk = quad * kXWarpBytes;                       // this warp's block of an exchange buffer
+        uint8_t *wstage = smem + kOffStage + grp * kXBytes + xblk;
+        uint32_t *my_stage = reinterpret_cast<uint32_t *>(wstage + lane * kXRowBytes);
+        const uint32_t peer_xbuf = map_peer(smem + kOffX + grp * kXBytes + xblk, peer);
+        const uint32_t peer_xfull = map_peer(&bar->x_full[grp], peer);
+        const uint32_t peer_xfree = map_peer(&bar->x_free[grp], peer);
+        // This CTA's 288 query columns of row h into tensor memory (lanes =
+        // heads, bf16 pairs per 32-bit column, lower column in the low half,
+        // which is how consecutive bf16 values sit in memory), written by the
+        // group that sends the segment's first tile.
+        auto load_q = [&](int b, int nseg) -> bool {
             if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) return false;
             ptx::tc_fence_after();
             const bool row_ok = h < p.H;
+            const uint4 *src = reinterpret_cast<const uint4 *>(q_abs + ((int64_t)b * p.H + h) * kRLat + rank * kOCols);
             const uint4 *rs = reinterpret_cast<const uint4 *>(q_rope + ((int64_t)b * p.H + h) * 64 + rank * 32);
-            uint32_t w[16];
+            // Two 128-byte groups of the row in flight at a time.
+            uint4 va[8], vb[8], vr[4];
+            auto fetch = [&](uint4 (&v)[8], int c) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 v = row_ok ? rs[i] : make_uint4(0, 0, 0, 0);
-                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+                for (int i = 0; i < 8; ++i) v[i] = row_ok ? src[c * 8 + i] : make_uint4(0, 0, 0, 0);
+            };
+            auto put = [&](const uint4 (&v)[8], int c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    w[4 * i] = v[i].x; w[4 * i + 1] = v[i].y; w[4 * i + 2] = v[i].z; w[4 * i + 3] = v[i].w;
+                }
+                ptx::tmem_st32(tmem + lane_off + kQCol + c * 32, w);
+            };
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vr[i] = row_ok ? rs[i] : make_uint4(0, 0, 0, 0);
+            fetch(va, 0);
+            fetch(vb, 1);
+            put(va, 0);
+            fetch(va, 2);
+            put(vb, 1);
+            fetch(vb, 3);
+            put(va, 2);
+            put(vb, 3);
+            {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    w[4 * i] = vr[i].x; w[4 * i + 1] = vr[i].y; w[4 * i + 2] = vr[i].z; w[4 * i + 3] = vr[i].w;
+                }
+                ptx::tmem_st16(tmem + lane_off + kQRCol, w);
             }
-            ptx::tmem_st16(tmem + lane_off + kQRCol, w);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bar->qr_full);
+            ptx::mbar_arrive(&bar->q_full);
             return true;
         };
-        // Read this thread's score row of tile g and send it into the peer's
-        // exchange buffer g & 1.
+        // Row h of the partial scores of this group's tiles, scaled to log2
+        // units and rounded to fp16: the current tile's and the one sent ahead.
+        uint32_t own[kBKV / 2], own_next[kBKV / 2];
+        // Read the partial of tile g into own_next, free its score buffer,
+        // stage it and copy the warp's block into the peer's buffer grp.
         auto send = [&](int g) -> bool {
             const int sb = g % kSBuf;
             if (!ptx::mbar_wait(&bar->s_full[sb], (g / kSBuf) & 1, abort_flag)) return false;
-            if (!ptx::mbar_wait_cluster(&bar->x_free[g & 1], ((g >> 1) & 1) ^ 1, abort_flag)) return false;
+            if (!ptx::mbar_wait_cluster(&bar->x_free[grp], ((g >> 1) & 1) ^ 1, abort_flag)) return false;
             ptx::tc_fence_after();
             uint32_t r0[32], r1[16];
             ptx::tmem_ld32(tmem + lane_off + kSCol + sb * kBKV, r0);
             ptx::tmem_ld16(tmem + lane_off + kSCol + sb * kBKV + 32, r1);
             ptx::tmem_ld_wait();
-            uint32_t w[kBKV / 2];
-            pack_partial(r0, r1, p.scale_log2, w);
-            // Stage the row locally (the previous bulk copy has finished
-            // reading the staging buffer: its issuer waited before the last
-            // softmax barrier); one thread then copies all rows to the peer.
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar->s_free[sb]);  // score buffer sb may take tile g + 2
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                own_next[j] = pack_f16_sat(__uint_as_float(r0[2 * j]) * p.scale_log2,
+                                           __uint_as_float(r0[2 * j + 1]) * p.scale_log2);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                own_next[16 + j] = pack_f16_sat(__uint_as_float(r1[2 * j]) * p.scale_log2,
+                                                __uint_as_float(r1[2 * j + 1]) * p.scale_log2);
+            // Stage the row once the warp's previous copy has read its block,
+            // then one lane copies the warp's block to the peer.
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < kBKV / 8; ++c)
-                *reinterpret_cast<uint4 *>(my_stage + 4 * c) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                *reinterpret_cast<uint4 *>(my_stage + 4 * c) =
+                    make_uint4(own_next[4 * c], own_next[4 * c + 1], own_next[4 * c + 2], own_next[4 * c + 3]);
             ptx::fence_proxy_async_smem();
-            stage_bar();
-            if (h == 0) bulk_to_peer(peer_xbuf[g & 1], smem + kOffStage, kXBytes, peer_xfull[g & 1]);
+            __syncwarp();
+            if (lane == 0) bulk_to_peer(peer_xbuf, wstage, kXWarpBytes, peer_xfull);
             return true;
         };
-        TileCursor nx;  // the tile after the current one (the send runs one tile ahead)
+        TileCursor nx;  // the next tile of this group to send (sends run two tiles ahead)
         nx.init(p.prefix, p.B, cid, chunk);
-        if (nx.valid) {
-            if (!load_qr(nx.b, 0) || !send(0)) fail();
+        if (grp == 1 && nx.valid) nx.step();
+        if (ok && nx.valid) {
+            if ((nx.t == 0 && !load_q(nx.b, nx.nseg)) || !send(nx.g)) fail();
+#pragma unroll
+            for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];
             nx.step();
+            if (nx.valid) nx.step();
         }
         SegIter it;
         it.init(p.prefix, p.B, cid, chunk);
@@ -499,60 +535,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool whole;
         int g = 0;
         while (ok && it.next(b, k0, k1, whole)) {
-            float m_run = -INFINITY, l_run = 0.f;
+            // The reference max this group last used and its share of the
+            // row sum (relative to that max).
+            float m_grp = -INFINITY, l_grp = 0.f;
             const int len = k1 - k0;
             const int ntiles = (len + kBKV - 1) / kBKV;
             for (int t = 0; t < ntiles; ++t, ++g) {
+                if ((g & 1) != grp) continue;
                 const int valid = min(kBKV, len - t * kBKV);
-                const int xb = g & 1, sb = g % kSBuf;
-                // 1. Full scores of tile g: own partial (still in tensor
-                //    memory) plus the peer's, same operand order in both CTAs.
-                if (!ptx::mbar_wait_cluster(&bar->x_full[xb], (g >> 1) & 1, abort_flag)) { fail(); break; }
+                // 1. Scores of tile g: the two fp16-rounded partials, added
+                //    identically in both CTAs.
+                if (!ptx::mbar_wait_cluster(&bar->x_full[grp], (g >> 1) & 1, abort_flag)) { fail(); break; }
                 float s[kBKV];
+                float mt = -INFINITY;
                 {
-                    uint32_t r0[32], r1[16];
-                    ptx::tmem_ld32(tmem + lane_off + kSCol + sb * kBKV, r0);
-                    ptx::tmem_ld16(tmem + lane_off + kSCol + sb * kBKV + 32, r1);
-                    ptx::tmem_ld_wait();
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(&bar->s_free[sb]);  // score buffer sb may take tile g + 4
-                    uint32_t w[kBKV / 2];
-                    pack_partial(r0, r1, p.scale_log2, w);
-                    const uint32_t *xr = reinterpret_cast<const uint32_t *>(sX) + xb * (kXBytes / 4) + h * kXStride;
+                    const uint32_t *xr =
+                        reinterpret_cast<const uint32_t *>(smem + kOffX + grp * kXBytes + xblk + lane * kXRowBytes);
 #pragma unroll
                     for (int c = 0; c < kBKV / 8; ++c) {
                         const uint4 v = *reinterpret_cast<const uint4 *>(xr + 4 * c);
                         const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float2 a = unpack_f16(w[4 * c + i]), b = unpack_f16(pw[i]);
-                            s[8 * c + 2 * i] = a.x + b.x;
-                            s[8 * c + 2 * i + 1] = a.y + b.y;
+                            const float2 a = unpack_f16(own[4 * c + i]), bb = unpack_f16(pw[i]);
+                            s[8 * c + 2 * i] = a.x + bb.x;
+                            s[8 * c + 2 * i + 1] = a.y + bb.y;
                         }
                     }
-                }
-                if (h == 0) bulk_wait_read();  // the staging buffer may be rewritten
-                softmax_bar();  // every row of exchange buffer xb has been read
-                if (h == 0) {
-                    ptx::mbar_expect_tx(&bar->x_full[xb], kXTx);  // arm its next use (tile g + 2)
-                    arrive_remote_relaxed(peer_xfree[xb]);        // the peer may overwrite it
-                }
-                // 2. The next tile: its rope query (at a segment boundary) and its partial.
-                if (nx.valid) {
-                    if (nx.t == 0 && !load_qr(nx.b, nx.nseg)) { fail(); break; }
-                    if (!send(g + 1)) { fail(); break; }
-                    nx.step();
-                }
-                // 3. Online softmax of tile g.
-                float mt = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < kBKV; ++j) {
-                    s[j] = (j < valid) ? s[j] : -INFINITY;
-                    mt = fmaxf(mt, s[j]);
+                    for (int j = 0; j < kBKV; ++j) {
+                        s[j] = (j < valid) ? s[j] : -INFINITY;
+                        mt = fmaxf(mt, s[j]);
+                    }
                 }
-                const bool resc = mt > m_run + kRescaleThreshold;
-                const float m_new = resc ? mt : m_run;
-                const float corr = exp2f(m_run - m_new);
+                // The warp's block of exchange buffer grp is read: the peer may
+                // overwrite it once the group's four warps said so (the
+                // group's first warp re-arms the buffer's barrier first).
+                __syncwarp();
+                if (lane == 0) {
+                    if (h == 0) ptx::mbar_expect_tx(&bar->x_full[grp], kXTx);
+                    arrive_remote_relaxed(peer_xfree);
+                }
+                // 2. Reference max after tile g: the previous tile's (from the
+                //    other group) raised only when this tile exceeds it by
+                //    more than the threshold.
+                float m_prev = -INFINITY;
+                if (t > 0) {
+                    if (!ptx::mbar_wait(&bar->hand[grp ^ 1][quad], hand_in & 1, abort_flag)) { fail(); break; }
+                    ++hand_in;
+                    m_prev = mslot[((g - 1) & 1) * kH + h];
+                }
+                const float m_new = (mt > m_prev + kRescaleThreshold) ? mt : m_prev;
+                mslot[(g & 1) * kH + h] = m_new;
+                if (t + 1 < ntiles) ptx::mbar_arrive(&bar->hand[grp][quad]);
+                // 3. The group's next tile: its query (at a segment boundary) and its partial.
+                if (nx.valid) {
+                    if (nx.t == 0 && !load_q(nx.b, nx.nseg)) { fail(); break; }
+                    if (!send(nx.g)) { fail(); break; }
+                    nx.step();
+                    if (nx.valid) nx.step();
+                }
+                // 4. P = 2^(s - m_new) (bf16) and the group's row sum.
                 float psum = 0.f;
                 uint32_t pk[kBKV / 2];
 #pragma unroll
@@ -561,16 +604,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     psum += a0 + a1;
                     pk[j] = ptx::pack_bf16(a0, a1);
                 }
-                l_run = l_run * corr + psum;
-                m_run = m_new;
-                // P buffer g & 1 held P(g - 2): wait for P.V(g - 2).  Each
+                l_grp = l_grp * exp2f(m_grp - m_new) + psum;
+                m_grp = m_new;
+#pragma unroll
+                for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];
+                // P buffer grp held P(g - 2): wait for P.V(g - 2).  Each
                 // pv_done barrier is waited on phase by phase, never two
                 // phases behind (P.V(g) cannot finish before P(g) exists).
-                if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[xb], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
-                if (resc && t > 0) {
-                    // O must hold every earlier P.V before it is rescaled.
-                    if (!ptx::mbar_wait(&bar->pv_done[xb ^ 1], ((g - 1) >> 1) & 1, abort_flag)) { fail(); break; }
+                if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[grp], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                if (t > 0 && m_new != m_prev) {
+                    // Raised: O must hold every earlier P.V before it is
+                    // rescaled to the new reference.
+                    if (!ptx::mbar_wait(&bar->pv_done[grp ^ 1], ((g - 1) >> 1) & 1, abort_flag)) { fail(); break; }
                     ptx::tc_fence_after();
+                    const float corr = exp2f(m_prev - m_new);
 #pragma unroll 1
                     for (int c = 0; c < kOCols; c += 32) {
                         uint32_t o[32];
@@ -580,11 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
                         ptx::tmem_st32(tmem + lane_off + c, o);
                     }
+                    ptx::tmem_st_wait();
                 }
-                ptx::tc_fence_after();
-                ptx::tmem_st16(tmem + lane_off + kPCol + xb * (kBKV / 2), pk);
-                ptx::tmem_st8(tmem + lane_off + kPCol + xb * (kBKV / 2) + 16, pk + 16);
-                ptx::tmem_st_wait();
+                {
+                    uint8_t *prow = smem + kOffP + grp * kPBytes + (h >> 3) * kPGroup + (h & 7) * 16;
+#pragma unroll
+                    for (int c = 0; c < kBKV / 8; ++c)
+                        *reinterpret_cast<uint4 *>(prow + c * 128) =
+                            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                }
                 if (valid < kBKV) {
                     // Rows past the segment may hold arbitrary cache contents;
                     // P is 0 there, but 0 * NaN is not 0: zero those rows.
@@ -595,48 +646,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                         *reinterpret_cast<uint4 *>(stg + a * kAtom + (valid + rr) * 128 + ch * 16) =
                             make_uint4(0, 0, 0, 0);
                     }
-                    ptx::fence_proxy_async_smem();
                 }
+                ptx::fence_proxy_async_smem();  // P and zeroed rows visible to the tensor core
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(&bar->p_full[xb]);
+                ptx::mbar_arrive(&bar->p_full[grp]);
             }
             if (!ok) break;
-            // Segment done: read the accumulator once its last P.V completed.
-            if (!ptx::mbar_wait(&bar->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag)) { fail(); break; }
+            // Segment done: the two groups' (max, sum) give the row sum
+            // relative to the final reference max; then each group stores
+            // half of the accumulator's columns once its last P.V completed.
+            eslot[(grp * 2) * kH + h] = m_grp;
+            eslot[(grp * 2 + 1) * kH + h] = l_grp;
+            ptx::mbar_arrive(&bar->seg[quad]);
+            if (!ptx::mbar_wait(&bar->seg[quad], nseg_done & 1, abort_flag)) { fail(); break; }
+            ++nseg_done;
+            const float m_o = eslot[((grp ^ 1) * 2) * kH + h], l_o = eslot[((grp ^ 1) * 2 + 1) * kH + h];
+            const float m_fin = fmaxf(m_grp, m_o);
+            const float l_tot = l_grp * exp2f(m_grp - m_fin) + (m_o == -INFINITY ? 0.f : l_o * exp2f(m_o - m_fin));
+            const int gl = g - 1;  // last tile of the segment
+            if (!ptx::mbar_wait(&bar->pv_done[gl & 1], (gl >> 1) & 1, abort_flag)) { fail(); break; }
             ptx::tc_fence_after();
-            const bool row_ok = h < p.H;
             const int slot = cid + b;
+            // Each warp stages 32 rows x 64 bytes at a time in its group's P
+            // buffer (free: every P.V of the segment has completed), so the
+            // global stores go out as 64-byte row pieces: fp32 partials 16
+            // columns per chunk, bf16 outputs 32.  The 16-byte pieces of a
+            // row are rotated by (row / 2) % 4 against bank conflicts.
+            uint8_t *wst = smem + kOffP + grp * kPBytes + quad * 2048;
+            const int rd_row = lane >> 2, rd_piece = lane & 3;
+            const int ncols = whole ? 32 : 16;
 #pragma unroll 1
-            for (int c = 0; c < kOCols; c += 32) {
-                uint32_t o[32];
-                ptx::tmem_ld32(tmem + lane_off + c, o);
-                ptx::tmem_ld_wait();
-                if (!row_ok) continue;
-                const int col = (int)rank * kOCols + c;
+            for (int c = grp * (kOCols / 2); c < (grp + 1) * (kOCols / 2); c += ncols) {
+                uint32_t w[16];
                 if (whole) {
-                    const float inv = 1.f / l_run;
-                    bf16 *dst = p.o_lat + ((int64_t)b * p.H + h) * kRLat + col;
+                    uint32_t o[32];
+                    ptx::tmem_ld32(tmem + lane_off + c, o);
+                    ptx::tmem_ld_wait();
+                    const float inv = 1.f / l_tot;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 w;
-                        w.x = ptx::pack_bf16(__uint_as_float(o[j]) * inv, __uint_as_float(o[j + 1]) * inv);
-                        w.y = ptx::pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-                        w.z = ptx::pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
-                        w.w = ptx::pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(dst + j) = w;
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        w[j] = ptx::pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
                 } else {
-                    float *dst = p.o_part + ((int64_t)slot * p.H + h) * kRLat + col;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dst + j) =
-                            make_float4(__uint_as_float(o[j]), __uint_as_float(o[j + 1]),
-                                        __uint_as_float(o[j + 2]), __uint_as_float(o[j + 3]));
+                    ptx::tmem_ld16(tmem + lane_off + c, w);
+                    ptx::tmem_ld_wait();
                 }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4 *>(wst + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
+                        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = rd_row + 8 * k;               // row within the warp
+                    const int hr = quad * 32 + r;               // head
+                    const uint4 v = *reinterpret_cast<const uint4 *>(wst + r * 64 + ((rd_piece ^ ((r >> 1) & 3)) * 16));
+                    if (hr < p.H) {
+                        const int col = (int)rank * kOCols + c;
+                        if (whole)
+                            *reinterpret_cast<uint4 *>(p.o_lat + ((int64_t)b * p.H + hr) * kRLat + col + rd_piece * 8) = v;
+                        else
+                            *reinterpret_cast<uint4 *>(p.o_part + ((int64_t)slot * p.H + hr) * kRLat + col + rd_piece * 4) = v;
+                    }
+                }
+                __syncwarp();
             }
-            if (row_ok && !whole && rank == 0) {
-                p.ml_part[((int64_t)slot * p.H + h) * 2] = m_run;
-                p.ml_part[((int64_t)slot * p.H + h) * 2 + 1] = l_run;
+            const bool row_ok = h < p.H;
+            if (row_ok && !whole && rank == 0 && grp == 0) {
+                p.ml_part[((int64_t)slot * p.H + h) * 2] = m_fin;
+                p.ml_part[((int64_t)slot * p.H + h) * 2 + 1] = l_tot;
             }
             ptx::tc_fence_before();
             ptx::mbar_arrive(&bar->o_empty);
@@ -740,10 +817,8 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
 {
     CUtensorMap tl, tr;
     const int64_t c_rows = (int64_t)a.max_batch * a.max_seq;
-    CUtensorMap tq;
     if (!make_tmap_bf16(&tl, a.lat, c_rows, kRLat, a.lat_stride, 64, kBKV) ||
-        !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV) ||
-        !make_tmap_bf16(&tq, a.q_abs, (int64_t)a.B * a.H, kRLat, kRLat, 64, kH))
+        !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV))
         return cudaErrorInvalidValue;
     decode_schedule_kernel<<<1, 1024, 0, s>>>(a.seq_lens, a.B, a.max_seq, a.n_clusters, a.prefix, a.chunk,
                                               a.status);
@@ -774,7 +849,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     profile_begin(MLA_PROFILE_DECODE_ATTENTION, s);
-    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tl, tr, tq, (const bf16 *)a.q_rope, p);
+    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tl, tr, (const bf16 *)a.q_abs, (const bf16 *)a.q_rope, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
     if (e != cudaSuccess) return e;
