@@ -60,8 +60,9 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     nt = r / gm;
 }
 
-// Epilogue of one accumulator row chunk of NC columns (32 or 64) starting at
-// output column n0 of row m of batch entry z.
+// Epilogue of one accumulator row chunk of NC columns (8, 32 or 64; RoPE in
+// the half-split form needs whole 64-column groups) starting at output
+// column n0 of row m of batch entry z.
 template <int NC>
 __device__ __forceinline__ void store_chunk(const TcGemmParams &p, int z, int m, int n0, float (&v)[64])
 {
@@ -307,7 +308,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Sum of the split-K partials of one NC-column chunk of one row, then the
-// usual epilogue (RoPE, cache scatter, conversion).
+// usual epilogue (RoPE, cache scatter, conversion).  With NC = 8 a warp
+// reads 1 KB of each split's partials contiguously; the partial loads of all
+// splits are issued before the sums (they are independent).
 template <int NC>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(TcGemmParams p)
 {
@@ -318,11 +321,28 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(TcGemmParams p)
     float v[64];
 #pragma unroll
     for (int j = 0; j < NC; ++j) v[j] = 0.f;
-    for (int ks = 0; ks < p.splits; ++ks) {
-        const float4 *src = reinterpret_cast<const float4 *>(p.partial + ((int64_t)ks * p.M + m) * p.N + n0);
+    const int64_t split_stride = (int64_t)p.M * p.N / 4;
+    const float4 *src = reinterpret_cast<const float4 *>(p.partial + (int64_t)m * p.N + n0);
+    int ks = 0;
+    if (NC == 8) {
+        for (; ks + 4 <= p.splits; ks += 4) {
+            float4 w[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                w[u][0] = __ldcs(src + (ks + u) * split_stride);
+                w[u][1] = __ldcs(src + (ks + u) * split_stride + 1);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                v[0] += w[u][0].x; v[1] += w[u][0].y; v[2] += w[u][0].z; v[3] += w[u][0].w;
+                v[4] += w[u][1].x; v[5] += w[u][1].y; v[6] += w[u][1].z; v[7] += w[u][1].w;
+            }
+        }
+    }
+    for (; ks < p.splits; ++ks) {
 #pragma unroll
         for (int j = 0; j < NC / 4; ++j) {
-            const float4 w = src[j];
+            const float4 w = __ldcs(src + ks * split_stride + j);
             v[4 * j] += w.x;
             v[4 * j + 1] += w.y;
             v[4 * j + 2] += w.z;
@@ -391,8 +411,8 @@ GemmPlan gemm_tc_plan(const GemmArgs &a, int num_sms)
     else if (a.N % 128 == 0 && tiles(128) >= num_sms) pl.bn = 128;
     pl.splits = 1;
     const int nk = (a.K + kBK - 1) / kBK;
-    const int t64 = tiles(64);
-    if (t64 < num_sms && a.batch == 1 && a.epi.batch_stride == 0 && nk >= 2 && !a.trans_b) {
+    const bool skinny = a.M <= kBM;  // one row tile: the GEMM streams the weights once
+    if ((skinny || tiles(64) < num_sms) && a.batch == 1 && a.epi.batch_stride == 0 && !a.trans_b) {
         // Estimated time ~ bytes moved (weights, plus the fp32 partials written
         // and read back) / fraction of the SMs kept busy over whole waves.
         const double wbytes = 2.0 * a.N * a.K + 2.0 * a.M * a.K;
@@ -402,10 +422,10 @@ GemmPlan gemm_tc_plan(const GemmArgs &a, int num_sms)
             return (wbytes + (sp > 1 ? 8.0 * sp * a.M * a.N : 0.0)) / eff;
         };
         double best = cost(tiles(pl.bn), 1);
-        for (int bn : {128, 64}) {
-            if (bn == 128 && a.N % 128) continue;
+        for (int bn : {256, 128, 64}) {
+            if (a.N % bn && bn != 64) continue;
             const int t = tiles(bn);
-            for (int sp = 2; sp <= std::min(nk, 64); ++sp) {
+            for (int sp = 1; sp <= std::min(nk, 64); ++sp) {
                 const int kbps = (nk + sp - 1) / sp;
                 const int real = (nk + kbps - 1) / kbps;
                 const double c = cost(t * real, real);
@@ -458,11 +478,11 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (pl.splits > 1) {
-        const int nc = a.epi.rope_mode == kRopeHalf ? 64 : 32;
+        const int nc = a.epi.rope_mode == kRopeHalf ? 64 : 8;
         const int64_t threads = (int64_t)a.M * (a.N / nc);
         const unsigned blocks = (unsigned)((threads + 255) / 256);
         if (nc == 64) splitk_reduce_kernel<64><<<blocks, 256, 0, s>>>(p);
-        else splitk_reduce_kernel<32><<<blocks, 256, 0, s>>>(p);
+        else splitk_reduce_kernel<8><<<blocks, 256, 0, s>>>(p);
         note_launch();
         e = cudaGetLastError();
     }
