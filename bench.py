@@ -36,6 +36,11 @@ METRIC = "MLA decode latent-cache HBM GB/s (% of peak); prefill TFLOP/s (% bf16 
 DECODE = syn.WORKLOADS["dsv2_decode"]
 PREFILL = syn.WORKLOADS["dsv2_prefill"]
 L2_FLUSH_BYTES = 512 << 20
+# DRAM bytes (read + write) of one decode attention launch on this workload,
+# from an ncu capture of the current kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum); None whenever the kernel changes until it is
+# captured again.
+DECODE_TRAFFIC_BYTES = int(213.58e6 + 4.32e6)
 
 
 def peaks():
@@ -317,7 +322,8 @@ def run_ours(args, rank, world, device):
         "roofline": {"bound": "hbm", "kernel": "decode split-KV latent attention",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
-                     "kernel_ms": round(kms, 5), "traffic": None},
+                     "kernel_ms": round(kms, 5), "traffic": DECODE_TRAFFIC_BYTES,
+                     "traffic_unit": "bytes per launch"},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
