@@ -76,25 +76,84 @@ struct ProjGemms {
     int n = 0;
 };
 
-ProjGemms project_gemms(const mla_config &c, int64_t T)
+// The projection GEMMs of mla_project_latent, as they are launched (the
+// pointers may be null when only the workspace is being sized).  Products
+// that read the same input form one segment list; a decode-sized bfloat16
+// call launches each list as one grouped weight-streaming GEMM, any other
+// call one GEMM per product.
+ProjGemms project_gemms(const mla_handle *h, int64_t T, bool allow_group, const mla_weights *w = nullptr,
+                        const void *x = nullptr, const int32_t *seq_idx = nullptr, const int32_t *pos = nullptr,
+                        const mla_cache *cache = nullptr, void *q_nope = nullptr, void *q_rope = nullptr,
+                        void *cq = nullptr)
 {
-    ProjGemms r;
+    const mla_config &c = h->cfg;
     const int M = (int)T, H = c.n_heads;
-    auto lin = [&](int N, int K) {
-        GemmArgs g;
-        g.A = Mat2D{nullptr, M, K, K};
-        g.B = Mat2D{nullptr, N, K, K};
-        g.M = M; g.N = N; g.K = K;
-        return g;
+    const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
+    Epilogue e_lat;
+    e_lat.out = cache ? cache->lat : nullptr;
+    e_lat.ldc = cache ? cache->lat_stride : c.r_kv;
+    e_lat.row_seq = seq_idx; e_lat.row_pos = pos; e_lat.seq_rows = c.max_seq;
+    e_lat.max_batch = c.max_batch; e_lat.max_seq = c.max_seq;
+    Epilogue e_rope = e_lat;
+    e_rope.out = cache ? cache->rope : nullptr;
+    e_rope.ldc = cache ? cache->rope_stride : c.d_rope;
+    e_rope.rope_mode = kRopeInterleaved; e_rope.rope_dim = c.d_rope;
+    e_rope.rope_table = h->rope_table; e_rope.rope_pos = pos;
+    Epilogue e_cq;
+    e_cq.out = cq; e_cq.ldc = c.r_q;
+    Epilogue e_qn;
+    e_qn.out = q_nope; e_qn.ldc = (int64_t)H * c.d_nope;
+    Epilogue e_qr;
+    e_qr.out = q_rope; e_qr.ldc = (int64_t)H * c.d_rope;
+    e_qr.rope_mode = kRopeInterleaved; e_qr.rope_dim = c.d_rope;
+    e_qr.rope_table = h->rope_table; e_qr.rope_pos = pos; e_qr.max_seq = c.max_seq;
+    if (c.variant == MLA_VARIANT_SMALL) {
+        e_qn.rope_mode = kRopeHalf; e_qn.rope_dim = c.d_nope;
+        e_qn.rope_table = h->rope_table; e_qn.rope_pos = pos; e_qn.max_seq = c.max_seq;
+    }
+    auto seg = [](const void *W, int N, int K, const Epilogue &e) {
+        GemmSegment s;
+        s.B = Mat2D{W, N, K, K};
+        s.epi = e;
+        s.N = N;
+        return s;
     };
-    r.g[r.n++] = lin(c.r_kv, c.d_model);
-    if (c.variant == MLA_VARIANT_DECOUPLED) {
-        r.g[r.n++] = lin(c.d_rope, c.d_model);
-        r.g[r.n++] = lin(c.r_q, c.d_model);
-        r.g[r.n++] = lin(H * c.d_nope, c.r_q);
-        r.g[r.n++] = lin(H * c.d_rope, c.r_q);
+    GemmSegment lists[2][kMaxSeg];
+    int nl[2] = {0, 0};
+    lists[0][nl[0]++] = seg(w ? w->W_DKV : nullptr, c.r_kv, c.d_model, e_lat);
+    if (dec) {
+        lists[0][nl[0]++] = seg(w ? w->W_KR : nullptr, c.d_rope, c.d_model, e_rope);
+        lists[0][nl[0]++] = seg(w ? w->W_DQ : nullptr, c.r_q, c.d_model, e_cq);
+        lists[1][nl[1]++] = seg(w ? w->W_UQ : nullptr, H * c.d_nope, c.r_q, e_qn);
+        lists[1][nl[1]++] = seg(w ? w->W_QR : nullptr, H * c.d_rope, c.r_q, e_qr);
     } else {
-        r.g[r.n++] = lin(H * c.d_nope, c.d_model);
+        lists[0][nl[0]++] = seg(w ? w->W_Q : nullptr, H * c.d_nope, c.d_model, e_qn);
+    }
+    const void *inputs[2] = {x, cq};
+    const int in_cols[2] = {c.d_model, c.r_q};
+    ProjGemms r;
+    for (int l = 0; l < 2; ++l) {
+        if (!nl[l]) continue;
+        GemmArgs g;
+        g.A = Mat2D{inputs[l], M, in_cols[l], in_cols[l]};
+        g.M = M;
+        g.K = in_cols[l];
+        g.nseg = nl[l];
+        for (int i = 0; i < nl[l]; ++i) g.seg[i] = lists[l][i];
+        if (allow_group && c.dtype == MLA_DTYPE_BF16 && M <= 128 && nl[l] > 1 && gemm_tc_supported(g)) {
+            r.g[r.n++] = g;
+            continue;
+        }
+        for (int i = 0; i < nl[l]; ++i) {
+            GemmArgs one;
+            one.A = g.A;
+            one.M = M;
+            one.K = g.K;
+            one.B = lists[l][i].B;
+            one.N = lists[l][i].N;
+            one.epi = lists[l][i].epi;
+            r.g[r.n++] = one;
+        }
     }
     return r;
 }
@@ -113,8 +172,11 @@ ProjectWs project_ws(const mla_handle *h, int64_t T)
     w.split = round_up(w.cq + n, 256);
     size_t sb = 0;
     if (T > 0 && T <= INT32_MAX) {
-        ProjGemms pg = project_gemms(c, T);
-        for (int i = 0; i < pg.n; ++i) sb = std::max(sb, split_bytes(h, pg.g[i]));
+        // Either launch form may run (grouping depends on the caller's strides).
+        for (bool grouped : {false, true}) {
+            const ProjGemms pg = project_gemms(h, T, grouped);
+            for (int i = 0; i < pg.n; ++i) sb = std::max(sb, split_bytes(h, pg.g[i]));
+        }
     }
     w.end = round_up(w.split + sb, 256);
     return w;
@@ -207,6 +269,8 @@ GemmArgs linear_args(const void *x, int64_t ldx, const void *W, int64_t ldw, int
 mla_status run_gemm(const mla_handle *h, GemmArgs g, uint32_t *status, cudaStream_t s, float *split = nullptr)
 {
     if (!g.epi.status) g.epi.status = status;
+    for (int i = 0; i < g.nseg; ++i)
+        if (!g.seg[i].epi.status) g.seg[i].epi.status = status;
     g.split_ws = split;
     if (h->cfg.dtype == MLA_DTYPE_BF16) {
         if (!gemm_tc_supported(g)) return MLA_ERR_UNSUPPORTED;
@@ -356,47 +420,13 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
     if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t *status = (uint32_t *)ws;
-    const int M = (int)T, H = c.n_heads;
     char *wsb = (char *)ws;
     float *split = (float *)(wsb + L.split);
 
-    // Latent and (decoupled) rope key, written straight into the caches.
-    GemmArgs g = linear_args(x, c.d_model, w->W_DKV, c.d_model, M, c.r_kv, c.d_model, cache->lat,
-                             cache->lat_stride);
-    g.epi.row_seq = seq_idx; g.epi.row_pos = pos; g.epi.seq_rows = c.max_seq;
-    g.epi.max_batch = c.max_batch; g.epi.max_seq = c.max_seq;
-    MLA_TRY(run_gemm(h, g, status, s, split));
-    if (dec) {
-        GemmArgs r = g;
-        r.B = Mat2D{w->W_KR, c.d_rope, c.d_model, c.d_model};
-        r.N = c.d_rope;
-        r.epi.out = cache->rope; r.epi.ldc = cache->rope_stride;
-        r.epi.rope_mode = kRopeInterleaved; r.epi.rope_dim = c.d_rope;
-        r.epi.rope_table = h->rope_table; r.epi.rope_pos = pos;
-        MLA_TRY(run_gemm(h, r, status, s, split));
-
-        void *cq = wsb + L.cq;
-        GemmArgs a = linear_args(x, c.d_model, w->W_DQ, c.d_model, M, c.r_q, c.d_model, cq, c.r_q);
-        MLA_TRY(run_gemm(h, a, status, s, split));
-        GemmArgs qn = linear_args(cq, c.r_q, w->W_UQ, c.r_q, M, H * c.d_nope, c.r_q, q_nope,
-                                  (int64_t)H * c.d_nope);
-        MLA_TRY(run_gemm(h, qn, status, s, split));
-        GemmArgs qr = linear_args(cq, c.r_q, w->W_QR, c.r_q, M, H * c.d_rope, c.r_q, q_rope,
-                                  (int64_t)H * c.d_rope);
-        qr.epi.rope_mode = kRopeInterleaved; qr.epi.rope_dim = c.d_rope;
-        qr.epi.rope_table = h->rope_table; qr.epi.rope_pos = pos;
-        qr.epi.max_seq = c.max_seq;
-        MLA_TRY(run_gemm(h, qr, status, s, split));
-    } else {
-        GemmArgs q = linear_args(x, c.d_model, w->W_Q, c.d_model, M, H * c.d_nope, c.d_model, q_nope,
-                                 (int64_t)H * c.d_nope);
-        if (c.variant == MLA_VARIANT_SMALL) {
-            q.epi.rope_mode = kRopeHalf; q.epi.rope_dim = c.d_nope;
-            q.epi.rope_table = h->rope_table; q.epi.rope_pos = pos;
-            q.epi.max_seq = c.max_seq;
-        }
-        MLA_TRY(run_gemm(h, q, status, s, split));
-    }
+    // Latent and (decoupled) rope key written straight into the caches, then
+    // the query projections.
+    const ProjGemms pg = project_gemms(h, T, true, w, x, seq_idx, pos, cache, q_nope, q_rope, dec ? wsb + L.cq : nullptr);
+    for (int i = 0; i < pg.n; ++i) MLA_TRY(run_gemm(h, pg.g[i], status, s, split));
     return MLA_OK;
 }
 

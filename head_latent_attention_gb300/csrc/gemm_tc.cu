@@ -33,7 +33,9 @@ struct TcGemmParams {
     int tiles_m, tiles_n;
     int splits, kb_per_split;  // split-K: unit u = (tile u % tiles, K slice u / tiles)
     float *partial;            // split-K partial sums [splits, M, N] (fp32), or null
-    Epilogue epi;
+    int nseg;                  // column segments: [seg_n0[i], seg_n0[i + 1]) uses epi[i]
+    int seg_n0[kMaxSeg + 1];
+    Epilogue epi[kMaxSeg];
     uint32_t *status;
 };
 
@@ -63,11 +65,22 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
 // Epilogue of one accumulator row chunk of NC columns (8, 32 or 64; RoPE in
 // the half-split form needs whole 64-column groups) starting at output
 // column n0 of row m of batch entry z.
-template <int NC>
-__device__ __forceinline__ void store_chunk(const TcGemmParams &p, int z, int m, int n0, float (&v)[64])
+// Segment of output column n (constant indices only: a dynamically indexed
+// kernel parameter would be copied to local memory).
+__device__ __forceinline__ int segment_of(const TcGemmParams &p, int n)
 {
-    const Epilogue &e = p.epi;
-    if (m >= p.M || n0 >= p.N) return;
+    return (p.nseg > 2 && n >= p.seg_n0[2]) ? 2 : ((p.nseg > 1 && n >= p.seg_n0[1]) ? 1 : 0);
+}
+__device__ __forceinline__ int segment_start(const TcGemmParams &p, int sg)
+{
+    return sg == 0 ? 0 : (sg == 1 ? p.seg_n0[1] : p.seg_n0[2]);
+}
+
+// Epilogue e applied to columns [n0, n0 + NC) of its segment.
+template <int NC>
+__device__ __forceinline__ void store_chunk_seg(const TcGemmParams &p, const Epilogue &e, int z, int m, int n0,
+                                                float (&v)[64])
+{
     if (e.rope_mode != kRopeNone) {
         const int pos = e.rope_pos ? e.rope_pos[m] : m;
         if (pos < 0 || pos >= e.max_seq) {
@@ -121,9 +134,22 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams &p, int z, int m,
     }
 }
 
+// Epilogue of one accumulator row chunk of NC columns starting at output
+// column ng (of the concatenated product) of row m of batch entry z.
+template <int NC>
+__device__ __forceinline__ void store_chunk(const TcGemmParams &p, int z, int m, int ng, float (&v)[64])
+{
+    if (m >= p.M || ng >= p.N) return;
+    const int sg = segment_of(p, ng);
+    if (sg == 0) store_chunk_seg<NC>(p, p.epi[0], z, m, ng, v);
+    else if (sg == 1) store_chunk_seg<NC>(p, p.epi[1], z, m, ng - p.seg_n0[1], v);
+    else store_chunk_seg<NC>(p, p.epi[2], z, m, ng - p.seg_n0[2], v);
+}
+
 template <int BN, bool kBMN>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
                    TcGemmParams p)
 {
     using C = Cfg<BN>;
@@ -166,7 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (ptx::elect_one()) {
             ptx::prefetch_tmap(&tmA);
-            ptx::prefetch_tmap(&tmB);
+            ptx::prefetch_tmap(&tmB0);
+            if (p.nseg > 1) ptx::prefetch_tmap(&tmB1);
+            if (p.nseg > 2) ptx::prefetch_tmap(&tmB2);
             int stage = 0;
             uint32_t phase = 0;
             int pending[S];
@@ -178,19 +206,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks = u / num_tiles;
                 const int kb0 = ks * p.kb_per_split, kb1 = min(nk, kb0 + p.kb_per_split);
                 const int ax = (int)(z * p.a_col_batch), ay = (int)(z * p.a_row_batch) + mt * kBM;
+                const int sg = segment_of(p, nt * BN);
+                const CUtensorMap *tmB = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
+                const int brow = nt * BN - segment_start(p, sg);  // first weight row of the tile in its segment
                 for (int kb = kb0; kb < kb1; ++kb) {
                     if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
                     ptx::mbar_expect_tx(&full[stage], C::kStageBytes);
                     ptx::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], ax + kb * kBK, ay);
                     uint8_t *dB = sB + stage * C::kBBytes;
                     if (!kBMN) {
-                        ptx::tma_load_2d(dB, &tmB, &full[stage], (int)(z * p.b_col_batch) + kb * kBK,
-                                         (int)(z * p.b_row_batch) + nt * BN);
+                        ptx::tma_load_2d(dB, tmB, &full[stage], (int)(z * p.b_col_batch) + kb * kBK,
+                                         (int)(z * p.b_row_batch) + brow);
                     } else {
 #pragma unroll
                         for (int a = 0; a < BN / 64; ++a)
-                            ptx::tma_load_2d(dB + a * (kBK * 128), &tmB, &full[stage],
-                                             (int)(z * p.b_col_batch) + nt * BN + a * 64,
+                            ptx::tma_load_2d(dB + a * (kBK * 128), tmB, &full[stage],
+                                             (int)(z * p.b_col_batch) + brow + a * 64,
                                              (int)(z * p.b_row_batch) + kb * kBK);
                     }
                     pending[stage] = (int)phase;
@@ -242,11 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quad = warp % 4;  // tensor-memory lane quadrant this warp may access
         int acc = 0;
         uint32_t acc_phase = 0;
-        const bool half_rope = p.epi.rope_mode == kRopeHalf;
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             int z, mt, nt;
             tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
             const int ks = u / num_tiles;
+            const int sg = segment_of(p, nt * BN);
+            const bool half_rope = (sg == 0 ? p.epi[0].rope_mode : (sg == 1 ? p.epi[1].rope_mode : p.epi[2].rope_mode)) ==
+                                   kRopeHalf;
             if (!ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag)) { ok = false; break; }
             ptx::tc_fence_after();
             const int m = mt * kBM + quad * 32 + lane;
@@ -387,28 +420,67 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
     return r == CUDA_SUCCESS;
 }
 
+// The column segments of a product (one, unless the call is grouped) and the
+// total width.
+static int segments_of(const GemmArgs &a, GemmSegment (&sg)[kMaxSeg], int &n_total)
+{
+    if (a.nseg <= 0) {
+        sg[0].B = a.B;
+        sg[0].epi = a.epi;
+        sg[0].N = a.N;
+        n_total = a.N;
+        return 1;
+    }
+    n_total = 0;
+    for (int i = 0; i < a.nseg && i < kMaxSeg; ++i) {
+        sg[i] = a.seg[i];
+        n_total += a.seg[i].N;
+    }
+    return a.nseg;
+}
+
 bool gemm_tc_supported(const GemmArgs &a)
 {
     auto al = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
-    if (!al(a.A.ptr) || !al(a.B.ptr) || !al(a.epi.out)) return false;
-    if ((a.A.ld * 2) % 16 || (a.B.ld * 2) % 16 || (a.epi.ldc * 2) % 16) return false;
-    if (a.N % 32 || (a.a_col_batch * 2) % 16 || (a.b_col_batch * 2) % 16 || (a.epi.batch_stride * 2) % 16)
-        return false;
-    if (a.epi.rope_mode == kRopeHalf && (a.epi.rope_dim > 64 || 64 % a.epi.rope_dim || a.N % 64)) return false;
-    if (a.trans_b && a.N % 64) return false;
+    if (a.nseg < 0 || a.nseg > kMaxSeg || (a.nseg > 0 && (a.trans_b || a.batch != 1))) return false;
+    GemmSegment sg[kMaxSeg];
+    int n_total = 0;
+    const int ns = segments_of(a, sg, n_total);
+    if (!al(a.A.ptr) || (a.A.ld * 2) % 16) return false;
+    if ((a.a_col_batch * 2) % 16 || (a.b_col_batch * 2) % 16) return false;
+    for (int i = 0; i < ns; ++i) {
+        const GemmSegment &g = sg[i];
+        if (!al(g.B.ptr) || !al(g.epi.out) || (g.B.ld * 2) % 16 || (g.epi.ldc * 2) % 16) return false;
+        if (g.N % (ns > 1 ? 64 : 32) || (g.epi.batch_stride * 2) % 16) return false;
+        if (g.epi.rope_mode == kRopeHalf && (g.epi.rope_dim > 64 || 64 % g.epi.rope_dim || g.N % 64)) return false;
+    }
+    if (a.trans_b && n_total % 64) return false;
     return true;
 }
 
 // Tile width and K split: large GEMMs take the widest tile that still gives
 // every SM a tile; skinny ones (few output tiles, e.g. one decode token per
 // sequence) split K so that the work units fill whole waves of SMs.
-GemmPlan gemm_tc_plan(const GemmArgs &a, int num_sms)
+GemmPlan gemm_tc_plan(const GemmArgs &a_in, int num_sms)
 {
+    GemmSegment sg[kMaxSeg];
+    int n_total = 0;
+    const int ns = segments_of(a_in, sg, n_total);
+    GemmArgs a = a_in;
+    a.N = n_total;
+    a.epi = sg[0].epi;
+    // Every segment boundary must fall on a tile boundary.
+    auto fits = [&](int bn) {
+        if (ns == 1) return a.N % bn == 0;
+        for (int i = 0; i < ns; ++i)
+            if (sg[i].N % bn) return false;
+        return true;
+    };
     auto tiles = [&](int bn) { return ((a.M + kBM - 1) / kBM) * ((a.N + bn - 1) / bn) * a.batch; };
     GemmPlan pl;
     pl.bn = 64;
-    if (a.N % 256 == 0 && tiles(256) >= num_sms) pl.bn = 256;
-    else if (a.N % 128 == 0 && tiles(128) >= num_sms) pl.bn = 128;
+    if (fits(256) && tiles(256) >= num_sms) pl.bn = 256;
+    else if (fits(128) && tiles(128) >= num_sms) pl.bn = 128;
     pl.splits = 1;
     const int nk = (a.K + kBK - 1) / kBK;
     const bool skinny = a.M <= kBM;  // one row tile: the GEMM streams the weights once
@@ -423,7 +495,7 @@ GemmPlan gemm_tc_plan(const GemmArgs &a, int num_sms)
         };
         double best = cost(tiles(pl.bn), 1);
         for (int bn : {256, 128, 64}) {
-            if (a.N % bn && bn != 64) continue;
+            if (bn != 64 && !fits(bn)) continue;
             const int t = tiles(bn);
             for (int sp = 1; sp <= std::min(nk, 64); ++sp) {
                 const int kbps = (nk + sp - 1) / sp;
@@ -443,43 +515,57 @@ GemmPlan gemm_tc_plan(const GemmArgs &a, int num_sms)
 
 size_t gemm_tc_workspace(const GemmArgs &a, int num_sms)
 {
+    GemmSegment sg[kMaxSeg];
+    int n_total = 0;
+    segments_of(a, sg, n_total);
     GemmPlan pl = gemm_tc_plan(a, num_sms);
-    return pl.splits > 1 ? (size_t)pl.splits * a.M * a.N * sizeof(float) : 0;
+    return pl.splits > 1 ? (size_t)pl.splits * a.M * n_total * sizeof(float) : 0;
 }
 
 template <int BN, bool kBMN>
 static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cudaStream_t s)
 {
     using C = Cfg<BN>;
-    CUtensorMap ta, tb;
+    GemmSegment sg[kMaxSeg];
+    int n_total = 0;
+    const int ns = segments_of(a, sg, n_total);
+    CUtensorMap ta, tb[kMaxSeg];
     if (!make_tmap_bf16(&ta, a.A.ptr, a.A.rows, a.A.cols, a.A.ld, 64, kBM)) return cudaErrorInvalidValue;
-    if (!kBMN) {
-        if (!make_tmap_bf16(&tb, a.B.ptr, a.B.rows, a.B.cols, a.B.ld, 64, BN)) return cudaErrorInvalidValue;
-    } else {
-        if (!make_tmap_bf16(&tb, a.B.ptr, a.B.rows, a.B.cols, a.B.ld, 64, kBK)) return cudaErrorInvalidValue;
+    for (int i = 0; i < ns; ++i) {
+        const Mat2D &B = sg[i].B;
+        if (!make_tmap_bf16(&tb[i], B.ptr, B.rows, B.cols, B.ld, 64, kBMN ? kBK : BN)) return cudaErrorInvalidValue;
     }
+    for (int i = ns; i < kMaxSeg; ++i) tb[i] = tb[0];
     TcGemmParams p;
-    p.M = a.M; p.N = a.N; p.K = a.K; p.batch = a.batch;
+    p.M = a.M; p.N = n_total; p.K = a.K; p.batch = a.batch;
     p.a_row_batch = a.a_row_batch; p.a_col_batch = a.a_col_batch;
     p.b_row_batch = a.b_row_batch; p.b_col_batch = a.b_col_batch;
     p.tiles_m = (a.M + kBM - 1) / kBM;
-    p.tiles_n = (a.N + BN - 1) / BN;
+    p.tiles_n = (n_total + BN - 1) / BN;
     p.splits = pl.splits;
     p.kb_per_split = pl.kb_per_split;
     p.partial = pl.splits > 1 ? a.split_ws : nullptr;
-    p.epi = a.epi;
-    p.status = a.epi.status;
+    p.nseg = ns;
+    p.seg_n0[0] = 0;
+    bool half_rope = false;
+    for (int i = 0; i < ns; ++i) {
+        p.epi[i] = sg[i].epi;
+        p.seg_n0[i + 1] = p.seg_n0[i] + sg[i].N;
+        half_rope = half_rope || sg[i].epi.rope_mode == kRopeHalf;
+    }
+    for (int i = ns; i < kMaxSeg; ++i) p.epi[i] = sg[0].epi;
+    p.status = sg[0].epi.status;
     if (pl.splits > 1 && !a.split_ws) return cudaErrorInvalidValue;
     const int units = p.tiles_m * p.tiles_n * a.batch * p.splits;
     static int smem_dev = -1;
     cudaError_t e = smem_limit_once(smem_dev, (const void *)gemm_tc_kernel<BN, kBMN>, C::kSmem);
     if (e != cudaSuccess) return e;
-    gemm_tc_kernel<BN, kBMN><<<std::min(units, num_sms), kThreads, C::kSmem, s>>>(ta, tb, p);
+    gemm_tc_kernel<BN, kBMN><<<std::min(units, num_sms), kThreads, C::kSmem, s>>>(ta, tb[0], tb[1], tb[2], p);
     note_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (pl.splits > 1) {
-        const int nc = a.epi.rope_mode == kRopeHalf ? 64 : 8;
-        const int64_t threads = (int64_t)a.M * (a.N / nc);
+        const int nc = half_rope ? 64 : 8;
+        const int64_t threads = (int64_t)a.M * (n_total / nc);
         const unsigned blocks = (unsigned)((threads + 255) / 256);
         if (nc == 64) splitk_reduce_kernel<64><<<blocks, 256, 0, s>>>(p);
         else splitk_reduce_kernel<8><<<blocks, 256, 0, s>>>(p);
@@ -491,7 +577,7 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
 
 cudaError_t gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t s)
 {
-    if (a.M == 0 || a.N == 0 || a.batch == 0) return cudaSuccess;
+    if (a.M == 0 || (a.nseg == 0 && a.N == 0) || a.batch == 0) return cudaSuccess;
     if (!gemm_tc_supported(a)) return cudaErrorInvalidValue;
     const GemmPlan pl = gemm_tc_plan(a, num_sms);
     if (a.trans_b) {

@@ -94,6 +94,16 @@ struct Mat2D {
 // (z * b_row_batch, z * b_col_batch) of the B view.  B holds element (n, k)
 // at (row n, col k) (K contiguous, "K-major") unless trans_b, in which case
 // at (row k, col n) (N contiguous, "MN-major").
+// One column segment of a grouped product: output columns [n0, n0 + N) of
+// the concatenated result take their weights from B ([N, K] row-major) and
+// their epilogue from epi.  Tensor-core path only; widths multiple of 64.
+struct GemmSegment {
+    Mat2D B;
+    Epilogue epi;
+    int N = 0;
+};
+constexpr int kMaxSeg = 3;
+
 struct GemmArgs {
     Mat2D A;
     int64_t a_row_batch = 0, a_col_batch = 0;
@@ -103,6 +113,12 @@ struct GemmArgs {
     int M = 0, N = 0, K = 0, batch = 1;
     Epilogue epi;
     float *split_ws = nullptr;  // tensor-core split-K partials (gemm_tc_workspace bytes)
+    // nseg > 0: one launch computes A [B_0 | B_1 | ...]^T over the segments
+    // below (same A, K and split workspace; B, N and epi above are unused).
+    // Decode-sized projections that share their input stream their weights
+    // as one GEMM this way.
+    int nseg = 0;
+    GemmSegment seg[kMaxSeg];
 };
 
 struct GemmPlan {
