@@ -35,6 +35,7 @@ import mla_synth as syn  # noqa: E402
 METRIC = "MLA decode latent-cache HBM GB/s (% of peak); prefill TFLOP/s (% bf16 peak)"
 DECODE = syn.WORKLOADS["dsv2_decode"]
 PREFILL = syn.WORKLOADS["dsv2_prefill"]
+MLRA = syn.WORKLOADS["mlra_decode"]
 L2_FLUSH_BYTES = 512 << 20
 # DRAM bytes (read + write) of one decode attention launch on this workload,
 # from an ncu capture of the current kernel (dram__bytes_read.sum +
@@ -331,6 +332,8 @@ def run_ours(args, rank, world, device):
     }
     if pre:
         out["prefill"] = pre
+    if args.mlra:
+        out["mlra_decode"] = run_mlra(args, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     return out
@@ -380,6 +383,60 @@ def run_prefill(args, lay_device):
             "roofline": {"bound": "tensor", "kernel": "causal flash attention",
                          "achieved": round(katt, 2), "peak": tf_peak, "unit": "TFLOP/s",
                          "frac": round(katt / tf_peak, 4), "peak_source": peak_src,
+                         "kernel_ms": round(kms, 4)}}
+
+
+def run_mlra(args, device):
+    """One MLRA decode layer step (latent projection with the cache append,
+    split-KV attention over the L latent sub-heads, output projection) on
+    the MLRA workload: 128 sequences, cache length 8192, L = 4 sub-heads of
+    rank 256.  The 2.1 GB cache is larger than L2, so steps need no flush."""
+    import torch
+    import head_latent_attention_gb300 as mla
+    hbm_peak, tf_peak, tf_sust, peak_src = peaks()
+    w = MLRA
+    B = w.batch
+    lens = syn.lengths(w)
+    lay = build_layer(w, device, B, w.seq, B, 0)
+    for b in range(B):
+        ls, _ = syn.cache_rows(w, b, int(lens[b]))
+        lay.cache_lat[b, :lens[b]] = to_dev(ls, device)
+    xs, _ = syn.activations(w, B)
+    x = to_dev(xs, device)
+    seq = torch.arange(B, dtype=torch.int32, device=device)
+    pos = torch.from_numpy(lens - 1).to(device)
+    sl = torch.from_numpy(lens).to(device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qn, _ = lay.project_latent(x, seq, pos)
+        o = lay.decode(qn, None, sl)
+        return lay.out_proj(o)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    K = args.mlra_steps
+    ev = timing_events(K)
+    kev = timing_events(K)
+    for i in range(K):
+        mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_ATTENTION, kev[i][0], kev[i][1])
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_ATTENTION, None, None)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    kms = sum(a.elapsed_time(b) for a, b in kev) / K
+    nbytes = int(np.sum(lens)) * w.r_kv * 2
+    del lay
+    torch.cuda.empty_cache()
+    return {"workload": "mlra_decode", "batch": B, "cache_len": int(lens[0]), "latent_heads": w.n_latent_heads,
+            "steps": K, "ms_per_step": round(ms, 4), "value": round(nbytes / (ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s", "cache_bytes_per_step": nbytes, "l2": "cache 2.1 GB > L2, no flush",
+            "roofline": {"bound": "hbm", "kernel": "MLRA split-KV latent attention",
+                         "achieved": round(nbytes / (kms * 1e-3) / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(nbytes / (kms * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": peak_src,
                          "kernel_ms": round(kms, 4)}}
 
 
@@ -464,6 +521,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--prefill-steps", type=int, default=3)
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--no-mlra", dest="mlra", action="store_false")
+    ap.add_argument("--mlra-steps", type=int, default=5)
+    ap.add_argument("--mlra-only", action="store_true", help="time only the MLRA decode layer (profiling aid)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--prefill-only", action="store_true",
@@ -488,10 +548,10 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device(device))
-    if args.prefill_only:
+    if args.prefill_only or args.mlra_only:
         from head_latent_attention_gb300 import _build
         _build.build()
-        out = run_prefill(args, device)
+        out = run_prefill(args, device) if args.prefill_only else run_mlra(args, device)
         if rank == 0:
             print(json.dumps(out), flush=True)
         return

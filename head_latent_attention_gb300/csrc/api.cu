@@ -207,13 +207,21 @@ bool use_tc_decode(const mla_handle *h)
            decode_tc_supported(c.n_heads, c.r_kv, c.d_rope);
 }
 
+bool use_mlra_tc(const mla_handle *h)
+{
+    const mla_config &c = h->cfg;
+    return c.dtype == MLA_DTYPE_BF16 && c.variant == MLA_VARIANT_MLRA &&
+           mlra_tc_supported(c.n_heads, c.n_latent_heads, c.r_kv, c.d_rope);
+}
+
 DecodeWs decode_ws(const mla_handle *h, int B)
 {
     const mla_config &c = h->cfg;
     DecodeWs w;
     size_t lat = (size_t)B * c.n_heads * r_lat_of(c);
-    size_t parts = use_tc_decode(h) ? (size_t)(h->decode_clusters + B) * c.n_heads
-                                    : (size_t)B * decode_splits(c) * c.n_heads;
+    size_t parts = use_tc_decode(h)  ? (size_t)(h->decode_clusters + B) * c.n_heads
+                   : use_mlra_tc(h) ? (size_t)(mlra_tc_ctas() + B) * c.n_heads
+                                     : (size_t)B * decode_splits(c) * c.n_heads;
     w.q_abs = kWsHeader;
     w.o_lat = round_up(w.q_abs + lat * esize(c), 256);
     w.o_part = round_up(w.o_lat + lat * esize(c), 256);
@@ -586,6 +594,22 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
             (cache->rope_stride * 2) % 16)
             return MLA_ERR_INVALID_ARG;
         MLA_TRY_CUDA(decode_tc(t, s));
+    } else if (use_mlra_tc(h)) {
+        if ((cache->lat_stride * 2) % 16) return MLA_ERR_INVALID_ARG;
+        MlraTcArgs t;
+        t.B = B; t.H = H; t.L = c.n_latent_heads; t.r_kv = c.r_kv;
+        t.max_batch = c.max_batch; t.max_seq = c.max_seq; t.n_ctas = mlra_tc_ctas();
+        t.q_abs = q_abs;
+        t.lat = cache->lat; t.lat_stride = cache->lat_stride;
+        t.seq_lens = seq_lens;
+        t.prefix = (int *)(wsb + L.prefix);
+        t.chunk = t.prefix + B + 1;
+        t.scale_log2 = scale_log2;
+        t.o_lat = o_lat;
+        t.o_part = (float *)(wsb + L.o_part);
+        t.ml_part = (float *)(wsb + L.ml_part);
+        t.status = (uint32_t *)ws;
+        MLA_TRY_CUDA(mlra_tc(t, s));
     } else {
     DecodeArgs d;
     d.dtype = c.dtype;

@@ -820,9 +820,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     if (!make_tmap_bf16(&tl, a.lat, c_rows, kRLat, a.lat_stride, 64, kBKV) ||
         !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV))
         return cudaErrorInvalidValue;
-    decode_schedule_kernel<<<1, 1024, 0, s>>>(a.seq_lens, a.B, a.max_seq, a.n_clusters, a.prefix, a.chunk,
-                                              a.status);
-    note_launch();
+    decode_schedule(a.seq_lens, a.B, a.max_seq, a.n_clusters, a.prefix, a.chunk, a.status, s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     static int smem_dev = -1;
@@ -853,13 +851,25 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
     if (e != cudaSuccess) return e;
-    decode_combine_tc_kernel<<<dim3(a.H, a.B), 128, 0, s>>>(a.prefix, a.chunk, a.B, a.H, kRLat, a.o_part,
-                                                            a.ml_part, (bf16 *)a.o_lat);
-    note_launch();
+    decode_combine(a.prefix, a.chunk, a.B, a.H, kRLat, a.o_part, a.ml_part, a.o_lat, s);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int *prefix, int *chunk,
+                     uint32_t *status, cudaStream_t s)
+{
+    decode_schedule_kernel<<<1, 1024, 0, s>>>(seq_lens, B, max_seq, n_ranges, prefix, chunk, status);
+    note_launch();
+}
+
+void decode_combine(const int *prefix, const int *chunk, int B, int H, int r_lat, const float *o_part,
+                    const float *ml_part, void *o_lat, cudaStream_t s)
+{
+    decode_combine_tc_kernel<<<dim3(H, B), 128, 0, s>>>(prefix, chunk, B, H, r_lat, o_part, ml_part, (bf16 *)o_lat);
+    note_launch();
+}
 
 int decode_tc_max_clusters()
 {

@@ -177,6 +177,34 @@ struct DecodeTcArgs {
     uint32_t *status;
 };
 int decode_tc_max_clusters();
+
+// Device-side scheduling shared by the split-KV decode kernels: prefix sums
+// of the valid lengths and the keys per work range (n_ranges ranges), and
+// the log-sum-exp merge of the partials of sequences split across ranges
+// (slot of range c and sequence b: c + b).
+void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int *prefix, int *chunk,
+                     uint32_t *status, cudaStream_t s);
+void decode_combine(const int *prefix, const int *chunk, int B, int H, int r_lat, const float *o_part,
+                    const float *ml_part, void *o_lat, cudaStream_t s);
+
+// Tensor-core split-KV decode for MLRA (mlra_tc.cu): bfloat16, latent blocks
+// of 256 columns, at most 16 heads per block, no rope.
+struct MlraTcArgs {
+    int B, H, L, r_kv, max_batch, max_seq, n_ctas;
+    const void *q_abs;  // [B, H, 256] (head h reads block h / (H / L))
+    const void *lat;    // [max_batch * max_seq, lat_stride]
+    int64_t lat_stride;
+    const int32_t *seq_lens;
+    int *prefix, *chunk;  // workspace: [B + 1], [1]
+    float scale_log2;
+    void *o_lat;          // [B, H, 256]
+    float *o_part;        // [(n_ctas + B), H, 256]
+    float *ml_part;       // [(n_ctas + B), H, 2]
+    uint32_t *status;
+};
+bool mlra_tc_supported(int H, int L, int r_kv, int d_rope);
+int mlra_tc_ctas();
+cudaError_t mlra_tc(const MlraTcArgs &a, cudaStream_t s);
 bool decode_tc_supported(int H, int r_kv, int d_rope);
 cudaError_t decode_tc(const DecodeTcArgs &a, cudaStream_t s);
 
