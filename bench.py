@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 512 << 20
 # from an ncu capture of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum); None whenever the kernel changes until it is
 # captured again.
-DECODE_TRAFFIC_BYTES = int(213.58e6 + 4.32e6)
+DECODE_TRAFFIC_BYTES = None
 
 
 def peaks():

@@ -46,7 +46,7 @@ namespace {
 
 constexpr int kH = 128;       // heads per CTA = MMA M
 constexpr int kBKV = 48;      // keys per tile
-constexpr int kStages = 5;    // KV ring
+constexpr int kStages = 6;    // KV ring
 constexpr int kSBuf = 2;      // score buffers in tensor memory
 constexpr int kSoftmaxThreads = 256;  // warps 2..9
 constexpr int kThreads = 64 + kSoftmaxThreads;
@@ -64,13 +64,15 @@ constexpr int kXWarpBytes = 32 * kXRowBytes;
 constexpr int kXBytes = kH * kXRowBytes;
 constexpr uint32_t kXTx = kXBytes;                    // one exchange = one bulk copy of a whole buffer
 constexpr int kOffX = kStages * kStageBytes;
-constexpr int kOffStage = kOffX + kXBuf * kXBytes;   // outgoing partials (one buffer per softmax group)
 // P (bf16, 128 heads x 48 keys) as the A operand of P.V: K-major without
 // swizzle, 8-row x 16-byte core matrices, the six core matrices of an 8-row
 // group adjacent (128 bytes apart), 8-row groups 768 bytes apart.
 constexpr int kPBytes = kH * kBKV * 2;
 constexpr int kPGroup = (kBKV / 8) * 128;
-constexpr int kOffP = kOffStage + 2 * kXBytes;
+// A softmax group's P buffer also stages its outgoing partial: each warp's
+// 32 rows occupy the same 3 KB in both layouts.
+constexpr int kOffP = kOffX + kXBuf * kXBytes;
+static_assert(kXWarpBytes == 4 * kPGroup, "a warp's staging block is its P rows");
 constexpr int kOffRed = kOffP + 2 * kPBytes;          // reference maxima, segment-end (max, sum)
 constexpr int kOffBar = kOffRed + 6 * kH * 4;
 constexpr int kSmem = kOffBar + 512 + 1024;
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t hand_in = 0, nseg_done = 0;                       // handoffs received, segments finished
         float *eslot = mslot + 2 * kH;                             // [2 groups][2][kH] (max, sum) at a segment end
         const int xblk = quad * kXWarpBytes;                       // this warp's block of an exchange buffer
-        uint8_t *wstage = smem + kOffStage + grp * kXBytes + xblk;
+        uint8_t *wstage = smem + kOffP + grp * kPBytes + xblk;
         uint32_t *my_stage = reinterpret_cast<uint32_t *>(wstage + lane * kXRowBytes);
         const uint32_t peer_xbuf = map_peer(smem + kOffX + grp * kXBytes + xblk, peer);
         const uint32_t peer_xfull = map_peer(&bar->x_full[grp], peer);
@@ -588,7 +590,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_new = (mt > m_prev + kRescaleThreshold) ? mt : m_prev;
                 mslot[(g & 1) * kH + h] = m_new;
                 if (t + 1 < ntiles) ptx::mbar_arrive(&bar->hand[grp][quad]);
-                // 3. The group's next tile: its query (at a segment boundary) and its partial.
+                // 3. The group's next tile: its query (at a segment boundary)
+                //    and its partial, staged in P buffer grp once P.V(g - 2)
+                //    has read P(g - 2) from it.  Each pv_done barrier is
+                //    waited on phase by phase, never two phases behind
+                //    (P.V(g) cannot finish before P(g) exists).
+                if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[grp], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
                 if (nx.valid) {
                     if (nx.t == 0 && !load_q(nx.b, nx.nseg)) { fail(); break; }
                     if (!send(nx.g)) { fail(); break; }
@@ -608,10 +615,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_grp = m_new;
 #pragma unroll
                 for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];
-                // P buffer grp held P(g - 2): wait for P.V(g - 2).  Each
-                // pv_done barrier is waited on phase by phase, never two
-                // phases behind (P.V(g) cannot finish before P(g) exists).
-                if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[grp], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
                 if (t > 0 && m_new != m_prev) {
                     // Raised: O must hold every earlier P.V before it is
                     // rescaled to the new reference.
@@ -629,6 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tmem_st_wait();
                 }
+                // P over the staged partial once the warp's copy has read it.
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
                 {
                     uint8_t *prow = smem + kOffP + grp * kPBytes + (h >> 3) * kPGroup + (h & 7) * 16;
 #pragma unroll
@@ -667,12 +673,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ptx::mbar_wait(&bar->pv_done[gl & 1], (gl >> 1) & 1, abort_flag)) { fail(); break; }
             ptx::tc_fence_after();
             const int slot = cid + b;
-            // Each warp stages 32 rows x 64 bytes at a time in its group's P
-            // buffer (free: every P.V of the segment has completed), so the
+            // Each warp stages 32 rows x 64 bytes at a time in its own block
+            // of its group's P buffer (free: every P.V of the segment has
+            // completed, and the warp's last copy to the peer has read it), so the
             // global stores go out as 64-byte row pieces: fp32 partials 16
             // columns per chunk, bf16 outputs 32.  The 16-byte pieces of a
             // row are rotated by (row / 2) % 4 against bank conflicts.
-            uint8_t *wst = smem + kOffP + grp * kPBytes + quad * 2048;
+            uint8_t *wst = smem + kOffP + grp * kPBytes + xblk;
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
             const int rd_row = lane >> 2, rd_piece = lane & 3;
             const int ncols = whole ? 32 : 16;
 #pragma unroll 1
