@@ -308,6 +308,35 @@ def test_small_lm_prefill_full_sampled(mla, oracle_mod):
 
 
 # ---------------------------------------------------------------------------
+# Decode-sized projections (one grouped GEMM per shared input on the tensor
+# cores): cache rows scattered to (sequence, position) and the queries
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["dsv2_decode", "small_lm_prefill", "mlra_decode"])
+def test_project_decode_sized(mla, oracle_mod, name):
+    w = W[name]
+    T, B, S = 37, 5, 300
+    dev_w, ex_w = weights_of(w)
+    lay = make_layer(mla, w, dev_w, T, max_batch=B, max_seq=S)
+    xs, xe = syn.activations(w, T)
+    rng = np.random.default_rng(7)
+    seq = rng.integers(0, B, T).astype(np.int32)
+    pos = rng.permutation(S)[:T].astype(np.int32)  # distinct positions, no two tokens share a row
+    qn, qr = lay.project_latent(to_dev(xs), torch.from_numpy(seq).cuda(), torch.from_numpy(pos).cuda())
+    torch.cuda.synchronize()
+    assert lay.device_status()[0] == mla.MLA_OK
+    ref = oracle_mod.project(w, xe, pos, ex_w)
+    lat = to_f64(lay.cache_lat)[seq, pos]
+    compare(lat, ref["c_kv"], w.dtype, f"{name} latent rows")
+    if w.variant == syn.VARIANT_DECOUPLED:
+        compare(to_f64(lay.cache_rope)[seq, pos], ref["k_r"], w.dtype, f"{name} rope rows")
+        compare(to_f64(qn), ref["q_nope"], w.dtype, f"{name} q_nope")
+        compare(to_f64(qr), ref["q_rope"], w.dtype, f"{name} q_rope")
+    else:
+        compare(to_f64(qn), ref["q"], w.dtype, f"{name} q")
+
+
+# ---------------------------------------------------------------------------
 # Output projection stage and edge cases
 # ---------------------------------------------------------------------------
 
