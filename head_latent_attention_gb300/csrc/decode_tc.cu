@@ -607,11 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t pk[kBKV / 2];
 #pragma unroll
                 for (int j = 0; j < kBKV / 2; ++j) {
-                    const float a0 = exp2f(s[2 * j] - m_new), a1 = exp2f(s[2 * j + 1] - m_new);
+                    const float a0 = ptx::ex2(s[2 * j] - m_new), a1 = ptx::ex2(s[2 * j + 1] - m_new);
                     psum += a0 + a1;
                     pk[j] = ptx::pack_bf16(a0, a1);
                 }
-                l_grp = l_grp * exp2f(m_grp - m_new) + psum;
+                l_grp = l_grp * ptx::ex2(m_grp - m_new) + psum;
                 m_grp = m_new;
 #pragma unroll
                 for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];

@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float tmax =
                         fmaxf(fmaxf(red[h], red[kNH + h]), fmaxf(red[2 * kNH + h], red[3 * kNH + h]));
                     const float m_new = fmaxf(m_ref[h], tmax);
-                    corr[h] = (m_new == m_ref[h]) ? 1.f : exp2f(m_ref[h] - m_new);
+                    corr[h] = (m_new == m_ref[h]) ? 1.f : ptx::ex2(m_ref[h] - m_new);
                     changed = changed || (m_new != m_ref[h] && t > 0);
                     m_ref[h] = m_new;
                     l_part[h] *= corr[h];
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float pv[kNH];
 #pragma unroll
             for (int h = 0; h < kNH; ++h) {
-                pv[h] = exp2f(s[h] - m_ref[h]);
+                pv[h] = ptx::ex2(s[h] - m_ref[h]);
                 if (h < hpb) l_part[h] += pv[h];
             }
             if (ok && g >= 2 && !ptx::mbar_wait(&bar->pv_done[g & 1], ((g >> 1) - 1) & 1, abort_flag)) ok = false;

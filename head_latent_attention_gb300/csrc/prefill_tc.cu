@@ -269,25 +269,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_ld32(tmem + lane_off + sbuf + 32, r1);
             ptx::tmem_ld_wait();
             const int lim = my_pos - t * kBN;  // keys t*64 + j with j <= lim are visible
+            // Raw scores; the scale is folded into the exponent below (it is
+            // positive, so the maximum commutes with it).  Only the diagonal
+            // tile needs the causal mask.
             float s[64];
             float mt = -INFINITY;
+            if (lim >= kBN - 1) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                s[j] = (j <= lim) ? __uint_as_float(r0[j]) * p.scale_log2 : -INFINITY;
-                s[32 + j] = (32 + j <= lim) ? __uint_as_float(r1[j]) * p.scale_log2 : -INFINITY;
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = __uint_as_float(r0[j]);
+                    s[32 + j] = __uint_as_float(r1[j]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    s[j] = (j <= lim) ? __uint_as_float(r0[j]) : -INFINITY;
+                    s[32 + j] = (32 + j <= lim) ? __uint_as_float(r1[j]) : -INFINITY;
+                }
             }
 #pragma unroll
             for (int j = 0; j < 64; ++j) mt = fmaxf(mt, s[j]);
+            mt *= p.scale_log2;
             const bool resc = mt > m_run + kRescaleThreshold;
             const float m_new = resc ? mt : m_run;
             // Rows past the sequence end see no key; keep their state finite.
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-            const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_use);
+            const float corr = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - m_use);
             float psum = 0.f;
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float a0 = exp2f(s[2 * j] - m_use), a1 = exp2f(s[2 * j + 1] - m_use);
+                const float a0 = ptx::ex2(fmaf(s[2 * j], p.scale_log2, -m_use));
+                const float a1 = ptx::ex2(fmaf(s[2 * j + 1], p.scale_log2, -m_use));
                 psum += a0 + a1;
                 pk[j] = ptx::pack_f16(a0, a1);
             }

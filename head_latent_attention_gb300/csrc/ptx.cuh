@@ -350,6 +350,16 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
 }
 
 // --------------------------------------------------------------- conversion
+// 2^x with the hardware approximation (ex2.approx, relative error about
+// 2^-22, subnormal results flushed to zero): ample for softmax weights that
+// are then rounded to 16 bits.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
