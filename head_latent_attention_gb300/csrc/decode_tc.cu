@@ -398,7 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t d = tmem + kSCol + sb * kBKV;
                         // K steps 0..15: latent (keys in 128-byte swizzled
                         // atoms); 16..17: rope (keys 64-byte swizzled); the
-                        // query is read from tensor memory.
+                        // query is read from tensor memory.  (One straight-line
+                        // burst: a runtime-indexed issue loop slows the MMAs.)
 #pragma unroll
                         for (int k = 0; k < 16; ++k)
                             ptx::mma_f16_tmem_a(d, tmem + kQCol + k * 8,
@@ -564,11 +565,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             s[8 * c + 2 * i + 1] = a.y + bb.y;
                         }
                     }
+                    if (valid < kBKV) {
 #pragma unroll
-                    for (int j = 0; j < kBKV; ++j) {
-                        s[j] = (j < valid) ? s[j] : -INFINITY;
-                        mt = fmaxf(mt, s[j]);
+                        for (int j = 0; j < kBKV; ++j) s[j] = (j < valid) ? s[j] : -INFINITY;
                     }
+#pragma unroll
+                    for (int j = 0; j < kBKV; ++j) mt = fmaxf(mt, s[j]);
                 }
                 // The warp's block of exchange buffer grp is read: the peer may
                 // overwrite it once the group's four warps said so (the
