@@ -575,6 +575,11 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     MLA_TRY(run_gemm(h, ga, (uint32_t *)ws, s));
 
     const float scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
+    // The tensor-core kernels leave split sequences as partials in slot order
+    // (range + sequence); they are merged by the fused finish kernel or by
+    // decode_combine before the value up-projection GEMM.
+    const bool tc_split = use_tc_decode(h) || use_mlra_tc(h);
+    int *prefix = (int *)(wsb + L.prefix);
     if (use_tc_decode(h)) {
         DecodeTcArgs t;
         t.B = B; t.H = H; t.r_kv = c.r_kv; t.d_rope = c.d_rope;
@@ -611,24 +616,43 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         t.status = (uint32_t *)ws;
         MLA_TRY_CUDA(mlra_tc(t, s));
     } else {
-    DecodeArgs d;
-    d.dtype = c.dtype;
-    d.B = B; d.H = H; d.r_lat = r_lat; d.d_rope = dec ? c.d_rope : 0;
-    d.heads_per_block_lat = heads_per_block_of(c);
-    d.q_abs = q_abs; d.q_rope = dec ? q_rope : nullptr;
-    d.lat = cache->lat; d.lat_stride = cache->lat_stride;
-    d.rope = dec ? cache->rope : nullptr; d.rope_stride = cache->rope_stride;
-    d.max_seq = c.max_seq;
-    d.seq_lens = seq_lens;
-    d.scale_log2 = scale_log2;
-    d.o_part = (float *)(wsb + L.o_part);
-    d.ml_part = (float *)(wsb + L.ml_part);
-    d.n_split = decode_splits(c);
-    d.chunk = kDecodeChunk;
-    d.o_lat = o_lat;
-    d.status = (uint32_t *)ws;
-    if (d.n_split > 64) return MLA_ERR_UNSUPPORTED;
-    MLA_TRY_CUDA(decode_simt(d, s));
+        DecodeArgs d;
+        d.dtype = c.dtype;
+        d.B = B; d.H = H; d.r_lat = r_lat; d.d_rope = dec ? c.d_rope : 0;
+        d.heads_per_block_lat = heads_per_block_of(c);
+        d.q_abs = q_abs; d.q_rope = dec ? q_rope : nullptr;
+        d.lat = cache->lat; d.lat_stride = cache->lat_stride;
+        d.rope = dec ? cache->rope : nullptr; d.rope_stride = cache->rope_stride;
+        d.max_seq = c.max_seq;
+        d.seq_lens = seq_lens;
+        d.scale_log2 = scale_log2;
+        d.o_part = (float *)(wsb + L.o_part);
+        d.ml_part = (float *)(wsb + L.ml_part);
+        d.n_split = decode_splits(c);
+        d.chunk = kDecodeChunk;
+        d.o_lat = o_lat;
+        d.status = (uint32_t *)ws;
+        if (d.n_split > 64) return MLA_ERR_UNSUPPORTED;
+        MLA_TRY_CUDA(decode_simt(d, s));
+    }
+
+    if (tc_split && decode_finish_supported(r_lat, c.d_v)) {
+        FinishArgs f;
+        f.B = B; f.H = H; f.r_lat = r_lat; f.d_v = c.d_v;
+        f.prefix = prefix; f.chunk = prefix + B + 1;
+        f.o_part = (float *)(wsb + L.o_part);
+        f.ml_part = (float *)(wsb + L.ml_part);
+        f.o_lat = o_lat;
+        f.W_UV = w->W_UV;
+        f.o = o;
+        f.status = (uint32_t *)ws;
+        MLA_TRY_CUDA(decode_finish(f, s));
+        return MLA_OK;
+    }
+    if (tc_split) {
+        decode_combine(prefix, prefix + B + 1, B, H, r_lat, (float *)(wsb + L.o_part), (float *)(wsb + L.ml_part),
+                       o_lat, s);
+        MLA_TRY_CUDA(cudaGetLastError());
     }
 
     // o[b, h] = W_UV,h o_lat[b, h]: per head h, [B, r_lat] x [r_lat, d_v].

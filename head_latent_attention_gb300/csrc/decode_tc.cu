@@ -861,9 +861,7 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tl, tr, (const bf16 *)a.q_abs, (const bf16 *)a.q_rope, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
-    if (e != cudaSuccess) return e;
-    decode_combine(a.prefix, a.chunk, a.B, a.H, kRLat, a.o_part, a.ml_part, a.o_lat, s);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

@@ -1,0 +1,266 @@
+// End of the weight-absorbed decode on the tensor cores: the log-sum-exp
+// merge of the split-KV partials and the value up-projection, fused.
+//
+// deepseek-mla `MultiHeadLatentAttention.forward` (and mlra_attn per latent
+// block) weights the up-projected values W_UV,h c_j by the softmax; by
+// linearity o_h = W_UV,h (sum_j p_hj c_j), so the split-KV kernels attend in
+// latent space and leave, per work range, an unnormalised latent average
+// with its running max and denominator.  This kernel finishes the head:
+//
+// One CTA per (head h, group of 64 sequences):
+//   1. TMA copies W_UV,h ([128, r_lat] bfloat16, K-major) into shared memory;
+//   2. the eight warps merge the partials of each sequence of the group
+//      (or read the latent average that a single range wrote directly) and
+//      store the bfloat16 result as a K-major, 128-byte-swizzled operand;
+//   3. one thread issues o_h^T[128, 64] = W_UV,h [128, r_lat] * o_lat^T
+//      (tcgen05.mma M=128, N=64, accumulator in tensor memory);
+//   4. the eight warps read the accumulator back and store o[b, h, :].
+// The merged latent average never leaves the SM.  Every wait is bounded.
+#include <cudaTypedefs.h>
+
+#include "mla_internal.cuh"
+#include "ptx.cuh"
+
+namespace mla {
+
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                    int box_rows);
+
+namespace {
+
+constexpr int kTok = 64;        // sequences per CTA (MMA N)
+constexpr int kDv = 128;        // value head width (MMA M)
+constexpr int kThreads = 256;
+constexpr int kWBlk = kDv * 128;   // one 64-column block of W_UV,h: 16 KB
+constexpr int kOBlk = kTok * 128;  // one 64-column block of the latent operand: 8 KB
+
+template <int R>
+struct FinCfg {
+    static constexpr int kBlocks = R / 64;
+    static constexpr int kSmem = kBlocks * (kWBlk + kOBlk) + 1024 /*align*/ + 64 /*barriers*/;
+};
+
+struct FinParams {
+    const int *prefix;     // [B + 1] prefix sums of the valid lengths
+    const int *chunk;      // keys per range
+    int B, H;
+    const float *o_part;   // [(ranges + B), H, R] unnormalised partial averages
+    const float *ml_part;  // [(ranges + B), H, 2] (max in log2 units, denominator)
+    const bf16 *o_lat;     // [B, H, R] written directly for single-range sequences
+    bf16 *o;               // [B, H, 128]
+    uint32_t *status;
+};
+
+// Latent average of sequence b, head h, columns [lane * CPL, lane * CPL + CPL)
+// (CPL = R / 32), as bfloat16 pairs.
+template <int R>
+__device__ __forceinline__ void merged_row(const FinParams &p, int b, int h, int lane, uint32_t (&out)[R / 64])
+{
+    constexpr int CPL = R / 32;
+#pragma unroll
+    for (int i = 0; i < CPL / 2; ++i) out[i] = 0u;
+    if (b >= p.B) return;
+    const int lo = p.prefix[b], hi = p.prefix[b + 1];
+    if (hi <= lo) return;  // empty or invalid length: zero output
+    const int chunk = *p.chunk;
+    const int fc = lo / chunk, lc = (hi - 1) / chunk;
+    if (fc == lc) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.o_lat + ((int64_t)b * p.H + h) * R + lane * CPL);
+#pragma unroll
+        for (int i = 0; i < CPL / 8; ++i) {
+            const uint4 v = src[i];
+            out[4 * i] = v.x; out[4 * i + 1] = v.y; out[4 * i + 2] = v.z; out[4 * i + 3] = v.w;
+        }
+        return;
+    }
+    // Reference max and denominator over the ranges, lanes in parallel.
+    float m = -INFINITY;
+    for (int c = fc + lane; c <= lc; c += 32) m = fmaxf(m, p.ml_part[((int64_t)(c + b) * p.H + h) * 2]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float den = 0.f;
+    for (int c = fc + lane; c <= lc; c += 32) {
+        const float2 ml = *reinterpret_cast<const float2 *>(p.ml_part + ((int64_t)(c + b) * p.H + h) * 2);
+        den += exp2f(ml.x - m) * ml.y;
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    float acc[CPL];
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
+    // Four ranges per pass, their loads issued before the sums.
+    for (int c0 = fc; c0 <= lc; c0 += 4) {
+        float4 v[4][CPL / 4];
+        float wgt[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u;
+            if (c <= lc) {
+                const int64_t slot = (int64_t)(c + b) * p.H + h;
+                const float4 *src = reinterpret_cast<const float4 *>(p.o_part + slot * R + lane * CPL);
+#pragma unroll
+                for (int j = 0; j < CPL / 4; ++j) v[u][j] = __ldcs(src + j);
+                wgt[u] = exp2f(p.ml_part[slot * 2] - m);
+            } else {
+#pragma unroll
+                for (int j = 0; j < CPL / 4; ++j) v[u][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                wgt[u] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int j = 0; j < CPL / 4; ++j) {
+                acc[4 * j] += wgt[u] * v[u][j].x;
+                acc[4 * j + 1] += wgt[u] * v[u][j].y;
+                acc[4 * j + 2] += wgt[u] * v[u][j].z;
+                acc[4 * j + 3] += wgt[u] * v[u][j].w;
+            }
+    }
+    const float inv = 1.f / den;
+#pragma unroll
+    for (int i = 0; i < CPL / 2; ++i) out[i] = ptx::pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1) decode_finish_kernel(const __grid_constant__ CUtensorMap tw,
+                                                                    FinParams p)
+{
+    using C = FinCfg<R>;
+    constexpr int CPL = R / 32;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sW = smem;
+    uint8_t *sO = smem + C::kBlocks * kWBlk;
+    uint64_t *w_full = (uint64_t *)(sO + C::kBlocks * kOBlk);
+    uint64_t *mma_done = w_full + 1;
+    uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
+    volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
+
+    const int h = blockIdx.x, b0 = blockIdx.y * kTok;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(w_full, 1);
+        ptx::mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 0) ptx::tmem_alloc(tmem_slot, 64);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // 1. The weights of head h, in the background.
+    if (threadIdx.x == 0) {
+        ptx::prefetch_tmap(&tw);
+        ptx::mbar_expect_tx(w_full, C::kBlocks * kWBlk);
+#pragma unroll
+        for (int kb = 0; kb < C::kBlocks; ++kb) ptx::tma_load_2d(sW + kb * kWBlk, &tw, w_full, kb * 64, h * kDv);
+    }
+
+    // 2. Merged latent averages of the group's sequences, one per warp pass.
+    for (int t = warp; t < kTok; t += kThreads / 32) {
+        uint32_t v[R / 64];
+        merged_row<R>(p, b0 + t, h, lane, v);
+        // Columns [lane * CPL, +CPL) are CPL / 8 chunks of 16 bytes; chunk g
+        // sits in 64-column block g / 8, at position (g % 8) ^ (t % 8) of row t.
+#pragma unroll
+        for (int i = 0; i < CPL / 8; ++i) {
+            const int g = lane * (CPL / 8) + i;
+            uint8_t *dst = sO + (g >> 3) * kOBlk + t * 128 + (((g & 7) ^ (t & 7)) << 4);
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+    }
+    ptx::fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
+    __syncthreads();
+
+    // 3. o_h^T = W_UV,h * o_lat^T.
+    if (warp == 0) {
+        if (ptx::elect_one()) {
+            if (ptx::mbar_wait(w_full, 0, abort_flag)) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idesc = ptx::idesc_bf16(kDv, kTok, false, false);
+                const uint32_t w0 = ptx::smem_u32(sW), o0 = ptx::smem_u32(sO);
+#pragma unroll
+                for (int kb = 0; kb < C::kBlocks; ++kb)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        ptx::mma_bf16(tmem, ptx::sdesc_sw128(w0 + kb * kWBlk + k * 32, 16, 1024),
+                                      ptx::sdesc_sw128(o0 + kb * kOBlk + k * 32, 16, 1024), idesc,
+                                      (kb | k) != 0 ? 1u : 0u);
+                ptx::mma_commit(mma_done);
+            } else {
+                *abort_flag = 1;
+            }
+        }
+        __syncwarp();
+    }
+
+    // 4. Accumulator row d (tensor-memory lane d) holds o[b0 + t, h, d] in
+    // column t; warps w and w + 4 share lane quadrant w % 4 and take token
+    // halves.
+    if (ptx::mbar_wait(mma_done, 0, abort_flag)) {
+        ptx::tc_fence_after();
+        const int quad = warp % 4, half = warp / 4;
+        const int d = quad * 32 + lane;
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + half * 32, r);
+        ptx::tmem_ld_wait();
+        bf16 *dst = p.o + ((int64_t)(b0 + half * 32) * p.H + h) * kDv + d;
+        const int nt = min(32, p.B - b0 - half * 32);
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+            if (t < nt) dst[(int64_t)t * p.H * kDv] = __float2bfloat16_rn(__uint_as_float(r[t]));
+    } else {
+        *abort_flag = 1;
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        // A weight copy still in flight after a timeout must land before the
+        // CTA's shared memory is released.
+        if (*abort_flag) {
+            volatile int never = 0;
+            ptx::mbar_wait(w_full, 0, &never);
+        }
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 64);
+    }
+    if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, kStatusTimeout);
+}
+
+template <int R>
+cudaError_t launch_finish(const FinishArgs &a, cudaStream_t s)
+{
+    using C = FinCfg<R>;
+    CUtensorMap tw;
+    if (!make_tmap_bf16(&tw, a.W_UV, (int64_t)a.H * kDv, R, R, 64, kDv)) return cudaErrorInvalidValue;
+    static int smem_dev = -1;
+    cudaError_t e = smem_limit_once(smem_dev, (const void *)decode_finish_kernel<R>, C::kSmem);
+    if (e != cudaSuccess) return e;
+    FinParams p;
+    p.prefix = a.prefix; p.chunk = a.chunk;
+    p.B = a.B; p.H = a.H;
+    p.o_part = a.o_part; p.ml_part = a.ml_part;
+    p.o_lat = (const bf16 *)a.o_lat;
+    p.o = (bf16 *)a.o;
+    p.status = a.status;
+    decode_finish_kernel<R><<<dim3(a.H, (a.B + kTok - 1) / kTok), kThreads, C::kSmem, s>>>(tw, p);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_finish_supported(int r_lat, int d_v) { return d_v == kDv && (r_lat == 256 || r_lat == 512); }
+
+cudaError_t decode_finish(const FinishArgs &a, cudaStream_t s)
+{
+    if (a.B == 0) return cudaSuccess;
+    if (!decode_finish_supported(a.r_lat, a.d_v)) return cudaErrorInvalidValue;
+    return a.r_lat == 512 ? launch_finish<512>(a, s) : launch_finish<256>(a, s);
+}
+
+}  // namespace mla

@@ -187,6 +187,23 @@ void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, 
 void decode_combine(const int *prefix, const int *chunk, int B, int H, int r_lat, const float *o_part,
                     const float *ml_part, void *o_lat, cudaStream_t s);
 
+// Merge of the split-KV partials fused with the value up-projection
+// (finish_tc.cu): o[b, h] = W_UV,h o_lat[b, h] with o_lat merged on chip from
+// the partials decode_tc / mlra_tc leave (same slot layout as decode_combine).
+// bfloat16, d_v == 128, r_lat in {256, 512}; W_UV,h = rows [128 h, 128 h + 128)
+// of W_UV viewed as [H * 128, r_lat].
+struct FinishArgs {
+    int B, H, r_lat, d_v;
+    const int *prefix, *chunk;
+    const float *o_part, *ml_part;
+    const void *o_lat;  // [B, H, r_lat] (single-range sequences)
+    const void *W_UV;
+    void *o;            // [B, H, d_v]
+    uint32_t *status;
+};
+bool decode_finish_supported(int r_lat, int d_v);
+cudaError_t decode_finish(const FinishArgs &a, cudaStream_t s);
+
 // Tensor-core split-KV decode for MLRA (mlra_tc.cu): bfloat16, latent blocks
 // of 256 columns, at most 16 heads per block, no rope.
 struct MlraTcArgs {

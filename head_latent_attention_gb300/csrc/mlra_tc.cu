@@ -533,8 +533,6 @@ cudaError_t mlra_tc(const MlraTcArgs &a, cudaStream_t s)
     mlra_tc_kernel<<<a.n_ctas, kThreads, kSmem, s>>>(tkv, tq, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    decode_combine(a.prefix, a.chunk, a.B, a.H, kR, a.o_part, a.ml_part, a.o_lat, s);
     return cudaGetLastError();
 }
 
