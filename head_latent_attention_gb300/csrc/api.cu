@@ -17,6 +17,15 @@ static unsigned long long g_launches = 0;
 static cudaEvent_t g_prof_begin[MLA_PROFILE_COUNT] = {};
 static cudaEvent_t g_prof_end[MLA_PROFILE_COUNT] = {};
 
+bool pdl_enabled()
+{
+    static const bool on = [] {
+        const char *v = getenv("MLA_PDL");
+        return !(v && v[0] == '0');
+    }();
+    return on;
+}
+
 void note_launch(int n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
 
 // Inside stream capture the record is made external, so that it becomes an

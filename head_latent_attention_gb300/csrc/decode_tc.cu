@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
     };
     if (threadIdx.x == 0) {
+        ptx::pdl_trigger();
         ptx::mbar_init(&bar->q_full, kSoftmaxThreads / 2);  // the group that sends a segment's first tile
         ptx::mbar_init(&bar->q_empty, 1);
         for (int i = 0; i < kStages; ++i) {
@@ -325,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         evict_first = ptx::policy_evict_first();
 #pragma unroll
         for (int i = 0; i < kStages; ++i) pending[i] = -1;
+        ptx::pdl_wait();  // the schedule, queries and cache come from earlier kernels
         ld.init(p.prefix, p.B, cid, *p.chunk);
         for (int i = 0; i < kStages && ld.valid; ++i) issue_load();  // fresh ring: no waits
     }
@@ -333,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     cluster_sync();  // the peer's barriers exist before any remote arrive or store
     ptx::tc_fence_after();
+    ptx::pdl_wait();
     const uint32_t tmem = bar->tmem;
     const int chunk = *p.chunk;
     bool ok = true;
@@ -748,6 +751,8 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
                                                                int n_clusters, int *prefix, int *chunk,
                                                                uint32_t *status)
 {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     __shared__ int warp_sums[32];
     __shared__ int carry;
     if (threadIdx.x == 0) { carry = 0; prefix[0] = 0; }
@@ -797,6 +802,8 @@ __global__ void __launch_bounds__(128) decode_combine_tc_kernel(const int *prefi
                                                                 int H, int r_lat, const float *o_part,
                                                                 const float *ml_part, bf16 *o_lat)
 {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const int h = blockIdx.x, b = blockIdx.y;
     const int lo = prefix[b], hi = prefix[b + 1], chunk = *chunk_ptr;
     bf16 *dst = o_lat + ((int64_t)b * H + h) * r_lat;
@@ -845,20 +852,9 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     p.o_part = a.o_part;
     p.ml_part = a.ml_part;
     p.status = a.status;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * a.n_clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     profile_begin(MLA_PROFILE_DECODE_ATTENTION, s);
-    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel, tl, tr, (const bf16 *)a.q_abs, (const bf16 *)a.q_rope, p);
+    e = launch_ex(decode_tc_kernel, dim3(2 * a.n_clusters), dim3(kThreads), kSmem, s, 2, tl, tr,
+                  (const bf16 *)a.q_abs, (const bf16 *)a.q_rope, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
     return e;
@@ -869,14 +865,16 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
 void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int *prefix, int *chunk,
                      uint32_t *status, cudaStream_t s)
 {
-    decode_schedule_kernel<<<1, 1024, 0, s>>>(seq_lens, B, max_seq, n_ranges, prefix, chunk, status);
+    launch_ex(decode_schedule_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, B, max_seq, n_ranges, prefix, chunk,
+              status);
     note_launch();
 }
 
 void decode_combine(const int *prefix, const int *chunk, int B, int H, int r_lat, const float *o_part,
                     const float *ml_part, void *o_lat, cudaStream_t s)
 {
-    decode_combine_tc_kernel<<<dim3(H, B), 128, 0, s>>>(prefix, chunk, B, H, r_lat, o_part, ml_part, (bf16 *)o_lat);
+    launch_ex(decode_combine_tc_kernel, dim3(H, B), dim3(128), 0, s, 1, prefix, chunk, B, H, r_lat, o_part, ml_part,
+              (bf16 *)o_lat);
     note_launch();
 }
 

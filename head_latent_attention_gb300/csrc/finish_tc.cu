@@ -151,14 +151,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_finish_kernel(const __grid
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // 1. The weights of head h, in the background.
+    // 1. The weights of head h, in the background (they do not depend on
+    // earlier kernels, so they go out before the wait for them).
     if (threadIdx.x == 0) {
+        ptx::pdl_trigger();
         ptx::prefetch_tmap(&tw);
         ptx::mbar_expect_tx(w_full, C::kBlocks * kWBlk);
 #pragma unroll
         for (int kb = 0; kb < C::kBlocks; ++kb) ptx::tma_load_2d(sW + kb * kWBlk, &tw, w_full, kb * 64, h * kDv);
     }
 
+    ptx::pdl_wait();
     // 2. Merged latent averages of the group's sequences, one per warp pass.
     for (int t = warp; t < kTok; t += kThreads / 32) {
         uint32_t v[R / 64];
@@ -247,9 +250,9 @@ cudaError_t launch_finish(const FinishArgs &a, cudaStream_t s)
     p.o_lat = (const bf16 *)a.o_lat;
     p.o = (bf16 *)a.o;
     p.status = a.status;
-    decode_finish_kernel<R><<<dim3(a.H, (a.B + kTok - 1) / kTok), kThreads, C::kSmem, s>>>(tw, p);
+    e = launch_ex(decode_finish_kernel<R>, dim3(a.H, (a.B + kTok - 1) / kTok), dim3(kThreads), C::kSmem, s, 1, tw, p);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

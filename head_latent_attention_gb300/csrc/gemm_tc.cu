@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nk = (p.K + kBK - 1) / kBK;
     bool ok = true;
 
+    if (threadIdx.x == 0) ptx::pdl_trigger();
     if (warp == 0) {
         if (ptx::elect_one()) {
             ptx::prefetch_tmap(&tmA);
@@ -200,6 +201,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pending[S];
 #pragma unroll
             for (int i = 0; i < S; ++i) pending[i] = -1;
+            // Weight (B) tile kb of a unit into a stage.
+            auto load_b = [&](int st, const CUtensorMap *tmB, int z, int brow, int kb) {
+                uint8_t *dB = sB + st * C::kBBytes;
+                if (!kBMN) {
+                    ptx::tma_load_2d(dB, tmB, &full[st], (int)(z * p.b_col_batch) + kb * kBK,
+                                     (int)(z * p.b_row_batch) + brow);
+                } else {
+#pragma unroll
+                    for (int a = 0; a < BN / 64; ++a)
+                        ptx::tma_load_2d(dB + a * (kBK * 128), tmB, &full[st], (int)(z * p.b_col_batch) + brow + a * 64,
+                                         (int)(z * p.b_row_batch) + kb * kBK);
+                }
+            };
+            // The weights do not depend on earlier kernels: the first unit's
+            // first stages of B go out before the wait for the previous
+            // kernel, overlapping its tail.
+            int pre = 0;
+            if ((int)blockIdx.x < num_units) {
+                int z, mt, nt;
+                const int u = blockIdx.x;
+                tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
+                const int kb0 = (u / num_tiles) * p.kb_per_split, kb1 = min(nk, kb0 + p.kb_per_split);
+                const int sg = segment_of(p, nt * BN);
+                const CUtensorMap *tmB = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
+                pre = max(0, min(S, kb1 - kb0));
+                for (int i = 0; i < pre; ++i) {
+                    ptx::mbar_expect_tx(&full[i], C::kStageBytes);
+                    load_b(i, tmB, z, nt * BN - segment_start(p, sg), kb0 + i);
+                }
+            }
+            ptx::pdl_wait();
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
                 int z, mt, nt;
                 tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
@@ -210,20 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const CUtensorMap *tmB = sg == 0 ? &tmB0 : (sg == 1 ? &tmB1 : &tmB2);
                 const int brow = nt * BN - segment_start(p, sg);  // first weight row of the tile in its segment
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-                    ptx::mbar_expect_tx(&full[stage], C::kStageBytes);
-                    ptx::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], ax + kb * kBK, ay);
-                    uint8_t *dB = sB + stage * C::kBBytes;
-                    if (!kBMN) {
-                        ptx::tma_load_2d(dB, tmB, &full[stage], (int)(z * p.b_col_batch) + kb * kBK,
-                                         (int)(z * p.b_row_batch) + brow);
+                    if (pre > 0) {
+                        // Stage already armed and holding its weights.
+                        --pre;
                     } else {
-#pragma unroll
-                        for (int a = 0; a < BN / 64; ++a)
-                            ptx::tma_load_2d(dB + a * (kBK * 128), tmB, &full[stage],
-                                             (int)(z * p.b_col_batch) + brow + a * 64,
-                                             (int)(z * p.b_row_batch) + kb * kBK);
+                        if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                        ptx::mbar_expect_tx(&full[stage], C::kStageBytes);
+                        load_b(stage, tmB, z, brow, kb);
                     }
+                    ptx::tma_load_2d(sA + stage * C::kABytes, &tmA, &full[stage], ax + kb * kBK, ay);
                     pending[stage] = (int)phase;
                     if (++stage == S) { stage = 0; phase ^= 1; }
                 }
@@ -235,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (pending[i] >= 0) ptx::mbar_wait(&full[i], (uint32_t)pending[i], &never);
         }
     } else if (warp == 1) {
+        ptx::pdl_wait();
         if (ptx::elect_one()) {
             constexpr uint32_t idesc = ptx::idesc_bf16(kBM, BN, false, kBMN);
             int stage = 0;
@@ -270,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) *abort_flag = 1;
         }
     } else {
+        ptx::pdl_wait();
         const int quad = warp % 4;  // tensor-memory lane quadrant this warp may access
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -347,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int NC>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(TcGemmParams p)
 {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const int chunks = p.N / NC;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (int64_t)p.M * chunks) return;
@@ -560,17 +591,17 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     static int smem_dev = -1;
     cudaError_t e = smem_limit_once(smem_dev, (const void *)gemm_tc_kernel<BN, kBMN>, C::kSmem);
     if (e != cudaSuccess) return e;
-    gemm_tc_kernel<BN, kBMN><<<std::min(units, num_sms), kThreads, C::kSmem, s>>>(ta, tb[0], tb[1], tb[2], p);
+    e = launch_ex(gemm_tc_kernel<BN, kBMN>, dim3(std::min(units, num_sms)), dim3(kThreads), C::kSmem, s, 1, ta,
+                  tb[0], tb[1], tb[2], p);
     note_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
     if (pl.splits > 1) {
         const int nc = half_rope ? 64 : 8;
         const int64_t threads = (int64_t)a.M * (n_total / nc);
         const unsigned blocks = (unsigned)((threads + 255) / 256);
-        if (nc == 64) splitk_reduce_kernel<64><<<blocks, 256, 0, s>>>(p);
-        else splitk_reduce_kernel<8><<<blocks, 256, 0, s>>>(p);
+        if (nc == 64) e = launch_ex(splitk_reduce_kernel<64>, dim3(blocks), dim3(256), 0, s, 1, p);
+        else e = launch_ex(splitk_reduce_kernel<8>, dim3(blocks), dim3(256), 0, s, 1, p);
         note_launch();
-        e = cudaGetLastError();
     }
     return e;
 }

@@ -38,6 +38,41 @@ inline cudaError_t smem_limit_once(int &set_on_device, const void *func, int byt
     return e;
 }
 
+// Launch of a tensor-core-path kernel with programmatic stream serialisation
+// (and, when cluster_x > 1, a cluster of cluster_x CTAs along x): the kernel
+// may begin while its predecessor in the stream finishes, so every kernel
+// launched this way calls ptx::pdl_wait() before touching memory that other
+// kernels write.  Setting the environment variable MLA_PDL=0 before the first
+// launch turns the attribute off (plain stream order).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             int cluster_x, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Workspace status bits (mirrors the values documented in mla.h).
 constexpr uint32_t kStatusPos = 1u;
 constexpr uint32_t kStatusSeq = 2u;

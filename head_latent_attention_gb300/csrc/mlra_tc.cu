@@ -177,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int L = p.H / p.hpb;
 
+    if (threadIdx.x == 0) ptx::pdl_trigger();
     // Query and P rows beyond the block's heads stay zero for the whole kernel.
     for (int i = threadIdx.x; i < (kQBytes + 2 * kPBytes) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(sQ)[i] = make_uint4(0, 0, 0, 0);
@@ -202,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    ptx::pdl_wait();  // the schedule, queries and cache come from earlier kernels
     const uint32_t tmem = bar->tmem;
     const int chunk = *p.chunk;
     const int cta = blockIdx.x;
@@ -530,7 +532,7 @@ cudaError_t mlra_tc(const MlraTcArgs &a, cudaStream_t s)
     p.status = a.status;
     (void)L;
     profile_begin(MLA_PROFILE_DECODE_ATTENTION, s);
-    mlra_tc_kernel<<<a.n_ctas, kThreads, kSmem, s>>>(tkv, tq, p);
+    e = launch_ex(mlra_tc_kernel, dim3(a.n_ctas), dim3(kThreads), kSmem, s, 1, tkv, tq, p);
     profile_end(MLA_PROFILE_DECODE_ATTENTION, s);
     note_launch();
     return cudaGetLastError();

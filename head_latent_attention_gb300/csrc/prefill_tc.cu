@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tV, PreTcParams p)
 {
     using C = PCfg<NQ, NV>;
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sKV = smem + C::kOffKV;
@@ -368,6 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 __global__ void __launch_bounds__(256) rope_to_f16_kernel(const uint16_t *rope, int64_t stride, int max_seq,
                                                           int64_t kv_rows, int B, uint16_t *out)
 {
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // one 8-element chunk
     const int64_t total = (int64_t)B * kv_rows * 8;
     if (i >= total) return;
@@ -394,9 +398,11 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
         if (!make_tmap_bf16(&tqr, a.q_rope, T, (int64_t)a.H * 64, (int64_t)a.H * 64, 64, kQ) ||
             !make_tmap_bf16(&tkr, a.k_rope16, KR, 64, 64, 64, kBN))
             return cudaErrorInvalidValue;
-        rope_to_f16_kernel<<<dim3((unsigned)((KR * 64 / 8 + 255) / 256)), 256, 0, s>>>(
-            (const uint16_t *)a.rope, a.rope_stride, a.max_seq, a.kv_rows, a.B, (uint16_t *)a.k_rope16);
+        cudaError_t e = launch_ex(rope_to_f16_kernel, dim3((unsigned)((KR * 64 / 8 + 255) / 256)), dim3(256), 0, s,
+                                  1, (const uint16_t *)a.rope, a.rope_stride, a.max_seq, a.kv_rows, a.B,
+                                  (uint16_t *)a.k_rope16);
         note_launch();
+        if (e != cudaSuccess) return e;
     } else {
         tqr = tq;
         tkr = tk;
@@ -415,10 +421,10 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
     p.status = a.status;
     dim3 grid(((a.S + kQ - 1) / kQ + 1) / 2, a.H, a.B);
     profile_begin(MLA_PROFILE_PREFILL_ATTENTION, s);
-    prefill_tc_kernel<NQ, NV><<<grid, kThreads, C::kSmem, s>>>(tq, tqr, tk, tkr, tv, p);
+    e = launch_ex(prefill_tc_kernel<NQ, NV>, grid, dim3(kThreads), C::kSmem, s, 1, tq, tqr, tk, tkr, tv, p);
     profile_end(MLA_PROFILE_PREFILL_ATTENTION, s);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

@@ -31,6 +31,18 @@ __device__ __forceinline__ uint32_t elect_one()
     return pred;
 }
 
+// ------------------------------------------------ programmatic dependent launch
+// A kernel launched with programmatic stream serialisation may start while
+// the previous kernel of the stream is still running.  pdl_wait() returns once
+// every prerequisite grid has completed and its memory operations are
+// visible; each such kernel calls it before its first access to memory that an
+// earlier kernel writes or reads, and only immutable inputs (weights, tensor
+// maps) may be touched before it.  pdl_trigger() lets the next kernel of the
+// stream be scheduled (its CTAs start as resources free up).  Both are no-ops
+// for a kernel launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
