@@ -573,21 +573,31 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
 
     // q_abs[b, h] = W_UK,h^T q_nope[b, h]: per head h, [B, d_nope] x [d_nope, r_lat].
     // (MLRA: the L stacked blocks [L, H*d/L, r/L] read as [H*d, r/L] rows.)
-    GemmArgs ga;
-    ga.A = Mat2D{q_nope, B, (int64_t)H * c.d_nope, (int64_t)H * c.d_nope};
-    ga.a_col_batch = c.d_nope;
-    ga.B = Mat2D{w->W_UK, (int64_t)H * c.d_nope, r_lat, r_lat};
-    ga.b_row_batch = c.d_nope;
-    ga.trans_b = true;
-    ga.M = B; ga.N = r_lat; ga.K = c.d_nope; ga.batch = H;
-    ga.epi.out = q_abs; ga.epi.ldc = (int64_t)H * r_lat; ga.epi.batch_stride = r_lat;
-    MLA_TRY(run_gemm(h, ga, (uint32_t *)ws, s));
+    const bool tc_split = use_tc_decode(h) || use_mlra_tc(h);
+    if (tc_split && absorb_supported(r_lat, c.d_nope)) {
+        AbsorbArgs ab;
+        ab.B = B; ab.H = H; ab.r_lat = r_lat; ab.d_nope = c.d_nope;
+        ab.q_nope = q_nope;
+        ab.W_UK = w->W_UK;
+        ab.q_abs = q_abs;
+        ab.status = (uint32_t *)ws;
+        MLA_TRY_CUDA(absorb(ab, s));
+    } else {
+        GemmArgs ga;
+        ga.A = Mat2D{q_nope, B, (int64_t)H * c.d_nope, (int64_t)H * c.d_nope};
+        ga.a_col_batch = c.d_nope;
+        ga.B = Mat2D{w->W_UK, (int64_t)H * c.d_nope, r_lat, r_lat};
+        ga.b_row_batch = c.d_nope;
+        ga.trans_b = true;
+        ga.M = B; ga.N = r_lat; ga.K = c.d_nope; ga.batch = H;
+        ga.epi.out = q_abs; ga.epi.ldc = (int64_t)H * r_lat; ga.epi.batch_stride = r_lat;
+        MLA_TRY(run_gemm(h, ga, (uint32_t *)ws, s));
+    }
 
     const float scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
     // The tensor-core kernels leave split sequences as partials in slot order
     // (range + sequence); they are merged by the fused finish kernel or by
     // decode_combine before the value up-projection GEMM.
-    const bool tc_split = use_tc_decode(h) || use_mlra_tc(h);
     int *prefix = (int *)(wsb + L.prefix);
     if (use_tc_decode(h)) {
         DecodeTcArgs t;

@@ -222,6 +222,19 @@ void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, 
 void decode_combine(const int *prefix, const int *chunk, int B, int H, int r_lat, const float *o_part,
                     const float *ml_part, void *o_lat, cudaStream_t s);
 
+// Absorbed decode queries (absorb_tc.cu): q_abs[b, h] = W_UK,h^T q_nope[b, h]
+// with W_UK,h = rows [128 h, 128 h + 128) of W_UK viewed as [H * 128, r_lat].
+// bfloat16, d_nope == 128, r_lat in {256, 512}.
+struct AbsorbArgs {
+    int B, H, r_lat, d_nope;
+    const void *q_nope;  // [B, H * 128]
+    const void *W_UK;
+    void *q_abs;         // [B, H, r_lat]
+    uint32_t *status;
+};
+bool absorb_supported(int r_lat, int d_nope);
+cudaError_t absorb(const AbsorbArgs &a, cudaStream_t s);
+
 // Merge of the split-KV partials fused with the value up-projection
 // (finish_tc.cu): o[b, h] = W_UV,h o_lat[b, h] with o_lat merged on chip from
 // the partials decode_tc / mlra_tc leave (same slot layout as decode_combine).
