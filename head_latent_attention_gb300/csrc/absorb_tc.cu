@@ -78,8 +78,10 @@ __global__ void __launch_bounds__(kThreads, 1) absorb_kernel(const __grid_consta
         ptx::prefetch_tmap(&tw);
         ptx::prefetch_tmap(&tq);
         ptx::mbar_expect_tx(w_full, C::kBoxes * kWBox);
+        const uint64_t evict_first = ptx::policy_evict_first();  // each weight byte is read once
 #pragma unroll
-        for (int i = 0; i < C::kBoxes; ++i) ptx::tma_load_2d(sW + i * kWBox, &tw, w_full, i * 64, h * kD);
+        for (int i = 0; i < C::kBoxes; ++i)
+            ptx::tma_load_2d_hint(sW + i * kWBox, &tw, w_full, i * 64, h * kD, evict_first);
         // The queries come from the projection kernel.
         ptx::pdl_wait();
         ptx::mbar_expect_tx(q_full, 2 * kQBox);

@@ -157,8 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_finish_kernel(const __grid
         ptx::pdl_trigger();
         ptx::prefetch_tmap(&tw);
         ptx::mbar_expect_tx(w_full, C::kBlocks * kWBlk);
+        const uint64_t evict_first = ptx::policy_evict_first();  // each weight byte is read once
 #pragma unroll
-        for (int kb = 0; kb < C::kBlocks; ++kb) ptx::tma_load_2d(sW + kb * kWBlk, &tw, w_full, kb * 64, h * kDv);
+        for (int kb = 0; kb < C::kBlocks; ++kb)
+            ptx::tma_load_2d_hint(sW + kb * kWBlk, &tw, w_full, kb * 64, h * kDv, evict_first);
     }
 
     ptx::pdl_wait();

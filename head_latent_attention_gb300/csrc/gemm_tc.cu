@@ -201,10 +201,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             int pending[S];
 #pragma unroll
             for (int i = 0; i < S; ++i) pending[i] = -1;
-            // Weight (B) tile kb of a unit into a stage.
+            // Weight (B) tile kb of a unit into a stage.  With a single row
+            // tile every weight byte is read once: it is marked evict-first so
+            // that the stream does not push reusable lines out of L2.
+            const bool stream_b = p.tiles_m == 1 && p.batch == 1;
+            const uint64_t evict_first = ptx::policy_evict_first();
             auto load_b = [&](int st, const CUtensorMap *tmB, int z, int brow, int kb) {
                 uint8_t *dB = sB + st * C::kBBytes;
-                if (!kBMN) {
+                if (!kBMN && stream_b) {
+                    ptx::tma_load_2d_hint(dB, tmB, &full[st], kb * kBK, brow, evict_first);
+                } else if (!kBMN) {
                     ptx::tma_load_2d(dB, tmB, &full[st], (int)(z * p.b_col_batch) + kb * kBK,
                                      (int)(z * p.b_row_batch) + brow);
                 } else {
