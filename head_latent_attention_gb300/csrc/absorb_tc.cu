@@ -46,7 +46,8 @@ struct AbsCfg {
 
 struct AbsParams {
     int B, H;
-    bf16 *q_abs;  // [B, H, R]
+    bf16 *q_abs;  // [B, H, R], or head-interleaved (see AbsorbArgs)
+    bool interleave;
     uint32_t *status;
 };
 
@@ -131,7 +132,10 @@ __global__ void __launch_bounds__(kThreads, 1) absorb_kernel(const __grid_consta
             uint32_t r[32];
             ptx::tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + m * kTok + half * 32, r);
             ptx::tmem_ld_wait();
-            bf16 *dst = p.q_abs + ((int64_t)(b0 + half * 32) * p.H + h) * R + m * 128 + quad * 32 + lane;
+            const int col = m * 128 + quad * 32 + lane;  // latent column
+            bf16 *dst = p.interleave
+                            ? p.q_abs + (((int64_t)(b0 + half * 32) * (R / 8) + col / 8) * p.H + h) * 8 + col % 8
+                            : p.q_abs + ((int64_t)(b0 + half * 32) * p.H + h) * R + col;
 #pragma unroll
             for (int t = 0; t < 32; ++t)
                 if (t < nt) dst[(int64_t)t * p.H * R] = __float2bfloat16_rn(__uint_as_float(r[t]));
@@ -170,6 +174,7 @@ cudaError_t launch_absorb(const AbsorbArgs &a, cudaStream_t s)
     AbsParams p;
     p.B = a.B; p.H = a.H;
     p.q_abs = (bf16 *)a.q_abs;
+    p.interleave = a.interleave;
     p.status = a.status;
     e = launch_ex(absorb_kernel<R>, dim3(a.H, (a.B + kTok - 1) / kTok), dim3(kThreads), C::kSmem, s, 1, tw, tq, p);
     note_launch();

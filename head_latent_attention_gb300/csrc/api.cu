@@ -53,6 +53,10 @@ void profile_end(int which, cudaStream_t s) { profile_record(g_prof_end[which], 
 namespace {
 
 constexpr int kDecodeChunk = 512;  // keys per split of the CUDA-core decode
+// Estimated cost of one extra segment of the tensor-core MLA decode, in keys:
+// the segment-end stores and the next query load take about as long as
+// 400 keys of attention.
+constexpr int kSegmentCostKeys = 384;
 constexpr double kLog2e = 1.4426950408889634;
 
 size_t esize(const mla_config &c) { return c.dtype == MLA_DTYPE_F32 ? 4 : 2; }
@@ -212,8 +216,10 @@ OutProjWs out_proj_ws(const mla_handle *h, int64_t T)
 bool use_tc_decode(const mla_handle *h)
 {
     const mla_config &c = h->cfg;
+    // The kernel reads the absorbed queries in the head-interleaved layout
+    // that only the absorption kernel writes.
     return c.dtype == MLA_DTYPE_BF16 && c.variant == MLA_VARIANT_DECOUPLED && h->decode_clusters > 0 &&
-           decode_tc_supported(c.n_heads, c.r_kv, c.d_rope);
+           decode_tc_supported(c.n_heads, c.r_kv, c.d_rope) && absorb_supported(r_lat_of(c), c.d_nope);
 }
 
 bool use_mlra_tc(const mla_handle *h)
@@ -236,7 +242,8 @@ DecodeWs decode_ws(const mla_handle *h, int B)
     w.o_part = round_up(w.o_lat + lat * esize(c), 256);
     w.ml_part = round_up(w.o_part + parts * r_lat_of(c) * 4, 256);
     w.prefix = round_up(w.ml_part + parts * 2 * 4, 256);
-    w.end = round_up(w.prefix + ((size_t)B + 2) * 4, 256);
+    // the split-KV schedule (at most one range per SM)
+    w.end = round_up(w.prefix + decode_sched_bytes(B, h->num_sms), 256);
     return w;
 }
 
@@ -574,12 +581,26 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     // q_abs[b, h] = W_UK,h^T q_nope[b, h]: per head h, [B, d_nope] x [d_nope, r_lat].
     // (MLRA: the L stacked blocks [L, H*d/L, r/L] read as [H*d, r/L] rows.)
     const bool tc_split = use_tc_decode(h) || use_mlra_tc(h);
+    const int n_ranges = use_tc_decode(h) ? h->decode_clusters : mlra_tc_ctas();
+    const DecodeSched sc = decode_sched_at(wsb + L.prefix, B, n_ranges);
+    if (tc_split) {
+        // The split-KV schedule first: the attention kernel reads it (and
+        // starts its cache loads) while the absorption kernel still runs.
+        // The MLA kernel's ranges are balanced by estimated time, a
+        // sequence start costing about as much as kSegmentCostKeys keys
+        // (segment-end stores and the next query load); the MLRA kernel's
+        // segments are cheap and its ranges uniform.
+        decode_schedule(seq_lens, B, c.max_seq, n_ranges, use_tc_decode(h) ? kSegmentCostKeys : 0, sc,
+                        (uint32_t *)ws, s);
+        MLA_TRY_CUDA(cudaGetLastError());
+    }
     if (tc_split && absorb_supported(r_lat, c.d_nope)) {
         AbsorbArgs ab;
         ab.B = B; ab.H = H; ab.r_lat = r_lat; ab.d_nope = c.d_nope;
         ab.q_nope = q_nope;
         ab.W_UK = w->W_UK;
         ab.q_abs = q_abs;
+        ab.interleave = use_tc_decode(h);  // the tensor-core MLA decode reads it head-interleaved
         ab.status = (uint32_t *)ws;
         MLA_TRY_CUDA(absorb(ab, s));
     } else {
@@ -598,7 +619,6 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     // The tensor-core kernels leave split sequences as partials in slot order
     // (range + sequence); they are merged by the fused finish kernel or by
     // decode_combine before the value up-projection GEMM.
-    int *prefix = (int *)(wsb + L.prefix);
     if (use_tc_decode(h)) {
         DecodeTcArgs t;
         t.B = B; t.H = H; t.r_kv = c.r_kv; t.d_rope = c.d_rope;
@@ -607,8 +627,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         t.lat = cache->lat; t.lat_stride = cache->lat_stride;
         t.rope = cache->rope; t.rope_stride = cache->rope_stride;
         t.seq_lens = seq_lens;
-        t.prefix = (int *)(wsb + L.prefix);
-        t.chunk = t.prefix + B + 1;
+        t.sc = sc;
         t.scale_log2 = scale_log2;
         t.o_lat = o_lat;
         t.o_part = (float *)(wsb + L.o_part);
@@ -626,8 +645,8 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         t.q_abs = q_abs;
         t.lat = cache->lat; t.lat_stride = cache->lat_stride;
         t.seq_lens = seq_lens;
-        t.prefix = (int *)(wsb + L.prefix);
-        t.chunk = t.prefix + B + 1;
+        t.prefix = sc.prefix;
+        t.chunk = sc.chunk;
         t.scale_log2 = scale_log2;
         t.o_lat = o_lat;
         t.o_part = (float *)(wsb + L.o_part);
@@ -658,7 +677,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     if (tc_split && decode_finish_supported(r_lat, c.d_v)) {
         FinishArgs f;
         f.B = B; f.H = H; f.r_lat = r_lat; f.d_v = c.d_v;
-        f.prefix = prefix; f.chunk = prefix + B + 1;
+        f.seq_fc = sc.seq_fc; f.seq_lc = sc.seq_lc;
         f.o_part = (float *)(wsb + L.o_part);
         f.ml_part = (float *)(wsb + L.ml_part);
         f.o_lat = o_lat;
@@ -669,8 +688,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         return MLA_OK;
     }
     if (tc_split) {
-        decode_combine(prefix, prefix + B + 1, B, H, r_lat, (float *)(wsb + L.o_part), (float *)(wsb + L.ml_part),
-                       o_lat, s);
+        decode_combine(sc, B, H, r_lat, (float *)(wsb + L.o_part), (float *)(wsb + L.ml_part), o_lat, s);
         MLA_TRY_CUDA(cudaGetLastError());
     }
 

@@ -75,7 +75,16 @@ constexpr int kOffP = kOffX + kXBuf * kXBytes;
 static_assert(kXWarpBytes == 4 * kPGroup, "a warp's staging block is its P rows");
 constexpr int kOffRed = kOffP + 2 * kPBytes;          // reference maxima, segment-end (max, sum)
 constexpr int kOffBar = kOffRed + 6 * kH * 4;
-constexpr int kSmem = kOffBar + 512 + 1024;
+// The cluster's view of the schedule: its range [start, end) of the
+// concatenated keys and the prefix sums of the sequences from the range's
+// first one on (kWin + 1 entries; later ones are read from global memory).
+constexpr int kWin = 63;
+struct SchedWin {
+    int start, end, b0, nwin;
+    int pf[kWin + 1];
+};
+constexpr int kOffSched = kOffBar + 512;
+constexpr int kSmem = kOffSched + (int)sizeof(SchedWin) + 1024;
 static_assert(kOffP % 16 == 0, "P operand alignment");
 static_assert(kSmem <= 232448, "shared memory per CTA");
 // Tensor memory: O in [0, 256), the query (256 latent + 32 rope bf16 = 144
@@ -90,8 +99,7 @@ static_assert(kQRCol + 16 <= 512, "tensor memory columns");
 
 struct DecTcParams {
     int B, H, max_seq;
-    const int *prefix;  // [B + 1] prefix sums of the valid lengths
-    const int *chunk;   // keys per cluster
+    DecodeSched sc;     // prefix sums, range starts, first sequence of each range
     float scale_log2;
     bf16 *o_lat;        // [B, H, r_kv]
     float *o_part;      // [slots, H, r_kv]
@@ -190,28 +198,24 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t w)
 
 // Segments of this cluster's key range [start, end) of the concatenated keys.
 struct SegIter {
+    const SchedWin *w;
     const int *prefix;
     int B, start, end, b;
-    __device__ void init(const int *pf, int nb, int cid, int chunk)
+    __device__ int pf(int i) const { return i - w->b0 <= w->nwin ? w->pf[i - w->b0] : prefix[i]; }
+    __device__ void init(const SchedWin *win, const int *pfx, int nb)
     {
-        prefix = pf;
+        w = win;
+        prefix = pfx;
         B = nb;
-        const int total = pf[nb];
-        start = min(total, cid * chunk);
-        end = min(total, start + chunk);
-        int lo = 0, hi = nb - 1;  // first b with prefix[b + 1] > start
-        while (lo < hi) {
-            int mid = (lo + hi) >> 1;
-            if (pf[mid + 1] > start) hi = mid;
-            else lo = mid + 1;
-        }
-        b = (start < end) ? lo : nb;
+        start = win->start;
+        end = win->end;
+        b = win->b0;
     }
     // Next non-empty segment: sequence b, keys [k0, k1), whole-sequence flag.
     __device__ bool next(int &sb, int &k0, int &k1, bool &whole)
     {
-        while (b < B && prefix[b] < end) {
-            const int lo = prefix[b], hi = prefix[b + 1];
+        while (b < B && pf(b) < end) {
+            const int lo = pf(b), hi = pf(b + 1);
             const int gs = max(start, lo), ge = min(end, hi);
             const int cur = b++;
             if (gs < ge) {
@@ -226,15 +230,34 @@ struct SegIter {
     }
 };
 
+// The range of cluster cid and the prefix window from its first sequence,
+// written by one warp (two rounds of independent loads) and read by every
+// cursor of the CTA after a barrier.
+__device__ void sched_window(SchedWin *w, const DecodeSched &sc, int nb, int cid, int lane)
+{
+    const int *pf = sc.prefix;
+    const int start = sc.range_start[cid], end = sc.range_start[cid + 1], first = sc.range_b0[cid];
+    const int b0 = (start < end) ? first : nb;
+    const int nwin = min(kWin, nb - b0);
+    for (int i = lane; i <= nwin; i += 32) w->pf[i] = pf[b0 + i];
+    if (lane == 0) {
+        w->start = start;
+        w->end = end;
+        w->b0 = b0;
+        w->nwin = nwin;
+    }
+    __syncwarp();
+}
+
 // Walks the tiles of this cluster's segments in order (g: global tile
 // index, t: tile within segment nseg).
 struct TileCursor {
     SegIter it;
     int b, k0, k1, nseg, t, ntiles, g;
     bool whole, valid;
-    __device__ void init(const int *pf, int nb, int cid, int chunk)
+    __device__ void init(const SchedWin *win, const int *pf, int nb)
     {
-        it.init(pf, nb, cid, chunk);
+        it.init(win, pf, nb);
         nseg = -1;
         g = 0;
         valid = true;
@@ -265,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sKV = smem;
     Bars *bar = (Bars *)(smem + kOffBar);
+    SchedWin *win = (SchedWin *)(smem + kOffSched);
     volatile int *abort_flag = &bar->abort;
 
     const uint32_t rank = cluster_rank(), peer = rank ^ 1u;
@@ -272,8 +296,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     // KV loads are issued by thread 0: the first kStages right after the
-    // barriers exist (before the CTA and cluster syncs, so the first HBM
-    // round trip overlaps the setup), the rest from the producer loop.
+    // barriers exist (before the CTA and cluster syncs, and before the wait
+    // for the previous kernel, so the first HBM round trip overlaps both),
+    // the rest from the producer loop.  The schedule and the cache rows are
+    // complete when this kernel starts: the scheduler runs before the
+    // kernel that precedes this one and does not let it start early, and it
+    // waits for every earlier kernel itself.  Only the queries come from the
+    // previous kernel.
     TileCursor ld;
     int pending[kStages];
     uint64_t evict_first = 0;
@@ -323,12 +352,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kXBuf; ++i) ptx::mbar_expect_tx(&bar->x_full[i], kXTx);  // arm every buffer
         ptx::prefetch_tmap(&tmL);
         ptx::prefetch_tmap(&tmR);
+    }
+    if (warp == 0) sched_window(win, p.sc, p.B, cid, lane);
+    if (threadIdx.x == 0) {
         evict_first = ptx::policy_evict_first();
 #pragma unroll
         for (int i = 0; i < kStages; ++i) pending[i] = -1;
-        ptx::pdl_wait();  // the schedule, queries and cache come from earlier kernels
-        ld.init(p.prefix, p.B, cid, *p.chunk);
+        ld.init(win, p.sc.prefix, p.B);
         for (int i = 0; i < kStages && ld.valid; ++i) issue_load();  // fresh ring: no waits
+        ptx::pdl_wait();
     }
     if (warp == 1) ptx::tmem_alloc(&bar->tmem, 512);
     ptx::tc_fence_before();
@@ -337,7 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::pdl_wait();
     const uint32_t tmem = bar->tmem;
-    const int chunk = *p.chunk;
     bool ok = true;
     auto fail = [&]() {
         ok = false;
@@ -363,8 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_o = ptx::idesc_bf16(kH, kLA * 64, false, true);
             const uint32_t kv0 = ptx::smem_u32(sKV), p0 = ptx::smem_u32(smem + kOffP);
             TileCursor qk, pv;
-            qk.init(p.prefix, p.B, cid, chunk);
-            pv.init(p.prefix, p.B, cid, chunk);
+            qk.init(win, p.sc.prefix, p.B);
+            pv.init(win, p.sc.prefix, p.B);
             long long last = clock64();
             while (ok && pv.valid) {
                 bool progressed = false;
@@ -449,13 +480,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nseg > 0 && !ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)) return false;
             ptx::tc_fence_after();
             const bool row_ok = h < p.H;
-            const uint4 *src = reinterpret_cast<const uint4 *>(q_abs + ((int64_t)b * p.H + h) * kRLat + rank * kOCols);
+            // q_abs is stored head-interleaved: 16-byte chunk c of row (b, h) at
+            // ((b * 64 + c) * H + h) * 16 bytes, so that a warp's load of one
+            // chunk for its 32 heads is 512 contiguous bytes.
+            const uint4 *src = reinterpret_cast<const uint4 *>(q_abs) + ((int64_t)b * 64 + rank * 32) * p.H + h;
             const uint4 *rs = reinterpret_cast<const uint4 *>(q_rope + ((int64_t)b * p.H + h) * 64 + rank * 32);
             // Two 128-byte groups of the row in flight at a time.
             uint4 va[8], vb[8], vr[4];
             auto fetch = [&](uint4 (&v)[8], int c) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = row_ok ? src[c * 8 + i] : make_uint4(0, 0, 0, 0);
+                for (int i = 0; i < 8; ++i) v[i] = row_ok ? src[(int64_t)(c * 8 + i) * p.H] : make_uint4(0, 0, 0, 0);
             };
             auto put = [&](const uint4 (&v)[8], int c) {
                 uint32_t w[32];
@@ -526,7 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return true;
         };
         TileCursor nx;  // the next tile of this group to send (sends run two tiles ahead)
-        nx.init(p.prefix, p.B, cid, chunk);
+        nx.init(win, p.sc.prefix, p.B);
         if (grp == 1 && nx.valid) nx.step();
         if (ok && nx.valid) {
             if ((nx.t == 0 && !load_q(nx.b, nx.nseg)) || !send(nx.g)) fail();
@@ -536,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nx.valid) nx.step();
         }
         SegIter it;
-        it.init(p.prefix, p.B, cid, chunk);
+        it.init(win, p.sc.prefix, p.B);
         int b, k0, k1;
         bool whole;
         int g = 0;
@@ -745,14 +779,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, kStatusTimeout);
 }
 
-// Prefix sums of the valid lengths (invalid ones count as 0 and are flagged)
-// and the per-cluster key range.
-__global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seq_lens, int B, int max_seq,
-                                                               int n_clusters, int *prefix, int *chunk,
-                                                               uint32_t *status)
+// Prefix sums of the valid lengths (invalid ones count as 0 and are
+// flagged), then the ranges (see DecodeSched) and each sequence's first and
+// last range.
+__device__ __forceinline__ int last_range_at_or_before(const int *range_start, int n, int x)
 {
-    ptx::pdl_trigger();
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (range_start[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+__global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seq_lens, int B, int max_seq, int n,
+                                                               int seg_cost, DecodeSched sc, uint32_t *status)
+{
+    // No early trigger: the kernel after this one starts only once the
+    // schedule is complete, so the split-KV kernel that follows it may read
+    // the schedule (and anything written before it) before its own wait.
     ptx::pdl_wait();
+    int *prefix = sc.prefix;
     __shared__ int warp_sums[32];
     __shared__ int carry;
     if (threadIdx.x == 0) { carry = 0; prefix[0] = 0; }
@@ -769,16 +817,16 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
         }
         int v = L;
         for (int off = 1; off < 32; off <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, v, off);
-            if ((threadIdx.x & 31) >= off) v += n;
+            const int nb = __shfl_up_sync(0xffffffffu, v, off);
+            if ((threadIdx.x & 31) >= off) v += nb;
         }
         if ((threadIdx.x & 31) == 31) warp_sums[threadIdx.x >> 5] = v;
         __syncthreads();
         if (threadIdx.x < 32) {
             int w = warp_sums[threadIdx.x];
             for (int off = 1; off < 32; off <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, w, off);
-                if (threadIdx.x >= off) w += n;
+                const int nb = __shfl_up_sync(0xffffffffu, w, off);
+                if (threadIdx.x >= off) w += nb;
             }
             warp_sums[threadIdx.x] = w;
         }
@@ -789,29 +837,71 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
         if (threadIdx.x == 1023) carry = incl;
         __syncthreads();
     }
-    if (threadIdx.x == 0) {
-        const int total = prefix[B];
-        *chunk = max(128, (total + n_clusters - 1) / n_clusters);
+    const int total = prefix[B];
+    const int chunk = max(128, (total + n - 1) / n);
+    if (threadIdx.x == 0) *sc.chunk = chunk;
+    // Range starts.  With a segment cost, cost position x of the sequence
+    // walk C(b) = prefix[b] + b * seg_cost (seg_cost phantom keys before
+    // each sequence) is cut into n equal parts.
+    const long long tcost = (long long)total + (long long)seg_cost * B;
+    for (int c = threadIdx.x; c <= n; c += blockDim.x) {
+        int st;
+        if (c == n) {
+            st = total;
+        } else if (seg_cost == 0) {
+            st = (int)min((long long)total, (long long)c * chunk);
+        } else {
+            const long long x = tcost * c / n;
+            int lo = 0, hi = B;  // last b with C(b) <= x
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if ((long long)prefix[mid] + (long long)mid * seg_cost <= x) lo = mid;
+                else hi = mid - 1;
+            }
+            if (lo >= B) {
+                st = total;
+            } else {
+                const long long off = x - ((long long)prefix[lo] + (long long)lo * seg_cost) - seg_cost;
+                const int len = prefix[lo + 1] - prefix[lo];
+                st = prefix[lo] + (int)min((long long)len, max(0ll, off));
+            }
+        }
+        sc.range_start[c] = st;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < n; c += blockDim.x) {
+        const int st = sc.range_start[c], en = sc.range_start[c + 1];
+        int lo = 0, hi = B;  // first b with prefix[b + 1] > st
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid + 1] > st) hi = mid;
+            else lo = mid + 1;
+        }
+        sc.range_b0[c] = st < en ? lo : B;
+    }
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+        const int lo = prefix[b], hi = prefix[b + 1];
+        sc.seq_fc[b] = hi > lo ? last_range_at_or_before(sc.range_start, n, lo) : -1;
+        sc.seq_lc[b] = hi > lo ? last_range_at_or_before(sc.range_start, n, hi - 1) : -1;
     }
 }
 
 // o_lat[b, h] = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s over the
 // partial slots of sequence b (sequences handled by one cluster were written
 // directly; invalid ones are zeroed).
-__global__ void __launch_bounds__(128) decode_combine_tc_kernel(const int *prefix, const int *chunk_ptr, int B,
-                                                                int H, int r_lat, const float *o_part,
-                                                                const float *ml_part, bf16 *o_lat)
+__global__ void __launch_bounds__(128) decode_combine_tc_kernel(DecodeSched sc, int B, int H, int r_lat,
+                                                                const float *o_part, const float *ml_part,
+                                                                bf16 *o_lat)
 {
     ptx::pdl_trigger();
     ptx::pdl_wait();
     const int h = blockIdx.x, b = blockIdx.y;
-    const int lo = prefix[b], hi = prefix[b + 1], chunk = *chunk_ptr;
+    const int fc = sc.seq_fc[b], lc = sc.seq_lc[b];
     bf16 *dst = o_lat + ((int64_t)b * H + h) * r_lat;
-    if (hi <= lo) {
+    if (fc < 0) {
         for (int c = threadIdx.x; c < r_lat; c += blockDim.x) dst[c] = __float2bfloat16_rn(0.f);
         return;
     }
-    const int fc = lo / chunk, lc = (hi - 1) / chunk;
     if (fc == lc) return;
     float m = -INFINITY;
     for (int c = fc; c <= lc; ++c) m = fmaxf(m, ml_part[((int64_t)(c + b) * H + h) * 2]);
@@ -838,15 +928,12 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
     if (!make_tmap_bf16(&tl, a.lat, c_rows, kRLat, a.lat_stride, 64, kBKV) ||
         !make_tmap_bf16(&tr, a.rope, c_rows, 64, a.rope_stride, 32, kBKV))
         return cudaErrorInvalidValue;
-    decode_schedule(a.seq_lens, a.B, a.max_seq, a.n_clusters, a.prefix, a.chunk, a.status, s);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     static int smem_dev = -1;
-    e = smem_limit_once(smem_dev, (const void *)decode_tc_kernel, kSmem);
+    cudaError_t e = smem_limit_once(smem_dev, (const void *)decode_tc_kernel, kSmem);
     if (e != cudaSuccess) return e;
     DecTcParams p;
     p.B = a.B; p.H = a.H; p.max_seq = a.max_seq;
-    p.prefix = a.prefix; p.chunk = a.chunk;
+    p.sc = a.sc;
     p.scale_log2 = a.scale_log2;
     p.o_lat = (bf16 *)a.o_lat;
     p.o_part = a.o_part;
@@ -862,18 +949,32 @@ cudaError_t launch_decode_tc(const DecodeTcArgs &a, cudaStream_t s)
 
 }  // namespace
 
-void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int *prefix, int *chunk,
+size_t decode_sched_bytes(int B, int n) { return ((size_t)B + 1 + 1 + (n + 1) + n + 2 * (size_t)B) * sizeof(int); }
+
+DecodeSched decode_sched_at(void *base, int B, int n)
+{
+    DecodeSched sc;
+    sc.prefix = (int *)base;
+    sc.chunk = sc.prefix + B + 1;
+    sc.range_start = sc.chunk + 1;
+    sc.range_b0 = sc.range_start + n + 1;
+    sc.seq_fc = sc.range_b0 + n;
+    sc.seq_lc = sc.seq_fc + B;
+    return sc;
+}
+
+void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int seg_cost, const DecodeSched &sc,
                      uint32_t *status, cudaStream_t s)
 {
-    launch_ex(decode_schedule_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, B, max_seq, n_ranges, prefix, chunk,
+    launch_ex(decode_schedule_kernel, dim3(1), dim3(1024), 0, s, 1, seq_lens, B, max_seq, n_ranges, seg_cost, sc,
               status);
     note_launch();
 }
 
-void decode_combine(const int *prefix, const int *chunk, int B, int H, int r_lat, const float *o_part,
-                    const float *ml_part, void *o_lat, cudaStream_t s)
+void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const float *o_part, const float *ml_part,
+                    void *o_lat, cudaStream_t s)
 {
-    launch_ex(decode_combine_tc_kernel, dim3(H, B), dim3(128), 0, s, 1, prefix, chunk, B, H, r_lat, o_part, ml_part,
+    launch_ex(decode_combine_tc_kernel, dim3(H, B), dim3(128), 0, s, 1, sc, B, H, r_lat, o_part, ml_part,
               (bf16 *)o_lat);
     note_launch();
 }

@@ -41,8 +41,8 @@ struct FinCfg {
 };
 
 struct FinParams {
-    const int *prefix;     // [B + 1] prefix sums of the valid lengths
-    const int *chunk;      // keys per range
+    const int *seq_fc;     // [B] first range covering each sequence (-1: empty)
+    const int *seq_lc;     // [B] last range covering each sequence
     int B, H;
     const float *o_part;   // [(ranges + B), H, R] unnormalised partial averages
     const float *ml_part;  // [(ranges + B), H, 2] (max in log2 units, denominator)
@@ -60,10 +60,8 @@ __device__ __forceinline__ void merged_row(const FinParams &p, int b, int h, int
 #pragma unroll
     for (int i = 0; i < CPL / 2; ++i) out[i] = 0u;
     if (b >= p.B) return;
-    const int lo = p.prefix[b], hi = p.prefix[b + 1];
-    if (hi <= lo) return;  // empty or invalid length: zero output
-    const int chunk = *p.chunk;
-    const int fc = lo / chunk, lc = (hi - 1) / chunk;
+    const int fc = p.seq_fc[b], lc = p.seq_lc[b];
+    if (fc < 0) return;  // empty or invalid length: zero output
     if (fc == lc) {
         const uint4 *src = reinterpret_cast<const uint4 *>(p.o_lat + ((int64_t)b * p.H + h) * R + lane * CPL);
 #pragma unroll
@@ -246,7 +244,7 @@ cudaError_t launch_finish(const FinishArgs &a, cudaStream_t s)
     cudaError_t e = smem_limit_once(smem_dev, (const void *)decode_finish_kernel<R>, C::kSmem);
     if (e != cudaSuccess) return e;
     FinParams p;
-    p.prefix = a.prefix; p.chunk = a.chunk;
+    p.seq_fc = a.seq_fc; p.seq_lc = a.seq_lc;
     p.B = a.B; p.H = a.H;
     p.o_part = a.o_part; p.ml_part = a.ml_part;
     p.o_lat = (const bf16 *)a.o_lat;

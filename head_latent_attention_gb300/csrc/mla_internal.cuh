@@ -192,19 +192,31 @@ struct DecodeArgs {
 };
 cudaError_t decode_simt(const DecodeArgs &a, cudaStream_t s);
 
+// Split-KV schedule shared by the decode kernels, in the workspace.  The
+// concatenation of all sequences' keys is cut into n contiguous ranges, one
+// per CTA or cluster; a range splits into one segment per sequence it
+// touches, and the partial result of range c for sequence b goes to slot
+// c + b (unique, since ranges and sequences both advance monotonically).
+struct DecodeSched {
+    int *prefix;       // [B + 1] prefix sums of the valid lengths (invalid ones count 0)
+    int *chunk;        // [1] keys per range of the uniform split
+    int *range_start;  // [n + 1] first key of each range; [n] = total keys
+    int *range_b0;     // [n] first sequence of each range (B when empty)
+    int *seq_fc;       // [B] first range covering each sequence (-1: empty or invalid)
+    int *seq_lc;       // [B] last range covering each sequence
+};
 // Tensor-core split-KV decode (decode_tc.cu): DECOUPLED, bfloat16, H <= 128,
 // r_kv == 512, d_rope == 64.
 struct DecodeTcArgs {
     int B, H, r_kv, d_rope, max_batch, max_seq, n_clusters;
-    const void *q_abs;        // [B, H, r_kv]
+    const void *q_abs;        // [B, r_kv / 8, H, 8] (head-interleaved 16-byte chunks, see AbsorbArgs)
     const void *q_rope;       // [B, H, d_rope]
     const void *lat;          // cache latent rows
     int64_t lat_stride;
     const void *rope;         // cache rope rows
     int64_t rope_stride;
     const int32_t *seq_lens;  // device [B]
-    int *prefix;              // workspace [B + 1]
-    int *chunk;               // workspace [1]
+    DecodeSched sc;           // written by decode_schedule (n = n_clusters)
     float scale_log2;
     void *o_lat;              // [B, H, r_kv] bf16
     float *o_part;            // [n_clusters + B, H, r_kv]
@@ -213,14 +225,20 @@ struct DecodeTcArgs {
 };
 int decode_tc_max_clusters();
 
-// Device-side scheduling shared by the split-KV decode kernels: prefix sums
-// of the valid lengths and the keys per work range (n_ranges ranges), and
-// the log-sum-exp merge of the partials of sequences split across ranges
-// (slot of range c and sequence b: c + b).
-void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int *prefix, int *chunk,
+size_t decode_sched_bytes(int B, int n);
+DecodeSched decode_sched_at(void *base, int B, int n);
+// seg_cost == 0: uniform ranges of `chunk` keys.  seg_cost > 0: ranges of
+// equal estimated cost, a sequence start counting as seg_cost extra keys
+// (the per-segment overhead of the kernel), which also moves range starts
+// that fall within seg_cost keys after a sequence start onto that start.
+// decode_schedule runs before the kernel that precedes the split-KV kernel
+// (the decode kernels read its output before their own dependency wait; see
+// decode_tc.cu), so callers launch it first.
+void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int seg_cost, const DecodeSched &sc,
                      uint32_t *status, cudaStream_t s);
-void decode_combine(const int *prefix, const int *chunk, int B, int H, int r_lat, const float *o_part,
-                    const float *ml_part, void *o_lat, cudaStream_t s);
+// Log-sum-exp merge of the partials of split sequences into o_lat.
+void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const float *o_part, const float *ml_part,
+                    void *o_lat, cudaStream_t s);
 
 // Absorbed decode queries (absorb_tc.cu): q_abs[b, h] = W_UK,h^T q_nope[b, h]
 // with W_UK,h = rows [128 h, 128 h + 128) of W_UK viewed as [H * 128, r_lat].
@@ -229,7 +247,8 @@ struct AbsorbArgs {
     int B, H, r_lat, d_nope;
     const void *q_nope;  // [B, H * 128]
     const void *W_UK;
-    void *q_abs;         // [B, H, r_lat]
+    void *q_abs;         // [B, H, r_lat]; interleave: element (b, h, r) at ((b * r_lat / 8 + r / 8) * H + h) * 8 + r % 8
+    bool interleave;
     uint32_t *status;
 };
 bool absorb_supported(int r_lat, int d_nope);
@@ -242,7 +261,7 @@ cudaError_t absorb(const AbsorbArgs &a, cudaStream_t s);
 // of W_UV viewed as [H * 128, r_lat].
 struct FinishArgs {
     int B, H, r_lat, d_v;
-    const int *prefix, *chunk;
+    const int *seq_fc, *seq_lc;  // ranges covering each sequence (DecodeSched)
     const float *o_part, *ml_part;
     const void *o_lat;  // [B, H, r_lat] (single-range sequences)
     const void *W_UV;

@@ -516,11 +516,8 @@ cudaError_t mlra_tc(const MlraTcArgs &a, cudaStream_t s)
     if (!make_tmap_bf16(&tkv, a.lat, (int64_t)a.max_batch * a.max_seq, a.r_kv, a.lat_stride, 64, kKeys) ||
         !make_tmap_bf16(&tq, a.q_abs, (int64_t)a.B * a.H, kR, kR, 64, hpb))
         return cudaErrorInvalidValue;
-    decode_schedule(a.seq_lens, a.B, a.max_seq, a.n_ctas, a.prefix, a.chunk, a.status, s);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     static int smem_dev = -1;
-    e = smem_limit_once(smem_dev, (const void *)mlra_tc_kernel, kSmem);
+    cudaError_t e = smem_limit_once(smem_dev, (const void *)mlra_tc_kernel, kSmem);
     if (e != cudaSuccess) return e;
     MlraParams p;
     p.B = a.B; p.H = a.H; p.hpb = hpb; p.max_seq = a.max_seq;
