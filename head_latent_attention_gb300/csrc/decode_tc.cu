@@ -51,6 +51,10 @@ constexpr int kSBuf = 2;      // score buffers in tensor memory
 constexpr int kSoftmaxThreads = 256;  // warps 2..9
 constexpr int kThreads = 64 + kSoftmaxThreads;
 constexpr float kRescaleThreshold = 8.f;
+// Q K^T(g + 2) is read two tiles ahead by the group that owns tile g, and
+// Q K^T(g + 3) by the other group at about the same time, so it may run
+// three tiles ahead of P.V(g).
+constexpr int kQKAhead = 3;
 constexpr int kLA = 4;        // 64-column latent atoms per CTA (r_kv = 512)
 
 // Shared memory (per CTA): the KV ring, the latent query, two exchange buffers.
@@ -196,6 +200,20 @@ __device__ __forceinline__ float2 unpack_f16(uint32_t w)
     return __half22float2(*reinterpret_cast<const __half2 *>(&w));
 }
 
+// Maximum and sum of a tile row as balanced trees (short dependency chains).
+template <int N>
+__device__ __forceinline__ float tree_max(const float (&v)[N])
+{
+    float t[N / 2];
+#pragma unroll
+    for (int j = 0; j < N / 2; ++j) t[j] = fmaxf(v[2 * j], v[2 * j + 1]);
+#pragma unroll
+    for (int w = N / 4; w >= 3; w /= 2)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+    return fmaxf(fmaxf(t[0], t[1]), t[2]);
+}
+
 // Segments of this cluster's key range [start, end) of the concatenated keys.
 struct SegIter {
     const SchedWin *w;
@@ -321,6 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ld.step();
         return true;
     };
+
     if (threadIdx.x == 0) {
         ptx::pdl_trigger();
         ptx::mbar_init(&bar->q_full, kSoftmaxThreads / 2);  // the group that sends a segment's first tile
@@ -419,7 +438,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         progressed = true;
                     }
                 }
-                if (qk.valid) {
+                // Q K^T runs at most kQKAhead tiles ahead of the next P.V: the
+                // tensor pipe executes in issue order, and a Q K^T queued
+                // early would delay the P.V that frees a KV stage.
+                if (qk.valid && qk.g <= pv.g + kQKAhead) {
                     const int st = qk.g % kStages, sb = qk.g % kSBuf;
                     bool ready = qk.t > 0 || ptx::mbar_test(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
                     ready = ready && ptx::mbar_test(ptx::smem_u32(&bar->kv_full[st]), (qk.g / kStages) & 1);
@@ -606,8 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < kBKV; ++j) s[j] = (j < valid) ? s[j] : -INFINITY;
                     }
-#pragma unroll
-                    for (int j = 0; j < kBKV; ++j) mt = fmaxf(mt, s[j]);
+                    mt = tree_max<kBKV>(s);
                 }
                 // The warp's block of exchange buffer grp is read: the peer may
                 // overwrite it once the group's four warps said so (the
@@ -642,13 +663,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (nx.valid) nx.step();
                 }
                 // 4. P = 2^(s - m_new) (bf16) and the group's row sum.
-                float psum = 0.f;
                 uint32_t pk[kBKV / 2];
+                float psum;
+                {
+                    float ps[kBKV / 2];
 #pragma unroll
-                for (int j = 0; j < kBKV / 2; ++j) {
-                    const float a0 = ptx::ex2(s[2 * j] - m_new), a1 = ptx::ex2(s[2 * j + 1] - m_new);
-                    psum += a0 + a1;
-                    pk[j] = ptx::pack_bf16(a0, a1);
+                    for (int j = 0; j < kBKV / 2; ++j) {
+                        const float a0 = ptx::ex2(s[2 * j] - m_new), a1 = ptx::ex2(s[2 * j + 1] - m_new);
+                        ps[j] = a0 + a1;
+                        pk[j] = ptx::pack_bf16(a0, a1);
+                    }
+#pragma unroll
+                    for (int w = kBKV / 4; w >= 3; w /= 2)
+#pragma unroll
+                        for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
+                    psum = (ps[0] + ps[1]) + ps[2];
                 }
                 l_grp = l_grp * ptx::ex2(m_grp - m_new) + psum;
                 m_grp = m_new;
