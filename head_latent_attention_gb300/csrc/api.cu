@@ -630,7 +630,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         t.sc = sc;
         t.scale_log2 = scale_log2;
         t.o_lat = o_lat;
-        t.o_part = (float *)(wsb + L.o_part);
+        t.o_part = (bf16 *)(wsb + L.o_part);
         t.ml_part = (float *)(wsb + L.ml_part);
         t.status = (uint32_t *)ws;
         if (!align_ok(c, {cache->lat, cache->rope}) || (cache->lat_stride * 2) % 16 ||
@@ -649,7 +649,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         t.chunk = sc.chunk;
         t.scale_log2 = scale_log2;
         t.o_lat = o_lat;
-        t.o_part = (float *)(wsb + L.o_part);
+        t.o_part = (bf16 *)(wsb + L.o_part);
         t.ml_part = (float *)(wsb + L.ml_part);
         t.status = (uint32_t *)ws;
         MLA_TRY_CUDA(mlra_tc(t, s));
@@ -678,7 +678,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         FinishArgs f;
         f.B = B; f.H = H; f.r_lat = r_lat; f.d_v = c.d_v;
         f.seq_fc = sc.seq_fc; f.seq_lc = sc.seq_lc;
-        f.o_part = (float *)(wsb + L.o_part);
+        f.o_part = (const bf16 *)(wsb + L.o_part);
         f.ml_part = (float *)(wsb + L.ml_part);
         f.o_lat = o_lat;
         f.W_UV = w->W_UV;
@@ -688,7 +688,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         return MLA_OK;
     }
     if (tc_split) {
-        decode_combine(sc, B, H, r_lat, (float *)(wsb + L.o_part), (float *)(wsb + L.ml_part), o_lat, s);
+        decode_combine(sc, B, H, r_lat, (const bf16 *)(wsb + L.o_part), (float *)(wsb + L.ml_part), o_lat, s);
         MLA_TRY_CUDA(cudaGetLastError());
     }
 

@@ -33,7 +33,7 @@
 // range per cluster (a device-side scheduler computes the prefix sums of the
 // lengths); a range splits into one segment per sequence it touches.  A
 // segment that covers a whole sequence writes o_lat directly; others write
-// (O, m, l) partials that a combine kernel merges.
+// their normalised latent average (bf16) with its (m, l), merged later.
 #include "mla_internal.cuh"
 #include "ptx.cuh"
 
@@ -106,7 +106,7 @@ struct DecTcParams {
     DecodeSched sc;     // prefix sums, range starts, first sequence of each range
     float scale_log2;
     bf16 *o_lat;        // [B, H, r_kv]
-    float *o_part;      // [slots, H, r_kv]
+    bf16 *o_part;       // [slots, H, r_kv]
     float *ml_part;     // [slots, H, 2]
     uint32_t *status;
 };
@@ -741,51 +741,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ptx::mbar_wait(&bar->pv_done[gl & 1], (gl >> 1) & 1, abort_flag)) { fail(); break; }
             ptx::tc_fence_after();
             const int slot = cid + b;
-            // Each warp stages 32 rows x 64 bytes at a time in its own block
-            // of its group's P buffer (free: every P.V of the segment has
-            // completed, and the warp's last copy to the peer has read it), so the
-            // global stores go out as 64-byte row pieces: fp32 partials 16
-            // columns per chunk, bf16 outputs 32.  The 16-byte pieces of a
-            // row are rotated by (row / 2) % 4 against bank conflicts.
+            // The normalised latent average in bfloat16, to o_lat for a whole
+            // sequence or to the range's partial slot.  Each warp stages 32
+            // rows x 64 bytes at a time in its own block of its group's P
+            // buffer (free: every P.V of the segment has completed, and the
+            // warp's last copy to the peer has read it), so the global stores
+            // go out as 64-byte row pieces; the 16-byte pieces of a row are
+            // rotated by (row / 2) % 4 against bank conflicts.  Two 32-column
+            // chunks are read from tensor memory per wait.
             uint8_t *wst = smem + kOffP + grp * kPBytes + xblk;
             if (lane == 0) bulk_wait_read();
             __syncwarp();
             const int rd_row = lane >> 2, rd_piece = lane & 3;
-            const int ncols = whole ? 32 : 16;
+            bf16 *dst_base = whole ? p.o_lat + (int64_t)b * p.H * kRLat : p.o_part + (int64_t)slot * p.H * kRLat;
+            const float inv = 1.f / l_tot;
 #pragma unroll 1
-            for (int c = grp * (kOCols / 2); c < (grp + 1) * (kOCols / 2); c += ncols) {
-                uint32_t w[16];
-                if (whole) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32(tmem + lane_off + c, o);
-                    ptx::tmem_ld_wait();
-                    const float inv = 1.f / l_tot;
+            for (int c2 = grp * (kOCols / 2); c2 < (grp + 1) * (kOCols / 2); c2 += 64) {
+                uint32_t o[2][32];
+                ptx::tmem_ld32(tmem + lane_off + c2, o[0]);
+                ptx::tmem_ld32(tmem + lane_off + c2 + 32, o[1]);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int c = c2 + 32 * half;
+                    uint32_t w[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        w[j] = ptx::pack_bf16(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-                } else {
-                    ptx::tmem_ld16(tmem + lane_off + c, w);
-                    ptx::tmem_ld_wait();
-                }
+                        w[j] = ptx::pack_bf16(__uint_as_float(o[half][2 * j]) * inv,
+                                              __uint_as_float(o[half][2 * j + 1]) * inv);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint4 *>(wst + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
-                        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                __syncwarp();
+                    for (int i = 0; i < 4; ++i)
+                        *reinterpret_cast<uint4 *>(wst + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
+                            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    __syncwarp();
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = rd_row + 8 * k;               // row within the warp
-                    const int hr = quad * 32 + r;               // head
-                    const uint4 v = *reinterpret_cast<const uint4 *>(wst + r * 64 + ((rd_piece ^ ((r >> 1) & 3)) * 16));
-                    if (hr < p.H) {
-                        const int col = (int)rank * kOCols + c;
-                        if (whole)
-                            *reinterpret_cast<uint4 *>(p.o_lat + ((int64_t)b * p.H + hr) * kRLat + col + rd_piece * 8) = v;
-                        else
-                            *reinterpret_cast<uint4 *>(p.o_part + ((int64_t)slot * p.H + hr) * kRLat + col + rd_piece * 4) = v;
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = rd_row + 8 * k;  // row within the warp
+                        const int hr = quad * 32 + r;  // head
+                        const uint4 v =
+                            *reinterpret_cast<const uint4 *>(wst + r * 64 + ((rd_piece ^ ((r >> 1) & 3)) * 16));
+                        if (hr < p.H)
+                            *reinterpret_cast<uint4 *>(dst_base + (int64_t)hr * kRLat + (int)rank * kOCols + c +
+                                                       rd_piece * 8) = v;
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
             }
             const bool row_ok = h < p.H;
             if (row_ok && !whole && rank == 0 && grp == 0) {
@@ -915,11 +915,12 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
     }
 }
 
-// o_lat[b, h] = sum_s 2^(m_s - m*) O_s / sum_s 2^(m_s - m*) l_s over the
-// partial slots of sequence b (sequences handled by one cluster were written
-// directly; invalid ones are zeroed).
+// o_lat[b, h] = sum_s w_s O_s / sum_s w_s, w_s = 2^(m_s - m*) l_s, over the
+// partial slots of sequence b (O_s normalised by its own row sum l_s;
+// sequences handled by one range were written directly; invalid ones are
+// zeroed).
 __global__ void __launch_bounds__(128) decode_combine_tc_kernel(DecodeSched sc, int B, int H, int r_lat,
-                                                                const float *o_part, const float *ml_part,
+                                                                const bf16 *o_part, const float *ml_part,
                                                                 bf16 *o_lat)
 {
     ptx::pdl_trigger();
@@ -943,8 +944,8 @@ __global__ void __launch_bounds__(128) decode_combine_tc_kernel(DecodeSched sc, 
     for (int col = threadIdx.x; col < r_lat; col += blockDim.x) {
         float acc = 0.f;
         for (int c = fc; c <= lc; ++c) {
-            const float w = exp2f(ml_part[((int64_t)(c + b) * H + h) * 2] - m);
-            acc += w * o_part[((int64_t)(c + b) * H + h) * r_lat + col];
+            const float *ml = ml_part + ((int64_t)(c + b) * H + h) * 2;
+            acc += exp2f(ml[0] - m) * ml[1] * __bfloat162float(o_part[((int64_t)(c + b) * H + h) * r_lat + col]);
         }
         dst[col] = __float2bfloat16_rn(acc * inv);
     }
@@ -1000,7 +1001,7 @@ void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, 
     note_launch();
 }
 
-void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const float *o_part, const float *ml_part,
+void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const bf16 *o_part, const float *ml_part,
                     void *o_lat, cudaStream_t s)
 {
     launch_ex(decode_combine_tc_kernel, dim3(H, B), dim3(128), 0, s, 1, sc, B, H, r_lat, o_part, ml_part,

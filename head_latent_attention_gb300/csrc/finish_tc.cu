@@ -44,8 +44,8 @@ struct FinParams {
     const int *seq_fc;     // [B] first range covering each sequence (-1: empty)
     const int *seq_lc;     // [B] last range covering each sequence
     int B, H;
-    const float *o_part;   // [(ranges + B), H, R] unnormalised partial averages
-    const float *ml_part;  // [(ranges + B), H, 2] (max in log2 units, denominator)
+    const bf16 *o_part;    // [(ranges + B), H, R] normalised partial averages
+    const float *ml_part;  // [(ranges + B), H, 2] (max in log2 units, row sum)
     const bf16 *o_lat;     // [B, H, R] written directly for single-range sequences
     bf16 *o;               // [B, H, 128]
     uint32_t *status;
@@ -86,33 +86,37 @@ __device__ __forceinline__ void merged_row(const FinParams &p, int b, int h, int
     float acc[CPL];
 #pragma unroll
     for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
-    // Four ranges per pass, their loads issued before the sums.
+    // Four ranges per pass, their loads issued before the sums.  Range c's
+    // average O_c (normalised by its row sum l_c) weighs 2^(m_c - m) l_c.
     for (int c0 = fc; c0 <= lc; c0 += 4) {
-        float4 v[4][CPL / 4];
+        uint4 v[4][CPL / 8];
         float wgt[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int c = c0 + u;
             if (c <= lc) {
                 const int64_t slot = (int64_t)(c + b) * p.H + h;
-                const float4 *src = reinterpret_cast<const float4 *>(p.o_part + slot * R + lane * CPL);
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.o_part + slot * R + lane * CPL);
 #pragma unroll
-                for (int j = 0; j < CPL / 4; ++j) v[u][j] = __ldcs(src + j);
-                wgt[u] = exp2f(p.ml_part[slot * 2] - m);
+                for (int j = 0; j < CPL / 8; ++j) v[u][j] = __ldcs(src + j);
+                const float2 ml = *reinterpret_cast<const float2 *>(p.ml_part + slot * 2);
+                wgt[u] = exp2f(ml.x - m) * ml.y;
             } else {
 #pragma unroll
-                for (int j = 0; j < CPL / 4; ++j) v[u][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < CPL / 8; ++j) v[u][j] = make_uint4(0, 0, 0, 0);
                 wgt[u] = 0.f;
             }
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int j = 0; j < CPL / 4; ++j) {
-                acc[4 * j] += wgt[u] * v[u][j].x;
-                acc[4 * j + 1] += wgt[u] * v[u][j].y;
-                acc[4 * j + 2] += wgt[u] * v[u][j].z;
-                acc[4 * j + 3] += wgt[u] * v[u][j].w;
+            for (int j = 0; j < CPL / 8; ++j) {
+                const uint32_t wd[4] = {v[u][j].x, v[u][j].y, v[u][j].z, v[u][j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[8 * j + 2 * q] += wgt[u] * __uint_as_float(wd[q] << 16);
+                    acc[8 * j + 2 * q + 1] += wgt[u] * __uint_as_float(wd[q] & 0xffff0000u);
+                }
             }
     }
     const float inv = 1.f / den;

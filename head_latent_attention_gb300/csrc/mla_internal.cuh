@@ -196,7 +196,10 @@ cudaError_t decode_simt(const DecodeArgs &a, cudaStream_t s);
 // concatenation of all sequences' keys is cut into n contiguous ranges, one
 // per CTA or cluster; a range splits into one segment per sequence it
 // touches, and the partial result of range c for sequence b goes to slot
-// c + b (unique, since ranges and sequences both advance monotonically).
+// c + b (unique, since ranges and sequences both advance monotonically):
+// the latent average over the segment's keys, normalised by its own row sum
+// and rounded to bfloat16 like a whole sequence's result, with its reference
+// max (log2 units) and row sum in fp32.
 struct DecodeSched {
     int *prefix;       // [B + 1] prefix sums of the valid lengths (invalid ones count 0)
     int *chunk;        // [1] keys per range of the uniform split
@@ -219,7 +222,7 @@ struct DecodeTcArgs {
     DecodeSched sc;           // written by decode_schedule (n = n_clusters)
     float scale_log2;
     void *o_lat;              // [B, H, r_kv] bf16
-    float *o_part;            // [n_clusters + B, H, r_kv]
+    bf16 *o_part;             // [n_clusters + B, H, r_kv] normalised partial averages
     float *ml_part;           // [n_clusters + B, H, 2]
     uint32_t *status;
 };
@@ -237,7 +240,7 @@ DecodeSched decode_sched_at(void *base, int B, int n);
 void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int seg_cost, const DecodeSched &sc,
                      uint32_t *status, cudaStream_t s);
 // Log-sum-exp merge of the partials of split sequences into o_lat.
-void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const float *o_part, const float *ml_part,
+void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const bf16 *o_part, const float *ml_part,
                     void *o_lat, cudaStream_t s);
 
 // Absorbed decode queries (absorb_tc.cu): q_abs[b, h] = W_UK,h^T q_nope[b, h]
@@ -262,7 +265,8 @@ cudaError_t absorb(const AbsorbArgs &a, cudaStream_t s);
 struct FinishArgs {
     int B, H, r_lat, d_v;
     const int *seq_fc, *seq_lc;  // ranges covering each sequence (DecodeSched)
-    const float *o_part, *ml_part;
+    const bf16 *o_part;  // [slots, H, r_lat] normalised partial averages
+    const float *ml_part;  // [slots, H, 2] (max in log2 units, row sum)
     const void *o_lat;  // [B, H, r_lat] (single-range sequences)
     const void *W_UV;
     void *o;            // [B, H, d_v]
@@ -282,7 +286,7 @@ struct MlraTcArgs {
     int *prefix, *chunk;  // workspace: [B + 1], [1]
     float scale_log2;
     void *o_lat;          // [B, H, 256]
-    float *o_part;        // [(n_ctas + B), H, 256]
+    bf16 *o_part;         // [(n_ctas + B), H, 256] normalised partial averages
     float *ml_part;       // [(n_ctas + B), H, 2]
     uint32_t *status;
 };

@@ -63,7 +63,7 @@ struct MlraParams {
     const int *chunk;
     float scale_log2;
     bf16 *o_lat;     // [B, H, 256]
-    float *o_part;   // [slots, H, 256]
+    bf16 *o_part;    // [slots, H, 256] normalised partial averages
     float *ml_part;  // [slots, H, 2]
     uint32_t *status;
 };
@@ -460,10 +460,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int col = mt * 128 + j;
                 for (int h = 0; h < hpb; ++h) {
                     const int head = blk * hpb + h;
-                    if (whole)
-                        p.o_lat[((int64_t)b * p.H + head) * kR + col] = __float2bfloat16_rn(__uint_as_float(o[h]) / lsum[h]);
-                    else
-                        p.o_part[((int64_t)slot * p.H + head) * kR + col] = __uint_as_float(o[h]);
+                    bf16 *dst = whole ? p.o_lat + ((int64_t)b * p.H + head) * kR
+                                      : p.o_part + ((int64_t)slot * p.H + head) * kR;
+                    dst[col] = __float2bfloat16_rn(__uint_as_float(o[h]) / lsum[h]);
                 }
             }
             if (!whole && j < hpb) {
