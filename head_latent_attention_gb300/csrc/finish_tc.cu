@@ -51,77 +51,112 @@ struct FinParams {
     uint32_t *status;
 };
 
-// Latent average of sequence b, head h, columns [lane * CPL, lane * CPL + CPL)
-// (CPL = R / 32), as bfloat16 pairs.
+// Loads of up to four partial slots of one sequence (ranges c0 .. c0 + 3,
+// clipped at lc): this lane's CPL columns of each normalised average and the
+// slots' (max, row sum).
 template <int R>
-__device__ __forceinline__ void merged_row(const FinParams &p, int b, int h, int lane, uint32_t (&out)[R / 64])
+struct SlotGroup {
+    uint4 v[4][R / 256];
+    float2 ml[4];
+};
+
+template <int R>
+__device__ __forceinline__ void load_group(const FinParams &p, int b, int h, int lane, int c0, int lc,
+                                           SlotGroup<R> &g)
 {
     constexpr int CPL = R / 32;
 #pragma unroll
-    for (int i = 0; i < CPL / 2; ++i) out[i] = 0u;
-    if (b >= p.B) return;
-    const int fc = p.seq_fc[b], lc = p.seq_lc[b];
-    if (fc < 0) return;  // empty or invalid length: zero output
-    if (fc == lc) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.o_lat + ((int64_t)b * p.H + h) * R + lane * CPL);
+    for (int u = 0; u < 4; ++u) {
+        const int c = c0 + u;
+        if (c <= lc) {
+            const int64_t slot = (int64_t)(c + b) * p.H + h;
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.o_part + slot * R + lane * CPL);
 #pragma unroll
-        for (int i = 0; i < CPL / 8; ++i) {
-            const uint4 v = src[i];
-            out[4 * i] = v.x; out[4 * i + 1] = v.y; out[4 * i + 2] = v.z; out[4 * i + 3] = v.w;
+            for (int j = 0; j < CPL / 8; ++j) g.v[u][j] = __ldcs(src + j);
+            g.ml[u] = *reinterpret_cast<const float2 *>(p.ml_part + slot * 2);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CPL / 8; ++j) g.v[u][j] = make_uint4(0, 0, 0, 0);
+            g.ml[u] = make_float2(-INFINITY, 0.f);
         }
-        return;
     }
-    // Reference max and denominator over the ranges, lanes in parallel.
-    float m = -INFINITY;
-    for (int c = fc + lane; c <= lc; c += 32) m = fmaxf(m, p.ml_part[((int64_t)(c + b) * p.H + h) * 2]);
+}
+
+// Online merge of a group into (m, den, acc): slot c's average O_c
+// (normalised by its row sum l_c) weighs 2^(m_c - m) l_c.
+template <int R>
+__device__ __forceinline__ void merge_group(const SlotGroup<R> &g, float &m, float &den, float (&acc)[R / 32])
+{
+    constexpr int CPL = R / 32;
+    const float mg = fmaxf(fmaxf(g.ml[0].x, g.ml[1].x), fmaxf(g.ml[2].x, g.ml[3].x));
+    const float m_new = fmaxf(m, mg);
+    const float sc = exp2f(m - m_new);  // 0 on the first group (m = -inf)
+    den *= sc;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    float den = 0.f;
-    for (int c = fc + lane; c <= lc; c += 32) {
-        const float2 ml = *reinterpret_cast<const float2 *>(p.ml_part + ((int64_t)(c + b) * p.H + h) * 2);
-        den += exp2f(ml.x - m) * ml.y;
-    }
+    for (int i = 0; i < CPL; ++i) acc[i] *= sc;
 #pragma unroll
-    for (int off = 16; off; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-    float acc[CPL];
+    for (int u = 0; u < 4; ++u) {
+        const float w = g.ml[u].y == 0.f ? 0.f : exp2f(g.ml[u].x - m_new) * g.ml[u].y;
+        den += w;
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
-    // Four ranges per pass, their loads issued before the sums.  Range c's
-    // average O_c (normalised by its row sum l_c) weighs 2^(m_c - m) l_c.
-    for (int c0 = fc; c0 <= lc; c0 += 4) {
-        uint4 v[4][CPL / 8];
-        float wgt[4];
+        for (int j = 0; j < CPL / 8; ++j) {
+            const uint32_t wd[4] = {g.v[u][j].x, g.v[u][j].y, g.v[u][j].z, g.v[u][j].w};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int c = c0 + u;
-            if (c <= lc) {
-                const int64_t slot = (int64_t)(c + b) * p.H + h;
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.o_part + slot * R + lane * CPL);
-#pragma unroll
-                for (int j = 0; j < CPL / 8; ++j) v[u][j] = __ldcs(src + j);
-                const float2 ml = *reinterpret_cast<const float2 *>(p.ml_part + slot * 2);
-                wgt[u] = exp2f(ml.x - m) * ml.y;
-            } else {
-#pragma unroll
-                for (int j = 0; j < CPL / 8; ++j) v[u][j] = make_uint4(0, 0, 0, 0);
-                wgt[u] = 0.f;
+            for (int q = 0; q < 4; ++q) {
+                acc[8 * j + 2 * q] += w * __uint_as_float(wd[q] << 16);
+                acc[8 * j + 2 * q + 1] += w * __uint_as_float(wd[q] & 0xffff0000u);
             }
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int j = 0; j < CPL / 8; ++j) {
-                const uint32_t wd[4] = {v[u][j].x, v[u][j].y, v[u][j].z, v[u][j].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[8 * j + 2 * q] += wgt[u] * __uint_as_float(wd[q] << 16);
-                    acc[8 * j + 2 * q + 1] += wgt[u] * __uint_as_float(wd[q] & 0xffff0000u);
-                }
-            }
     }
-    const float inv = 1.f / den;
+    m = m_new;
+}
+
+// Latent averages of sequences b and b + 1 (ranges fc[u] .. lc[u]), head h,
+// columns [lane * CPL, lane * CPL + CPL) (CPL = R / 32), as bfloat16 pairs.
+// The loads of both sequences go out before either is merged.
+template <int R>
+__device__ __forceinline__ void merged_pair(const FinParams &p, int b, const int (&fc)[2], const int (&lc)[2], int h,
+                                           int lane, uint32_t (&out)[2][R / 64])
+{
+    constexpr int CPL = R / 32;
+    SlotGroup<R> g[2];
+    uint4 direct[2][CPL / 8];
 #pragma unroll
-    for (int i = 0; i < CPL / 2; ++i) out[i] = ptx::pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    for (int u = 0; u < 2; ++u) {
+        if (fc[u] >= 0 && fc[u] == lc[u]) {
+            const uint4 *src =
+                reinterpret_cast<const uint4 *>(p.o_lat + ((int64_t)(b + u) * p.H + h) * R + lane * CPL);
+#pragma unroll
+            for (int i = 0; i < CPL / 8; ++i) direct[u][i] = src[i];
+        } else if (fc[u] >= 0) {
+            load_group<R>(p, b + u, h, lane, fc[u], lc[u], g[u]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+        for (int i = 0; i < CPL / 2; ++i) out[u][i] = 0u;
+        if (fc[u] < 0) continue;  // empty or invalid length (or past the batch): zero
+        if (fc[u] == lc[u]) {
+#pragma unroll
+            for (int i = 0; i < CPL / 8; ++i) {
+                out[u][4 * i] = direct[u][i].x; out[u][4 * i + 1] = direct[u][i].y;
+                out[u][4 * i + 2] = direct[u][i].z; out[u][4 * i + 3] = direct[u][i].w;
+            }
+            continue;
+        }
+        float m = -INFINITY, den = 0.f, acc[CPL];
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) acc[i] = 0.f;
+        merge_group<R>(g[u], m, den, acc);
+        for (int c0 = fc[u] + 4; c0 <= lc[u]; c0 += 4) {  // more than four ranges: rare
+            load_group<R>(p, b + u, h, lane, c0, lc[u], g[u]);
+            merge_group<R>(g[u], m, den, acc);
+        }
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int i = 0; i < CPL / 2; ++i) out[u][i] = ptx::pack_bf16(acc[2 * i] * inv, acc[2 * i + 1] * inv);
+    }
 }
 
 template <int R>
@@ -166,17 +201,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_finish_kernel(const __grid
     }
 
     ptx::pdl_wait();
-    // 2. Merged latent averages of the group's sequences, one per warp pass.
-    for (int t = warp; t < kTok; t += kThreads / 32) {
-        uint32_t v[R / 64];
-        merged_row<R>(p, b0 + t, h, lane, v);
-        // Columns [lane * CPL, +CPL) are CPL / 8 chunks of 16 bytes; chunk g
-        // sits in 64-column block g / 8, at position (g % 8) ^ (t % 8) of row t.
+    // 2. Merged latent averages of the group's sequences: warp w takes
+    //    sequences 8 w .. 8 w + 7, whose covering ranges its first lanes load
+    //    in one round trip, then merges them two at a time.
+    {
+        constexpr int kPerWarp = kTok / (kThreads / 32);
+        int fcv = -1, lcv = -1;
+        if (lane < kPerWarp && b0 + warp * kPerWarp + lane < p.B) {
+            fcv = p.seq_fc[b0 + warp * kPerWarp + lane];
+            lcv = p.seq_lc[b0 + warp * kPerWarp + lane];
+        }
+#pragma unroll 1
+        for (int i = 0; i < kPerWarp; i += 2) {
+            const int t = warp * kPerWarp + i;
+            int fc[2], lc[2];
 #pragma unroll
-        for (int i = 0; i < CPL / 8; ++i) {
-            const int g = lane * (CPL / 8) + i;
-            uint8_t *dst = sO + (g >> 3) * kOBlk + t * 128 + (((g & 7) ^ (t & 7)) << 4);
-            *reinterpret_cast<uint4 *>(dst) = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int u = 0; u < 2; ++u) {
+                fc[u] = __shfl_sync(0xffffffffu, fcv, i + u);
+                lc[u] = __shfl_sync(0xffffffffu, lcv, i + u);
+            }
+            uint32_t v[2][R / 64];
+            merged_pair<R>(p, b0 + t, fc, lc, h, lane, v);
+            // Columns [lane * CPL, +CPL) are CPL / 8 chunks of 16 bytes; chunk
+            // g sits in 64-column block g / 8, at position (g % 8) ^ (row % 8)
+            // of the row.
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int k = 0; k < CPL / 8; ++k) {
+                    const int g = lane * (CPL / 8) + k, row = t + u;
+                    uint8_t *dst = sO + (g >> 3) * kOBlk + row * 128 + (((g & 7) ^ (row & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) =
+                        make_uint4(v[u][4 * k], v[u][4 * k + 1], v[u][4 * k + 2], v[u][4 * k + 3]);
+                }
         }
     }
     ptx::fence_proxy_async_smem();  // generic-proxy stores -> tensor-core reads
