@@ -400,3 +400,75 @@ def test_edge_cases(mla, oracle_mod):
     qq = torch.zeros(2, ws_.n_heads, ws_.d_nope, dtype=dt, device="cuda")
     oo = torch.empty_like(qq)
     assert mla.mla_decode(lay2.h, lay2.w, qq, None, lay2.cache, sl[:2], 2, oo, lay2.ws) == 2
+
+
+# ---------------------------------------------------------------------------
+# Decode batches that stress the split-KV schedule and the merge
+# ---------------------------------------------------------------------------
+
+def decode_mixed(mla, oracle_mod, w, lens, max_seq, check_b):
+    """Decode a batch whose lengths may be invalid (< 1 or > max_seq): valid
+    sequences in check_b match the oracle, invalid ones come out zero and the
+    length flag is raised."""
+    B = len(lens)
+    dev_w, ex_w = weights_of(w)
+    lay = make_layer(mla, w, dev_w, B, max_batch=B, max_seq=max_seq, ws_max_len=0)
+    H = w.n_heads
+    qs, qe = syn.stage_inputs(w, "q_nope", (B, H, w.d_nope))
+    rs, re_ = syn.stage_inputs(w, "q_rope", (B, H, w.d_rope))
+    lat_h = np.zeros((B, max_seq, w.r_kv), np.uint16)
+    rope_h = np.zeros((B, max_seq, w.d_rope), np.uint16)
+    lat_e, rope_e = {}, {}
+    for b in range(B):
+        L = int(lens[b])
+        if 1 <= L <= max_seq:
+            ls, le = syn.cache_rows(w, b, L)
+            rs2, re2 = syn.cache_rows(w, b, L, "cache_rope")
+            lat_h[b, :L] = ls
+            rope_h[b, :L] = rs2
+            if b in check_b:
+                lat_e[b], rope_e[b] = le, re2
+    lay.cache_lat.copy_(to_dev(lat_h).view(lay.cache_lat.shape))
+    lay.cache_rope.copy_(to_dev(rope_h).view(lay.cache_rope.shape))
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    lay.device_status()
+    o = lay.decode(to_dev(qs), to_dev(rs), sl)
+    torch.cuda.synchronize()
+    st, bits = lay.device_status()
+    invalid = [b for b in range(B) if not 1 <= lens[b] <= max_seq]
+    if invalid:
+        assert st == mla.MLA_ERR_DEVICE_DATA and bits == 4, (st, bits)
+    else:
+        assert st == 0 and bits == 0
+    got = to_f64(o)
+    for b in invalid:
+        assert np.all(got[b] == 0.0), f"invalid length at b={b} must give a zero output"
+    for b in check_b:
+        L = int(lens[b])
+        if not 1 <= L <= max_seq:
+            continue
+        q = {"q_nope": qe[b:b + 1], "q_rope": re_[b:b + 1]}
+        ref = oracle_mod.attend(w, [0], [L - 1], q, lat_e[b][None], rope_e[b][None], ex_w, absorbed=True)
+        compare(got[b:b + 1], ref, w.dtype, f"decode b={b} L={L}")
+
+
+def test_decode_mixed_batch(mla, oracle_mod):
+    # 70 sequences: two groups of 64 in the absorption and merge kernels, the
+    # second ragged; invalid lengths (0 and max_seq + 1) between valid ones,
+    # one sequence of the full max_seq, several of one key.
+    w = W["dsv2_decode"].replace(n_heads=16)
+    rng = np.random.default_rng(7)
+    lens = [int(v) for v in rng.integers(1, 301, 70)]
+    lens[5], lens[33], lens[69], lens[2], lens[64] = 0, 301, 300, 1, 1
+    decode_mixed(mla, oracle_mod, w, lens, 300, check_b=[0, 2, 5, 33, 40, 63, 64, 65, 69])
+
+
+def test_decode_many_short_sequences(mla, oracle_mod):
+    # Thousands of 1..3-key sequences: every work range holds more sequences
+    # than the kernel's shared-memory window of prefix sums, and the merge
+    # runs over many groups of 64.
+    w = W["dsv2_decode"].replace(n_heads=8)
+    rng = np.random.default_rng(11)
+    B = 6000
+    lens = [int(v) for v in rng.integers(1, 4, B)]
+    decode_mixed(mla, oracle_mod, w, lens, 4, check_b=[0, 1, 63, 64, 2999, 4095, 5998, 5999])
