@@ -43,6 +43,13 @@
  *    workspace status word, read with mla_get_device_status().
  *  - A handle is immutable after mla_create(); calls on different streams
  *    are safe when their output buffers and workspaces differ.
+ *  - The tensor-core kernels are launched with programmatic dependent launch
+ *    (each may start while the previous kernel on the stream finishes and
+ *    waits for it before touching its results); setting the environment
+ *    variable MLA_PDL=0 before the first call launches them in plain stream
+ *    order.  Calls are captured into CUDA graphs as they are.
+ *  - After MLA_ERR_TIMEOUT the workspace should be zero-filled again before
+ *    reuse: an interrupted call can leave scratch state behind.
  */
 #ifndef MLA_GB300_H
 #define MLA_GB300_H
@@ -177,7 +184,10 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope,
  * MLA_ERR_UNSUPPORTED (RoPE sits between W_UK and the query, so there is no
  * absorbed form).  q_nope [B, H, d_nope], q_rope [B, H, d_rope] or NULL,
  * o [B, H, d_v]; seq_lens: DEVICE int32 [B], each in [1, max_seq] (others
- * skipped and flagged).  B <= max_batch. */
+ * are skipped, their output rows are zero, and the length bit is set in the
+ * workspace status word).  B <= max_batch.  bfloat16 MLA/MLRA run on the
+ * tensor cores: a scheduler kernel, the absorption, the split-KV attention
+ * and one kernel that merges split sequences and applies W_UV. */
 mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope,
                       const void *q_rope, const mla_cache *cache,
                       const int32_t *seq_lens, int B, void *o, void *ws,
