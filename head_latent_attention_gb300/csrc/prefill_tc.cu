@@ -289,22 +289,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s[32 + j] = (32 + j <= lim) ? __uint_as_float(r1[j]) : -INFINITY;
                 }
             }
+            {
+                // Balanced trees (short dependency chains) for the row max.
+                float t[32];
 #pragma unroll
-            for (int j = 0; j < 64; ++j) mt = fmaxf(mt, s[j]);
+                for (int j = 0; j < 32; ++j) t[j] = fmaxf(s[j], s[32 + j]);
+#pragma unroll
+                for (int w = 16; w >= 1; w /= 2)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+                mt = t[0];
+            }
             mt *= p.scale_log2;
             const bool resc = mt > m_run + kRescaleThreshold;
             const float m_new = resc ? mt : m_run;
             // Rows past the sequence end see no key; keep their state finite.
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
             const float corr = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - m_use);
-            float psum = 0.f;
+            float psum;
             uint32_t pk[32];
+            {
+                float ps[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float a0 = ptx::ex2(fmaf(s[2 * j], p.scale_log2, -m_use));
-                const float a1 = ptx::ex2(fmaf(s[2 * j + 1], p.scale_log2, -m_use));
-                psum += a0 + a1;
-                pk[j] = ptx::pack_f16(a0, a1);
+                for (int j = 0; j < 32; ++j) {
+                    const float a0 = ptx::ex2(fmaf(s[2 * j], p.scale_log2, -m_use));
+                    const float a1 = ptx::ex2(fmaf(s[2 * j + 1], p.scale_log2, -m_use));
+                    ps[j] = a0 + a1;
+                    pk[j] = ptx::pack_f16(a0, a1);
+                }
+#pragma unroll
+                for (int w = 16; w >= 1; w /= 2)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
+                psum = ps[0];
             }
             l_run = l_run * corr + psum;
             m_run = m_new;
