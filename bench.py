@@ -44,6 +44,25 @@ L2_FLUSH_BYTES = 512 << 20
 DECODE_TRAFFIC_BYTES = 217196032  # 213,539,840 read + 3,656,192 written
 
 
+def max_over_ranks(vals, world: int, device):
+    """Element-wise maximum of per-rank timings, returned on every rank (the
+    job is as slow as its slowest rank)."""
+    vals = [float(v) for v in vals]
+    if world <= 1:
+        return vals
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(world: int, units_per_rank: float, ms: float) -> float:
+    """Whole-job throughput: every rank processes units_per_rank in ms (weak
+    scaling), so the job processes world times that."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -302,12 +321,9 @@ def run_ours(args, rank, world, device):
     clocks = sampler.summary()
 
     nbytes = decode_bytes(lens)
-    if world > 1:
-        t = torch.tensor([ms, e2e_ms, kms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms, kms = t.tolist()
-    value = world * nbytes / (ms * 1e-3) / 1e9
-    e2e_val = world * nbytes / (e2e_ms * 1e-3) / 1e9
+    ms, e2e_ms, kms = max_over_ranks([ms, e2e_ms, kms], world, device)
+    value = job_rate(world, nbytes, ms) / 1e9
+    e2e_val = job_rate(world, nbytes, e2e_ms) / 1e9
     achieved = nbytes / (kms * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,

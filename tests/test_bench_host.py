@@ -1,0 +1,73 @@
+"""Host-side logic of bench.py for N > 1 ranks, on CPU: the timings are
+reduced to the slowest rank over a gloo process group of two ranks, the
+whole-job rate counts every rank's work, and only rank 0 of the reference arm
+prints."""
+from __future__ import annotations
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # Rank r measured (step, e2e, kernel) times; rank 1 is the slower one
+        # in the first two, rank 0 in the third.
+        mine = [1.0 + rank, 2.0 + 3 * rank, 5.0 - rank]
+        q.put((rank, bench.max_over_ranks(mine, world, "cpu")))
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    assert got[0] == got[1] == [2.0, 5.0, 5.0]
+
+
+def test_max_over_ranks_single_rank_is_identity():
+    assert bench.max_over_ranks([1, 2.5], 1, "cpu") == [1.0, 2.5]
+
+
+def test_job_rate_counts_every_rank():
+    # 188.7 MB per rank in 0.2 ms: 0.9435 TB/s per rank, 4 ranks -> 3.774 TB/s.
+    assert bench.job_rate(4, 188.7e6, 0.2) == pytest.approx(4 * 188.7e6 / 0.2e-3)
+    assert bench.job_rate(1, 10.0, 1000.0) == pytest.approx(10.0)
+
+
+def test_reference_arm_other_ranks_exit_silently():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
