@@ -340,6 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_st32(tmem + lane_off + q * C::kOCol + c, o);
                 }
             }
+            // Key rows at or past the sequence's end (sp + S) may hold
+            // arbitrary contents of unwritten cache rows; their P is 0, but
+            // 0 * NaN is not 0: zero those rows of the V tile (both query
+            // tiles write the same zeros before their own P.V).
+            const int v0 = sp + p.S - t * kBN;
+            if (v0 < kBN) {
+                uint8_t *vt = sKV + (t % kStages) * C::kStageBytes + NQ * C::kAtom;
+                const int r0 = max(v0, 0), nrow = kBN - r0;
+                for (int i = r; i < NV * nrow * 8; i += kQ) {
+                    const int a = i / (nrow * 8), rr = (i / 8) % nrow, ch = i % 8;
+                    *reinterpret_cast<uint4 *>(vt + a * C::kAtom + (r0 + rr) * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+                }
+                ptx::fence_proxy_async_smem();
+            }
             ptx::tmem_st32(tmem + lane_off + sbuf, pk);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();

@@ -69,9 +69,14 @@ def make_layer(mla, w, dev_w, max_tokens, max_batch=None, max_seq=None, ws_max_l
 # End-to-end prefill: x -> project_latent -> prefill -> out_proj
 # ---------------------------------------------------------------------------
 
-def run_prefill_e2e(mla, oracle_mod, w, B, S, start_pos=None):
+def run_prefill_e2e(mla, oracle_mod, w, B, S, start_pos=None, poison=False):
     dev_w, ex_w = weights_of(w)
     lay = make_layer(mla, w, dev_w, B * S, max_batch=B, max_seq=max(w.seq, S + max(start_pos or [0])))
+    if poison:
+        # Cache rows nobody writes hold NaN: they must not reach any output.
+        lay.cache_lat.fill_(float("nan"))
+        if w.d_rope:
+            lay.cache_rope.fill_(float("nan"))
     xs, xe = syn.activations(w, B * S)
     sp = np.zeros(B, np.int32) if start_pos is None else np.asarray(start_pos, np.int32)
     pos = (sp[:, None] + np.arange(S)[None, :]).reshape(-1).astype(np.int32)
@@ -132,6 +137,15 @@ def test_chunked_prefill(mla, oracle_mod):
     # Queries appended after a cached prefix (start_pos > 0), ragged per sequence.
     run_prefill_e2e(mla, oracle_mod, W["dsv2_prefill"].replace(seq=512), 2, 70, start_pos=[37, 200])
     run_prefill_e2e(mla, oracle_mod, W["small_lm_prefill"].replace(seq=512), 2, 45, start_pos=[0, 129])
+
+
+def test_chunked_prefill_unwritten_rows_nan(mla, oracle_mod):
+    # Ragged chunks: the shorter sequence's last key tile reaches past its
+    # written rows, which hold NaN here.
+    run_prefill_e2e(mla, oracle_mod, W["dsv2_prefill"].replace(seq=512), 2, 70, start_pos=[37, 200],
+                    poison=True)
+    run_prefill_e2e(mla, oracle_mod, W["small_lm_prefill"].replace(seq=512), 2, 45, start_pos=[0, 129],
+                    poison=True)
 
 
 def test_mlra_prefill_e2e(mla, oracle_mod):
