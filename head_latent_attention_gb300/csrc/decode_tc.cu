@@ -9,7 +9,7 @@
 // [256 r, 256 r + 256) and rope columns [32 r, 32 r + 32).  Each CTA
 //   - keeps O (256 columns), its 288 query columns (the A operand of Q K^T)
 //     and two 48-column score buffers in tensor memory;
-//   - streams 48-key tiles of its own cache columns through a 5-stage ring
+//   - streams 48-key tiles of its own cache columns through a 6-stage ring
 //     (TMA; 128-byte swizzle for the latent, 64-byte for rope);
 //   - computes a partial score tile S_r = Q_r K_r^T (M = 128 heads, N = 48
 //     keys, K = 288);
@@ -30,10 +30,13 @@
 // exact either way because P and the row sums use the same reference.
 //
 // Work: the concatenation of all sequences' keys is cut into one contiguous
-// range per cluster (a device-side scheduler computes the prefix sums of the
-// lengths); a range splits into one segment per sequence it touches.  A
-// segment that covers a whole sequence writes o_lat directly; others write
-// their normalised latent average (bf16) with its (m, l), merged later.
+// range per cluster by a device-side scheduler that runs before the kernel
+// preceding this one (ranges balanced by estimated time, a sequence start
+// costing a few hundred keys); a range splits into one segment per sequence
+// it touches.  A segment that covers a whole sequence writes o_lat
+// directly; others write their normalised latent average (bf16) with its
+// (m, l), merged later.  Warp roles: a Q K^T runs at most three tiles ahead
+// of the next P.V, since the tensor pipe executes in order.
 #include "mla_internal.cuh"
 #include "ptx.cuh"
 

@@ -4,8 +4,10 @@
 // deepseek-mla `MultiHeadLatentAttention.forward` (and mlra_attn per latent
 // block) weights the up-projected values W_UV,h c_j by the softmax; by
 // linearity o_h = W_UV,h (sum_j p_hj c_j), so the split-KV kernels attend in
-// latent space and leave, per work range, an unnormalised latent average
-// with its running max and denominator.  This kernel finishes the head:
+// latent space and leave, per work range that covers only part of a
+// sequence, its latent average (normalised by the range's own row sum, in
+// bfloat16) with the range's reference max and row sum.  This kernel
+// finishes the head:
 //
 // One CTA per (head h, group of 64 sequences):
 //   1. TMA copies W_UV,h ([128, r_lat] bfloat16, K-major) into shared memory;
