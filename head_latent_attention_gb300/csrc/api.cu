@@ -416,6 +416,7 @@ size_t mla_workspace_size(const mla_handle *h, int batch, int max_len, int64_t n
     need = std::max(need, project_ws(h, n_tokens).end);
     need = std::max(need, out_proj_ws(h, n_tokens).end);
     if (c.variant != MLA_VARIANT_SMALL) need = std::max(need, decode_ws(h, batch).end);
+    else need = std::max(need, prefill_ws(c, batch, c.max_seq).end);  // decode re-decompresses the cache
     need = std::max(need, prefill_ws(c, batch, max_len).end);
     return need;
 }
@@ -454,35 +455,18 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
     return MLA_OK;
 }
 
-mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
-                       const mla_cache *cache, int B, int S, const int32_t *start_pos, void *o,
-                       void *ws, size_t ws_bytes, void *stream)
+// The prefill computation once the (device) start positions are in the
+// workspace: up-projected keys and values of rows [0, kv_rows) of every
+// sequence, then causal attention of S queries per sequence.
+static mla_status prefill_core(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
+                               const mla_cache *cache, int B, int S, int64_t kv_rows, void *o, void *ws,
+                               cudaStream_t s)
 {
-    if (!h || !w || !cache || B < 0 || S < 0) return MLA_ERR_INVALID_ARG;
-    if (B == 0 || S == 0) return MLA_OK;
     const mla_config &c = h->cfg;
     const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
-    if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
-    if (!q_nope || !o || !ws || !cache->lat || !w->W_UK || !w->W_UV) return MLA_ERR_INVALID_ARG;
-    if (dec && (!q_rope || !cache->rope || cache->rope_stride < c.d_rope)) return MLA_ERR_INVALID_ARG;
-    if (!dec && q_rope) return MLA_ERR_INVALID_ARG;
-    if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
-    if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
-        return MLA_ERR_INVALID_ARG;
-    int64_t kv_rows = 0;
-    for (int b = 0; b < B; ++b) {
-        int sp = start_pos ? start_pos[b] : 0;
-        if (sp < 0) return MLA_ERR_INVALID_ARG;
-        if ((int64_t)sp + S > c.max_seq) return MLA_ERR_CACHE_OVERFLOW;
-        kv_rows = std::max<int64_t>(kv_rows, (int64_t)sp + S);
-    }
     PrefillWs L = prefill_ws(c, B, kv_rows);
-    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
-    cudaStream_t s = (cudaStream_t)stream;
     char *wsb = (char *)ws;
     int32_t *d_sp = (int32_t *)(wsb + L.start_pos);
-    if (start_pos) MLA_TRY_CUDA(cudaMemcpyAsync(d_sp, start_pos, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s));
-    else MLA_TRY_CUDA(cudaMemsetAsync(d_sp, 0, sizeof(int32_t) * B, s));
     void *kbuf = wsb + L.k, *vbuf = wsb + L.v;
     const int H = c.n_heads;
     const int64_t ldk = (int64_t)H * c.d_nope, ldv = (int64_t)H * c.d_v;
@@ -555,14 +539,63 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
     return MLA_OK;
 }
 
+mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
+                       const mla_cache *cache, int B, int S, const int32_t *start_pos, void *o,
+                       void *ws, size_t ws_bytes, void *stream)
+{
+    if (!h || !w || !cache || B < 0 || S < 0) return MLA_ERR_INVALID_ARG;
+    if (B == 0 || S == 0) return MLA_OK;
+    const mla_config &c = h->cfg;
+    const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
+    if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
+    if (!q_nope || !o || !ws || !cache->lat || !w->W_UK || !w->W_UV) return MLA_ERR_INVALID_ARG;
+    if (dec && (!q_rope || !cache->rope || cache->rope_stride < c.d_rope)) return MLA_ERR_INVALID_ARG;
+    if (!dec && q_rope) return MLA_ERR_INVALID_ARG;
+    if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
+    if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
+        return MLA_ERR_INVALID_ARG;
+    int64_t kv_rows = 0;
+    for (int b = 0; b < B; ++b) {
+        int sp = start_pos ? start_pos[b] : 0;
+        if (sp < 0) return MLA_ERR_INVALID_ARG;
+        if ((int64_t)sp + S > c.max_seq) return MLA_ERR_CACHE_OVERFLOW;
+        kv_rows = std::max<int64_t>(kv_rows, (int64_t)sp + S);
+    }
+    PrefillWs L = prefill_ws(c, B, kv_rows);
+    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t *d_sp = (int32_t *)((char *)ws + L.start_pos);
+    if (start_pos) MLA_TRY_CUDA(cudaMemcpyAsync(d_sp, start_pos, sizeof(int32_t) * B, cudaMemcpyHostToDevice, s));
+    else MLA_TRY_CUDA(cudaMemsetAsync(d_sp, 0, sizeof(int32_t) * B, s));
+    return prefill_core(h, w, q_nope, q_rope, cache, B, S, kv_rows, o, ws, s);
+}
+
 mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
                       const mla_cache *cache, const int32_t *seq_lens, int B, void *o, void *ws,
                       size_t ws_bytes, void *stream)
 {
     if (!h || !w || !cache || B < 0) return MLA_ERR_INVALID_ARG;
     const mla_config &c = h->cfg;
-    if (c.variant == MLA_VARIANT_SMALL) return MLA_ERR_UNSUPPORTED;
     if (B == 0) return MLA_OK;
+    if (c.variant == MLA_VARIANT_SMALL) {
+        // mla_attn decodes by re-decompressing the cached latent every step:
+        // RoPE sits between W_UK and the query, so there is no absorbed form.
+        // The prefill path with one query per sequence at position
+        // seq_lens[b] - 1 computes exactly that (keys and values of every
+        // cache row up to max_seq, causal attention).
+        if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
+        if (!q_nope || !o || !ws || !seq_lens || !cache->lat || !w->W_UK || !w->W_UV || q_rope)
+            return MLA_ERR_INVALID_ARG;
+        if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
+        if (!align_ok(c, {q_nope, cache->lat, w->W_UK, w->W_UV, o, ws})) return MLA_ERR_INVALID_ARG;
+        const int64_t kv_rows = c.max_seq;
+        PrefillWs L = prefill_ws(c, B, kv_rows);
+        if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
+        cudaStream_t s = (cudaStream_t)stream;
+        MLA_TRY_CUDA(positions_from_lengths(seq_lens, B, c.max_seq, (int32_t *)((char *)ws + L.start_pos),
+                                            (uint32_t *)ws, s));
+        return prefill_core(h, w, q_nope, nullptr, cache, B, 1, kv_rows, o, ws, s);
+    }
     const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
     if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
     if (!q_nope || !o || !ws || !seq_lens || !cache->lat || !w->W_UK || !w->W_UV) return MLA_ERR_INVALID_ARG;

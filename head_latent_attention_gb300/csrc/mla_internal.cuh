@@ -312,6 +312,10 @@ struct PrefillTcArgs {
     uint32_t *status;
 };
 bool prefill_tc_supported(int d_nope, int d_rope, int d_v);
+// start_pos[b] = seq_lens[b] - 1 for a decode step that runs the prefill
+// kernels (small-model form); -1 (zero output) and a flag for bad lengths.
+cudaError_t positions_from_lengths(const int32_t *seq_lens, int B, int max_seq, int32_t *start_pos,
+                                   uint32_t *status, cudaStream_t s);
 cudaError_t prefill_tc(const PrefillTcArgs &a, cudaStream_t s);
 
 struct PrefillArgs {

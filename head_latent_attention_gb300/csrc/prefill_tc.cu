@@ -397,6 +397,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && *abort_flag && p.status) atomicOr(p.status, kStatusTimeout);
 }
 
+// Query positions of a one-token-per-sequence step from the cache lengths
+// (the length includes the new token): start_pos[b] = seq_lens[b] - 1, or -1
+// (no visible key: a zero output) for a length outside [1, max_seq], which
+// is flagged.
+__global__ void __launch_bounds__(256) positions_from_lengths_kernel(const int32_t *seq_lens, int B, int max_seq,
+                                                                     int32_t *start_pos, uint32_t *status)
+{
+    ptx::pdl_trigger();
+    ptx::pdl_wait();
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int L = seq_lens[b];
+    const bool ok = L >= 1 && L <= max_seq;
+    if (!ok) atomicOr(status, kStatusLen);
+    start_pos[b] = ok ? L - 1 : -1;
+}
+
 // fp16 copy of the rope keys of rows [0, kv_rows) of every sequence.
 __global__ void __launch_bounds__(256) rope_to_f16_kernel(const uint16_t *rope, int64_t stride, int max_seq,
                                                           int64_t kv_rows, int B, uint16_t *out)
@@ -459,6 +476,16 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
 }
 
 }  // namespace
+
+cudaError_t positions_from_lengths(const int32_t *seq_lens, int B, int max_seq, int32_t *start_pos,
+                                   uint32_t *status, cudaStream_t s)
+{
+    if (B == 0) return cudaSuccess;
+    cudaError_t e = launch_ex(positions_from_lengths_kernel, dim3((B + 255) / 256), dim3(256), 0, s, 1, seq_lens, B,
+                              max_seq, start_pos, status);
+    note_launch();
+    return e;
+}
 
 bool prefill_tc_supported(int d_nope, int d_rope, int d_v)
 {

@@ -140,7 +140,8 @@ mla_status mla_create(const mla_config *cfg, mla_handle **out);
 void mla_destroy(mla_handle *h);
 
 /* Workspace bytes that any call on up to `batch` sequences of up to
- * `max_len` keys, or on up to `n_tokens` projected tokens, needs.
+ * `max_len` keys, or on up to `n_tokens` projected tokens, needs (a SMALL
+ * decode step always needs room for max_seq rows per sequence).
  * Returns 0 if h is NULL or a size is negative. */
 size_t mla_workspace_size(const mla_handle *h, int batch, int max_len,
                           int64_t n_tokens);
@@ -180,9 +181,12 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope,
  * (the length includes the new token, which mla_project_latent must have
  * appended).  DECOUPLED: q_abs = W_UK,h^T q_nope,h; scores q_abs . c_j +
  * q_rope,h . k_R,j over the latent cache; o_lat = softmax-weighted sum of c_j;
- * o_h = W_UV,h o_lat.  MLRA: the same per latent block.  SMALL returns
- * MLA_ERR_UNSUPPORTED (RoPE sits between W_UK and the query, so there is no
- * absorbed form).  q_nope [B, H, d_nope], q_rope [B, H, d_rope] or NULL,
+ * o_h = W_UV,h o_lat.  MLRA: the same per latent block.  SMALL: RoPE sits
+ * between W_UK and the query, so there is no absorbed form; the keys and
+ * values of every cache row up to max_seq are decompressed (keys rotated)
+ * into the workspace each step and attended like a one-token prefill (the
+ * workspace is then prefill-sized for max_seq rows, see
+ * mla_workspace_size).  q_nope [B, H, d_nope], q_rope [B, H, d_rope] or NULL,
  * o [B, H, d_v]; seq_lens: DEVICE int32 [B], each in [1, max_seq] (others
  * are skipped, their output rows are zero, and the length bit is set in the
  * workspace status word).  B <= max_batch.  bfloat16 MLA/MLRA run on the

@@ -212,6 +212,12 @@ def test_dsv2_decode_stage_ragged(mla, oracle_mod):
     decode_stage(mla, oracle_mod, W["dsv2_decode"], [1, 64, 65, 511, 513, 1500, 4096])
 
 
+def test_small_lm_decode_stage(mla, oracle_mod):
+    # The small-model form decodes by decompressing the cache each step.
+    w = W["small_lm_prefill"].replace(seq=600)
+    decode_stage(mla, oracle_mod, w, [1, 2, 63, 64, 65, 300, 600, 129], absorbed=False)
+
+
 def test_mlra_decode_stage(mla, oracle_mod):
     w = W["mlra_decode"].replace(seq=2048)
     decode_stage(mla, oracle_mod, w, [1, 2, 255, 257, 2048])
@@ -407,13 +413,18 @@ def test_edge_cases(mla, oracle_mod):
     assert mla.mla_project_latent(lay.h, lay.w, x, seq, pos, lay.cache, qa, qb, lay.ws) == 0
     st, bits = lay.device_status()
     assert st == mla.MLA_ERR_DEVICE_DATA and (bits & 1) and (bits & 2)
-    # Small-model decode has no absorbed form.
+    # Small-model decode (no absorbed form): a length beyond max_seq is
+    # skipped with a zero output and flagged, a rope query is refused.
     ws_ = W["small_lm_prefill"]
     dw, _ = weights_of(ws_)
     lay2 = make_layer(mla, ws_, dw, 4, max_batch=2, max_seq=64)
     qq = torch.zeros(2, ws_.n_heads, ws_.d_nope, dtype=dt, device="cuda")
-    oo = torch.empty_like(qq)
-    assert mla.mla_decode(lay2.h, lay2.w, qq, None, lay2.cache, sl[:2], 2, oo, lay2.ws) == 2
+    oo = torch.full_like(qq, float("nan"))
+    assert mla.mla_decode(lay2.h, lay2.w, qq, qq, lay2.cache, sl[:2], 2, oo, lay2.ws) == 1
+    assert mla.mla_decode(lay2.h, lay2.w, qq, None, lay2.cache, sl[:2], 2, oo, lay2.ws) == 0
+    st, bits = lay2.device_status()
+    assert st == mla.MLA_ERR_DEVICE_DATA and bits == 4
+    assert torch.all(oo[1] == 0)
 
 
 # ---------------------------------------------------------------------------
