@@ -69,7 +69,6 @@ __global__ void __launch_bounds__(kThreads, 1) absorb_kernel(const __grid_consta
     const int h = blockIdx.x, b0 = blockIdx.y * kTok;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (threadIdx.x == 0) {
-        ptx::pdl_trigger();
         ptx::mbar_init(w_full, 1);
         ptx::mbar_init(q_full, 1);
         ptx::mbar_init(mma_done, 1);
@@ -83,8 +82,11 @@ __global__ void __launch_bounds__(kThreads, 1) absorb_kernel(const __grid_consta
 #pragma unroll
         for (int i = 0; i < C::kBoxes; ++i)
             ptx::tma_load_2d_hint(sW + i * kWBox, &tw, w_full, i * 64, h * kD, evict_first);
-        // The queries come from the projection kernel.
+        // The queries come from the projection kernel.  The trigger comes after
+        // the wait: the split-KV kernel that follows reads the scheduler's
+        // output (written by the previous kernel) before its own wait.
         ptx::pdl_wait();
+        ptx::pdl_trigger();
         ptx::mbar_expect_tx(q_full, 2 * kQBox);
         ptx::tma_load_2d(sQ, &tq, q_full, h * kD, b0);
         ptx::tma_load_2d(sQ + kQBox, &tq, q_full, h * kD + 64, b0);

@@ -828,9 +828,11 @@ __device__ __forceinline__ int last_range_at_or_before(const int *range_start, i
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seq_lens, int B, int max_seq, int n,
                                                                int seg_cost, DecodeSched sc, uint32_t *status)
 {
-    // No early trigger: the kernel after this one starts only once the
-    // schedule is complete, so the split-KV kernel that follows it may read
-    // the schedule (and anything written before it) before its own wait.
+    // The kernel after this one (the absorption) lets its own successor start
+    // only after its wait for this kernel has returned, so the split-KV
+    // kernel may read the schedule (and anything written before it) before
+    // its own wait.
+    ptx::pdl_trigger();
     ptx::pdl_wait();
     int *prefix = sc.prefix;
     __shared__ int warp_sums[32];

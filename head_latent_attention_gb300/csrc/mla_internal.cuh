@@ -234,8 +234,9 @@ DecodeSched decode_sched_at(void *base, int B, int n);
 // equal estimated cost, a sequence start counting as seg_cost extra keys
 // (the per-segment overhead of the kernel), which also moves range starts
 // that fall within seg_cost keys after a sequence start onto that start.
-// decode_schedule runs before the kernel that precedes the split-KV kernel
-// (the decode kernels read its output before their own dependency wait; see
+// decode_schedule runs right before the absorption kernel, which lets the
+// split-KV kernel start only after its own wait for the scheduler (the decode
+// kernels read the schedule before their own dependency wait; see
 // decode_tc.cu), so callers launch it first.
 void decode_schedule(const int32_t *seq_lens, int B, int max_seq, int n_ranges, int seg_cost, const DecodeSched &sc,
                      uint32_t *status, cudaStream_t s);
