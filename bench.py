@@ -292,20 +292,22 @@ def run_ours(args, rank, world, device):
     kms = sum(kern_ms) / K
 
     # End to end through the C ABI from pinned host buffers: H2D of the step's
-    # inputs (token activations, positions, lengths) and D2H of its output,
-    # captured with the step in one graph.
-    x_h = torch.from_numpy(xs.view(np.int16)).view(torch.bfloat16).pin_memory()
-    pos_h = torch.from_numpy(lens - 1).pin_memory()
-    sl_h = torch.from_numpy(lens.copy()).pin_memory()
+    # inputs (token activations, positions, lengths: one pinned staging
+    # buffer, one copy) and D2H of its output, captured with the step in one
+    # graph.
+    nx, ni = x.numel() * 2, B * 4
+    inp_h = torch.empty(nx + 2 * ni, dtype=torch.uint8).pin_memory()
+    inp_h[:nx].copy_(torch.from_numpy(np.ascontiguousarray(xs).view(np.uint8).reshape(-1)))
+    inp_h[nx:nx + ni].copy_(torch.from_numpy((lens - 1).astype(np.int32).view(np.uint8)))
+    inp_h[nx + ni:].copy_(torch.from_numpy(lens.astype(np.int32).view(np.uint8)))
     y_h = torch.empty(B, w.d_model, dtype=torch.bfloat16).pin_memory()
-    x_d = torch.empty_like(x)
-    pos_d = torch.empty_like(pos)
-    sl_d = torch.empty_like(sl)
+    inp_d = torch.empty(inp_h.numel(), dtype=torch.uint8, device=device)
+    x_d = inp_d[:nx].view(torch.bfloat16).view(B, w.d_model)
+    pos_d = inp_d[nx:nx + ni].view(torch.int32)
+    sl_d = inp_d[nx + ni:].view(torch.int32)
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2):
-        x_d.copy_(x_h, non_blocking=True)
-        pos_d.copy_(pos_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
+        inp_d.copy_(inp_h, non_blocking=True)
         step(x_d, pos_d, sl_d)
         y_h.copy_(y, non_blocking=True)
     for _ in range(2):
@@ -322,7 +324,7 @@ def run_ours(args, rank, world, device):
     t3 = time.time()
     sampler.mark(t2, t3)
     e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / K
-    h2d = x_h.numel() * 2 + pos_h.numel() * 4 + sl_h.numel() * 4
+    h2d = inp_h.numel()
     d2h = y_h.numel() * 2
 
     # Secondary: prefill layer (project + causal attention + output projection).
