@@ -170,7 +170,7 @@ cudaError_t launch_absorb(const AbsorbArgs &a, cudaStream_t s)
     if (!make_tmap_bf16(&tw, a.W_UK, (int64_t)a.H * kD, R, R, 64, kD) ||
         !make_tmap_bf16(&tq, a.q_nope, a.B, (int64_t)a.H * kD, (int64_t)a.H * kD, 64, kTok))
         return cudaErrorInvalidValue;
-    static int smem_dev = -1;
+    static std::atomic<int> smem_dev{-1};
     cudaError_t e = smem_limit_once(smem_dev, (const void *)absorb_kernel<R>, C::kSmem);
     if (e != cudaSuccess) return e;
     AbsParams p;

@@ -54,8 +54,9 @@ namespace {
 
 constexpr int kDecodeChunk = 512;  // keys per split of the CUDA-core decode
 // Estimated cost of one extra segment of the tensor-core MLA decode, in keys:
-// the segment-end stores and the next query load take about as long as
-// 400 keys of attention.
+// a sequence boundary inside a range (segment-end stores, the next query
+// load, the pipeline refill) costs about 15,000 cycles against about 1,850
+// per 48-key tile, i.e. about eight tiles.
 constexpr int kSegmentCostKeys = 384;
 constexpr double kLog2e = 1.4426950408889634;
 
@@ -455,9 +456,18 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
     return MLA_OK;
 }
 
+// Whether the prefill runs on the tensor-core path (bfloat16, supported head
+// widths); its TMA reads of the rope cache need rows of whole 16-byte units.
+static bool prefill_uses_tc(const mla_config &c)
+{
+    const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
+    return c.dtype == MLA_DTYPE_BF16 && prefill_tc_supported(c.d_nope, dec ? c.d_rope : 0, c.d_v);
+}
+
 // The prefill computation once the (device) start positions are in the
 // workspace: up-projected keys and values of rows [0, kv_rows) of every
-// sequence, then causal attention of S queries per sequence.
+// sequence, then causal attention of S queries per sequence.  The caller has
+// validated every argument.
 static mla_status prefill_core(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
                                const mla_cache *cache, int B, int S, int64_t kv_rows, void *o, void *ws,
                                cudaStream_t s)
@@ -474,7 +484,7 @@ static mla_status prefill_core(mla_handle *h, const mla_weights *w, const void *
     // Keys and values of every cached row in use (deepseek-mla forward:
     // UK_proj / UV_proj of the cached latent; mla_attn: k is then rotated;
     // mlra_attn: block-wise up-projections concatenated per head).
-    const bool tc = c.dtype == MLA_DTYPE_BF16 && prefill_tc_supported(c.d_nope, dec ? c.d_rope : 0, c.d_v);
+    const bool tc = prefill_uses_tc(c);
     int nblk = c.variant == MLA_VARIANT_MLRA ? c.n_latent_heads : 1;
     int sub_rank = c.r_kv / nblk, sub_k = H * c.d_nope / nblk, sub_v = H * c.d_v / nblk;
     for (int blk = 0; blk < nblk; ++blk) {
@@ -507,7 +517,6 @@ static mla_status prefill_core(mla_handle *h, const mla_weights *w, const void *
     }
     const float scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
     if (tc) {
-        if ((cache->rope_stride * 2) % 16 && dec) return MLA_ERR_INVALID_ARG;
         PrefillTcArgs t;
         t.B = B; t.S = S; t.H = H;
         t.d_nope = c.d_nope; t.d_rope = dec ? c.d_rope : 0; t.d_v = c.d_v;
@@ -554,6 +563,7 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
     if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
     if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
         return MLA_ERR_INVALID_ARG;
+    if (dec && prefill_uses_tc(c) && (cache->rope_stride * 2) % 16) return MLA_ERR_INVALID_ARG;
     int64_t kv_rows = 0;
     for (int b = 0; b < B; ++b) {
         int sp = start_pos ? start_pos[b] : 0;
@@ -604,6 +614,12 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
     if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
         return MLA_ERR_INVALID_ARG;
+    // Every check comes before the first launch: a refused call leaves the
+    // stream untouched.  The TMA paths need cache rows of whole 16-byte units.
+    const bool tc_mla = use_tc_decode(h), tc_mlra = use_mlra_tc(h);
+    if (tc_mla && ((cache->lat_stride * 2) % 16 || (cache->rope_stride * 2) % 16)) return MLA_ERR_INVALID_ARG;
+    if (tc_mlra && (cache->lat_stride * 2) % 16) return MLA_ERR_INVALID_ARG;
+    if (!tc_mla && !tc_mlra && decode_splits(c) > 64) return MLA_ERR_UNSUPPORTED;
     DecodeWs L = decode_ws(h, B);
     if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
@@ -613,8 +629,8 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
 
     // q_abs[b, h] = W_UK,h^T q_nope[b, h]: per head h, [B, d_nope] x [d_nope, r_lat].
     // (MLRA: the L stacked blocks [L, H*d/L, r/L] read as [H*d, r/L] rows.)
-    const bool tc_split = use_tc_decode(h) || use_mlra_tc(h);
-    const int n_ranges = use_tc_decode(h) ? h->decode_clusters : mlra_tc_ctas();
+    const bool tc_split = tc_mla || tc_mlra;
+    const int n_ranges = tc_mla ? h->decode_clusters : mlra_tc_ctas();
     const DecodeSched sc = decode_sched_at(wsb + L.prefix, B, n_ranges);
     if (tc_split) {
         // The split-KV schedule first: the attention kernel reads it (and
@@ -623,7 +639,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         // sequence start costing about as much as kSegmentCostKeys keys
         // (segment-end stores and the next query load); the MLRA kernel's
         // segments are cheap and its ranges uniform.
-        decode_schedule(seq_lens, B, c.max_seq, n_ranges, use_tc_decode(h) ? kSegmentCostKeys : 0, sc,
+        decode_schedule(seq_lens, B, c.max_seq, n_ranges, tc_mla ? kSegmentCostKeys : 0, sc,
                         (uint32_t *)ws, s);
         MLA_TRY_CUDA(cudaGetLastError());
     }
@@ -633,7 +649,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         ab.q_nope = q_nope;
         ab.W_UK = w->W_UK;
         ab.q_abs = q_abs;
-        ab.interleave = use_tc_decode(h);  // the tensor-core MLA decode reads it head-interleaved
+        ab.interleave = tc_mla;  // the tensor-core MLA decode reads it head-interleaved
         ab.status = (uint32_t *)ws;
         MLA_TRY_CUDA(absorb(ab, s));
     } else {
@@ -652,7 +668,7 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     // The tensor-core kernels leave split sequences as partials in slot order
     // (range + sequence); they are merged by the fused finish kernel or by
     // decode_combine before the value up-projection GEMM.
-    if (use_tc_decode(h)) {
+    if (tc_mla) {
         DecodeTcArgs t;
         t.B = B; t.H = H; t.r_kv = c.r_kv; t.d_rope = c.d_rope;
         t.max_batch = c.max_batch; t.max_seq = c.max_seq; t.n_clusters = h->decode_clusters;
@@ -666,12 +682,8 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         t.o_part = (bf16 *)(wsb + L.o_part);
         t.ml_part = (float *)(wsb + L.ml_part);
         t.status = (uint32_t *)ws;
-        if (!align_ok(c, {cache->lat, cache->rope}) || (cache->lat_stride * 2) % 16 ||
-            (cache->rope_stride * 2) % 16)
-            return MLA_ERR_INVALID_ARG;
         MLA_TRY_CUDA(decode_tc(t, s));
-    } else if (use_mlra_tc(h)) {
-        if ((cache->lat_stride * 2) % 16) return MLA_ERR_INVALID_ARG;
+    } else if (tc_mlra) {
         MlraTcArgs t;
         t.B = B; t.H = H; t.L = c.n_latent_heads; t.r_kv = c.r_kv;
         t.max_batch = c.max_batch; t.max_seq = c.max_seq; t.n_ctas = mlra_tc_ctas();
@@ -703,7 +715,6 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
         d.chunk = kDecodeChunk;
         d.o_lat = o_lat;
         d.status = (uint32_t *)ws;
-        if (d.n_split > 64) return MLA_ERR_UNSUPPORTED;
         MLA_TRY_CUDA(decode_simt(d, s));
     }
 

@@ -303,7 +303,7 @@ cudaError_t launch_finish(const FinishArgs &a, cudaStream_t s)
     using C = FinCfg<R>;
     CUtensorMap tw;
     if (!make_tmap_bf16(&tw, a.W_UV, (int64_t)a.H * kDv, R, R, 64, kDv)) return cudaErrorInvalidValue;
-    static int smem_dev = -1;
+    static std::atomic<int> smem_dev{-1};
     cudaError_t e = smem_limit_once(smem_dev, (const void *)decode_finish_kernel<R>, C::kSmem);
     if (e != cudaSuccess) return e;
     FinParams p;

@@ -594,7 +594,7 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     p.status = sg[0].epi.status;
     if (pl.splits > 1 && !a.split_ws) return cudaErrorInvalidValue;
     const int units = p.tiles_m * p.tiles_n * a.batch * p.splits;
-    static int smem_dev = -1;
+    static std::atomic<int> smem_dev{-1};
     cudaError_t e = smem_limit_once(smem_dev, (const void *)gemm_tc_kernel<BN, kBMN>, C::kSmem);
     if (e != cudaSuccess) return e;
     e = launch_ex(gemm_tc_kernel<BN, kBMN>, dim3(std::min(units, num_sms)), dim3(kThreads), C::kSmem, s, 1, ta,

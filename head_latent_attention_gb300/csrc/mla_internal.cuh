@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "mla.h"
 
 struct mla_handle {
@@ -27,14 +29,16 @@ void profile_end(int which, cudaStream_t s);
 // Raise a kernel's dynamic shared-memory limit once per device (call site
 // keeps `set_on_device`, initially -1): the attribute need not be set per
 // launch, and setting it only once keeps launches cheap and capturable.
-inline cudaError_t smem_limit_once(int &set_on_device, const void *func, int bytes)
+// Threads that race on the first launch both set the same attribute, which
+// is harmless; the atomic keeps the cache itself well defined.
+inline cudaError_t smem_limit_once(std::atomic<int> &set_on_device, const void *func, int bytes)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (set_on_device == dev) return cudaSuccess;
+    if (set_on_device.load(std::memory_order_relaxed) == dev) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) set_on_device = dev;
+    if (e == cudaSuccess) set_on_device.store(dev, std::memory_order_relaxed);
     return e;
 }
 

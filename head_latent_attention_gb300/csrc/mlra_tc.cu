@@ -515,7 +515,7 @@ cudaError_t mlra_tc(const MlraTcArgs &a, cudaStream_t s)
     if (!make_tmap_bf16(&tkv, a.lat, (int64_t)a.max_batch * a.max_seq, a.r_kv, a.lat_stride, 64, kKeys) ||
         !make_tmap_bf16(&tq, a.q_abs, (int64_t)a.B * a.H, kR, kR, 64, hpb))
         return cudaErrorInvalidValue;
-    static int smem_dev = -1;
+    static std::atomic<int> smem_dev{-1};
     cudaError_t e = smem_limit_once(smem_dev, (const void *)mlra_tc_kernel, kSmem);
     if (e != cudaSuccess) return e;
     MlraParams p;

@@ -455,7 +455,7 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
         tqr = tq;
         tkr = tk;
     }
-    static int smem_dev = -1;
+    static std::atomic<int> smem_dev{-1};
     cudaError_t e = smem_limit_once(smem_dev, (const void *)prefill_tc_kernel<NQ, NV>, C::kSmem);
     if (e != cudaSuccess) return e;
     PreTcParams p;

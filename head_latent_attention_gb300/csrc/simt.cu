@@ -346,7 +346,7 @@ template <typename T, int HG>
 cudaError_t launch_decode_hg(const DecodeArgs &a, cudaStream_t s)
 {
     size_t smem = sizeof(float) * (size_t)HG * (a.r_lat + a.d_rope + a.chunk);
-    static int smem_dev = -1;
+    static std::atomic<int> smem_dev{-1};
     static int smem_set = 0;
     if ((int)smem > smem_set) smem_dev = -1;  // the chunk size can grow the request
     cudaError_t e = smem_limit_once(smem_dev, (const void *)decode_partial_kernel<T, HG>, (int)smem);
@@ -379,7 +379,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s)
     int dq = a.d_qk_nope + a.d_rope;
     size_t smem = sizeof(float) * ((size_t)kPQ * dq + (size_t)kPK * dq + (size_t)kPK * a.d_v +
                                    (size_t)kPQ * (kPK + 1));
-    static int smem_dev = -1;
+    static std::atomic<int> smem_dev{-1};
     static int smem_set = 0;
     if ((int)smem > smem_set) smem_dev = -1;  // the head widths can grow the request
     cudaError_t e = smem_limit_once(smem_dev, (const void *)prefill_kernel<T>, (int)smem);

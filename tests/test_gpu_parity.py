@@ -395,6 +395,14 @@ def test_edge_cases(mla, oracle_mod):
     # Batch above capacity.
     q5 = torch.zeros(5, H, w.d_nope, dtype=dt, device="cuda")
     assert mla.mla_decode(lay.h, lay.w, q5, r1, lay.cache, sl, 5, o1, lay.ws) == 1
+    # Cache rows that are not whole 16-byte units: refused before any launch.
+    odd = mla.MlaCache(lay.cache.lat, lay.cache.rope, w.r_kv + 1, lay.cache.rope_stride)
+    n0 = mla.mla_launch_count()
+    assert mla.mla_decode(lay.h, lay.w, q1, r1, odd, sl, 4, o1, lay.ws) == 1
+    odd_r = mla.MlaCache(lay.cache.lat, lay.cache.rope, lay.cache.lat_stride, w.d_rope + 1)
+    assert mla.mla_decode(lay.h, lay.w, q1, r1, odd_r, sl, 4, o1, lay.ws) == 1
+    assert mla.mla_prefill(lay.h, lay.w, q1, r1, odd_r, 1, 1, [0], o1, lay.ws) == 1
+    assert mla.mla_launch_count() == n0
     # Prefill beyond the cache.
     assert mla.mla_prefill(lay.h, lay.w, q1, r1, lay.cache, 1, 200, [100], o1, lay.ws) == 4
     # Device-side bad lengths (0 and max_seq + 1) are skipped and flagged.
