@@ -75,6 +75,17 @@ def decode_bytes(lens) -> int:
     return int(np.sum(lens)) * (DECODE.r_kv + DECODE.d_rope) * 2
 
 
+def decode_call_extra_bytes(B: int) -> int:
+    """Bytes an mla_decode call moves besides the cache rows: the absorption
+    and value weights W_UK and W_UV, the queries read and the output written
+    (bf16)."""
+    w = DECODE
+    weights = 2 * w.n_heads * w.d_nope * w.r_kv * 2
+    q = B * w.n_heads * (w.d_nope + w.d_rope) * 2
+    out = B * w.n_heads * w.d_v * 2
+    return weights + q + out
+
+
 def decode_flops(lens) -> float:
     w = DECODE
     return float(np.sum(lens)) * w.n_heads * 2 * ((w.r_kv + w.d_rope) + w.r_kv)
@@ -253,11 +264,19 @@ def run_ours(args, rank, world, device):
     with torch.cuda.graph(graph_k):
         step(x, pos, sl)
     mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_ATTENTION, None, None)
+    # A third capture brackets the whole mla_decode call (absorption,
+    # schedule, attention, merge, W_UV).
+    cb, ce = timing_events(1)[0]
+    mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_CALL, cb, ce)
+    graph_c = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_c):
+        step(x, pos, sl)
+    mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_CALL, None, None)
+    graphs = (graph, graph_k, graph_c)
     for _ in range(max(args.warmup, 3)):
-        flush.zero_()
-        graph.replay()
-        flush.zero_()
-        graph_k.replay()
+        for g in graphs:
+            flush.zero_()
+            g.replay()
     torch.cuda.synchronize()
 
     uuid = str(getattr(torch.cuda.get_device_properties(device), "uuid", ""))
@@ -267,7 +286,7 @@ def run_ours(args, rank, world, device):
     time.sleep(0.2)
     K = args.steps
     ev = timing_events(K)
-    kern_ms = []
+    kern_ms, call_ms = [], []
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -279,17 +298,21 @@ def run_ours(args, rank, world, device):
         ev[i][1].record(stream)
         flush.zero_()
         graph_k.replay()
-        ke.synchronize()
+        flush.zero_()
+        graph_c.replay()
+        ce.synchronize()
         kern_ms.append(kb.elapsed_time(ke))
+        call_ms.append(cb.elapsed_time(ce))
     torch.cuda.synchronize()
     t1 = time.time()
     if world > 1:
         dist.barrier()
-    launches = launches_per_step * 2 * K  # the step graph and the one with the kernel's events
+    launches = launches_per_step * len(graphs) * K  # the step graph and the two with timing events
     sampler.mark(t0, t1)
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = sum(step_ms) / K
     kms = sum(kern_ms) / K
+    cms = sum(call_ms) / K
 
     # End to end through the C ABI from pinned host buffers: H2D of the step's
     # inputs (token activations, positions, lengths: one pinned staging
@@ -333,8 +356,9 @@ def run_ours(args, rank, world, device):
     clocks = sampler.summary()
 
     nbytes = decode_bytes(lens)
-    ms, e2e_ms, kms = max_over_ranks([ms, e2e_ms, kms], world, device)
+    ms, e2e_ms, kms, cms = max_over_ranks([ms, e2e_ms, kms, cms], world, device)
     value = job_rate(world, nbytes, ms) / 1e9
+    call_bytes = nbytes + decode_call_extra_bytes(B)
     e2e_val = job_rate(world, nbytes, e2e_ms) / 1e9
     achieved = nbytes / (kms * 1e-3) / 1e9
     out = {
@@ -348,13 +372,19 @@ def run_ours(args, rank, world, device):
                    "cache_bytes_per_step": nbytes,
                    "l2": "flushed between steps (512 MiB write, outside the step events)",
                    "timing": "step events around a graph of the step; the attention kernel's events "
-                             "in a second capture of the step replayed after it in the same loop",
+                             "and the decode call's events in two more captures of the step replayed "
+                             "after it in the same loop",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "kernel": "decode split-KV latent attention",
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "kernel_ms": round(kms, 5), "traffic": DECODE_TRAFFIC_BYTES,
                      "traffic_unit": "bytes per launch"},
+        "decode_call": {"what": "one mla_decode call: absorption, split-KV attention, merge, W_UV",
+                        "ms": round(cms, 5), "bytes": call_bytes,
+                        "bytes_are": "cache rows read + W_UK + W_UV + q_nope + q_rope read + o written",
+                        "GB/s": round(call_bytes / (cms * 1e-3) / 1e9, 1),
+                        "frac": round(call_bytes / (cms * 1e-3) / 1e9 / hbm_peak, 4)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),

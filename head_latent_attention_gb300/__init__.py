@@ -38,6 +38,7 @@ EXPORTS = ("mla_check_config", "mla_create", "mla_destroy", "mla_workspace_size"
            "mla_set_profile_events", "mla_out_proj_static")
 MLA_PROFILE_DECODE_ATTENTION = 0
 MLA_PROFILE_PREFILL_ATTENTION = 1
+MLA_PROFILE_DECODE_CALL = 2
 
 
 class MlaConfig(ctypes.Structure):

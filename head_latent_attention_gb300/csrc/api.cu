@@ -580,49 +580,14 @@ mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope, 
     return prefill_core(h, w, q_nope, q_rope, cache, B, S, kv_rows, o, ws, s);
 }
 
-mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
-                      const mla_cache *cache, const int32_t *seq_lens, int B, void *o, void *ws,
-                      size_t ws_bytes, void *stream)
+// The launches of a validated absorbed-form decode call: absorption, the
+// split-KV schedule and attention, the merge and W_UV.
+static mla_status decode_launch(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
+                                const mla_cache *cache, const int32_t *seq_lens, int B, void *o, void *ws,
+                                const DecodeWs &L, bool tc_mla, bool tc_mlra, cudaStream_t s)
 {
-    if (!h || !w || !cache || B < 0) return MLA_ERR_INVALID_ARG;
     const mla_config &c = h->cfg;
-    if (B == 0) return MLA_OK;
-    if (c.variant == MLA_VARIANT_SMALL) {
-        // mla_attn decodes by re-decompressing the cached latent every step:
-        // RoPE sits between W_UK and the query, so there is no absorbed form.
-        // The prefill path with one query per sequence at position
-        // seq_lens[b] - 1 computes exactly that (keys and values of every
-        // cache row up to max_seq, causal attention).
-        if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
-        if (!q_nope || !o || !ws || !seq_lens || !cache->lat || !w->W_UK || !w->W_UV || q_rope)
-            return MLA_ERR_INVALID_ARG;
-        if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
-        if (!align_ok(c, {q_nope, cache->lat, w->W_UK, w->W_UV, o, ws})) return MLA_ERR_INVALID_ARG;
-        const int64_t kv_rows = c.max_seq;
-        PrefillWs L = prefill_ws(c, B, kv_rows);
-        if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
-        cudaStream_t s = (cudaStream_t)stream;
-        MLA_TRY_CUDA(positions_from_lengths(seq_lens, B, c.max_seq, (int32_t *)((char *)ws + L.start_pos),
-                                            (uint32_t *)ws, s));
-        return prefill_core(h, w, q_nope, nullptr, cache, B, 1, kv_rows, o, ws, s);
-    }
     const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
-    if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
-    if (!q_nope || !o || !ws || !seq_lens || !cache->lat || !w->W_UK || !w->W_UV) return MLA_ERR_INVALID_ARG;
-    if (dec && (!q_rope || !cache->rope || cache->rope_stride < c.d_rope)) return MLA_ERR_INVALID_ARG;
-    if (!dec && q_rope) return MLA_ERR_INVALID_ARG;
-    if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
-    if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
-        return MLA_ERR_INVALID_ARG;
-    // Every check comes before the first launch: a refused call leaves the
-    // stream untouched.  The TMA paths need cache rows of whole 16-byte units.
-    const bool tc_mla = use_tc_decode(h), tc_mlra = use_mlra_tc(h);
-    if (tc_mla && ((cache->lat_stride * 2) % 16 || (cache->rope_stride * 2) % 16)) return MLA_ERR_INVALID_ARG;
-    if (tc_mlra && (cache->lat_stride * 2) % 16) return MLA_ERR_INVALID_ARG;
-    if (!tc_mla && !tc_mlra && decode_splits(c) > 64) return MLA_ERR_UNSUPPORTED;
-    DecodeWs L = decode_ws(h, B);
-    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
-    cudaStream_t s = (cudaStream_t)stream;
     char *wsb = (char *)ws;
     const int H = c.n_heads, r_lat = r_lat_of(c);
     void *q_abs = wsb + L.q_abs, *o_lat = wsb + L.o_lat;
@@ -746,6 +711,60 @@ mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, c
     gv.epi.out = o; gv.epi.ldc = (int64_t)H * c.d_v; gv.epi.batch_stride = c.d_v;
     MLA_TRY(run_gemm(h, gv, (uint32_t *)ws, s));
     return MLA_OK;
+}
+
+mla_status mla_decode(mla_handle *h, const mla_weights *w, const void *q_nope, const void *q_rope,
+                      const mla_cache *cache, const int32_t *seq_lens, int B, void *o, void *ws,
+                      size_t ws_bytes, void *stream)
+{
+    if (!h || !w || !cache || B < 0) return MLA_ERR_INVALID_ARG;
+    const mla_config &c = h->cfg;
+    if (B == 0) return MLA_OK;
+    if (c.variant == MLA_VARIANT_SMALL) {
+        // mla_attn decodes by re-decompressing the cached latent every step:
+        // RoPE sits between W_UK and the query, so there is no absorbed form.
+        // The prefill path with one query per sequence at position
+        // seq_lens[b] - 1 computes exactly that (keys and values of every
+        // cache row up to max_seq, causal attention).
+        if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
+        if (!q_nope || !o || !ws || !seq_lens || !cache->lat || !w->W_UK || !w->W_UV || q_rope)
+            return MLA_ERR_INVALID_ARG;
+        if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
+        if (!align_ok(c, {q_nope, cache->lat, w->W_UK, w->W_UV, o, ws})) return MLA_ERR_INVALID_ARG;
+        const int64_t kv_rows = c.max_seq;
+        PrefillWs L = prefill_ws(c, B, kv_rows);
+        if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
+        cudaStream_t s = (cudaStream_t)stream;
+        profile_begin(MLA_PROFILE_DECODE_CALL, s);
+        const mla_status st =
+            positions_from_lengths(seq_lens, B, c.max_seq, (int32_t *)((char *)ws + L.start_pos), (uint32_t *)ws,
+                                   s) == cudaSuccess
+                ? prefill_core(h, w, q_nope, nullptr, cache, B, 1, kv_rows, o, ws, s)
+                : MLA_ERR_CUDA;
+        profile_end(MLA_PROFILE_DECODE_CALL, s);
+        return st;
+    }
+    const bool dec = c.variant == MLA_VARIANT_DECOUPLED;
+    if (B > c.max_batch) return MLA_ERR_INVALID_ARG;
+    if (!q_nope || !o || !ws || !seq_lens || !cache->lat || !w->W_UK || !w->W_UV) return MLA_ERR_INVALID_ARG;
+    if (dec && (!q_rope || !cache->rope || cache->rope_stride < c.d_rope)) return MLA_ERR_INVALID_ARG;
+    if (!dec && q_rope) return MLA_ERR_INVALID_ARG;
+    if (cache->lat_stride < c.r_kv) return MLA_ERR_INVALID_ARG;
+    if (!align_ok(c, {q_nope, q_rope, cache->lat, cache->rope, w->W_UK, w->W_UV, o, ws}))
+        return MLA_ERR_INVALID_ARG;
+    // Every check comes before the first launch: a refused call leaves the
+    // stream untouched.  The TMA paths need cache rows of whole 16-byte units.
+    const bool tc_mla = use_tc_decode(h), tc_mlra = use_mlra_tc(h);
+    if (tc_mla && ((cache->lat_stride * 2) % 16 || (cache->rope_stride * 2) % 16)) return MLA_ERR_INVALID_ARG;
+    if (tc_mlra && (cache->lat_stride * 2) % 16) return MLA_ERR_INVALID_ARG;
+    if (!tc_mla && !tc_mlra && decode_splits(c) > 64) return MLA_ERR_UNSUPPORTED;
+    DecodeWs L = decode_ws(h, B);
+    if (ws_bytes < L.end) return MLA_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    profile_begin(MLA_PROFILE_DECODE_CALL, s);
+    const mla_status st = decode_launch(h, w, q_nope, q_rope, cache, seq_lens, B, o, ws, L, tc_mla, tc_mlra, s);
+    profile_end(MLA_PROFILE_DECODE_CALL, s);
+    return st;
 }
 
 mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int64_t T, void *y, void *ws,

@@ -246,7 +246,9 @@ uint64_t mla_launch_count(void);
 typedef enum {
     MLA_PROFILE_DECODE_ATTENTION = 0,  /* the split-KV latent attention kernel */
     MLA_PROFILE_PREFILL_ATTENTION = 1, /* the causal flash attention kernel */
-    MLA_PROFILE_COUNT = 2
+    MLA_PROFILE_DECODE_CALL = 2,       /* every launch of one mla_decode call (absorption, split-KV
+                                          attention, merge, W_UV), from the first to the last */
+    MLA_PROFILE_COUNT = 3
 } mla_profile_point;
 
 /* Process-wide timing hook: while set, every launch of the kernel named by
