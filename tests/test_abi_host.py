@@ -119,3 +119,15 @@ def test_status_strings(lib):
         s = lib.mla_status_string(code)
         assert s and s != "unknown status"
     assert lib.mla_status_string(99) == "unknown status"
+
+
+def test_profile_hook_arguments(lib):
+    # Host-only bookkeeping: clearing any declared point is accepted, an
+    # unknown point or a half-given pair is refused.
+    L = lib.load_library()
+    for which in (lib.MLA_PROFILE_DECODE_ATTENTION, lib.MLA_PROFILE_PREFILL_ATTENTION,
+                  lib.MLA_PROFILE_DECODE_CALL):
+        assert L.mla_set_profile_events(which, None, None) == lib.MLA_OK
+    assert L.mla_set_profile_events(3, None, None) == lib.MLA_ERR_INVALID_ARG
+    assert L.mla_set_profile_events(-1, None, None) == lib.MLA_ERR_INVALID_ARG
+    assert L.mla_set_profile_events(0, ctypes.c_void_p(16), None) == lib.MLA_ERR_INVALID_ARG
