@@ -159,7 +159,7 @@ static int *max_pos_per_seq(long n_q, const int *q_b, const int *q_pos,
 /* ------------------------------------------------------------------------ */
 
 /* Decoupled MLA, per token at absolute position pos[t] ([DS] forward, query
- * path and use_cache branch; [GI] "lets first do query" / "key-value"):
+ * path and use_cache branch; [GI] mla.py, its query and key-value steps):
  *   c_Q    = W_DQ x                       [r_q]
  *   q_nope = W_UQ c_Q                     [H, d_nope]
  *   q_rope = RoPE_pos(W_QR c_Q)  per head [H, d_rope]  (interleaved pairs)
