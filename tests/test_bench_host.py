@@ -71,3 +71,20 @@ def test_reference_arm_other_ranks_exit_silently():
                         "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_work_accounting_matches_the_workload_figures():
+    # Prefill layer at B=4, S=4096 (DeepSeek-V2 dims): the projections
+    # 2 * 149,225,472 FLOP per token, the causal attention
+    # B * H * S(S+1)/2 * 2 * ((d_nope + d_rope) + d_v), unabsorbed count.
+    total, attn = bench.prefill_flops()
+    T = 4 * 4096
+    assert attn == 4 * 128 * (4096 * 4097 / 2) * 2 * (192 + 128)
+    assert total - attn == 2 * 149_225_472 * T
+    assert total == pytest.approx(7.64e12, rel=2e-3)
+    # Decode: 1152 cache bytes per cached token (512 latent + 64 rope, bf16).
+    import numpy as np
+    assert bench.decode_bytes(np.array([1, 2, 3])) == 6 * 1152
+    # The decode call adds W_UK and W_UV (128 heads x 128 x 512 bf16 each),
+    # the queries (128 + 64 per head) and the output (128 per head).
+    assert bench.decode_call_extra_bytes(64) == 2 * 128 * 128 * 512 * 2 + 64 * 128 * (192 + 128) * 2
