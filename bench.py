@@ -63,6 +63,13 @@ def job_rate(world: int, units_per_rank: float, ms: float) -> float:
     return world * units_per_rank / (ms * 1e-3)
 
 
+def spread(ms_list):
+    """Median and 10th / 90th percentiles of per-step times (ms)."""
+    a = np.asarray(ms_list, np.float64)
+    return {"median": round(float(np.median(a)), 5), "p10": round(float(np.percentile(a, 10)), 5),
+            "p90": round(float(np.percentile(a, 90)), 5)}
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -388,12 +395,18 @@ def run_ours(args, rank, world, device):
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(launches),
+        "step_ms": spread(step_ms),
+        "kernel_ms_spread": spread(kern_ms),
         "clocks": clocks,
     }
     if pre:
         out["prefill"] = pre
+    if args.small:
+        out["small_lm_decode"] = run_small_decode(args, device)
     if args.mlra:
         out["mlra_decode"] = run_mlra(args, device)
+        if world > 1:
+            out["mlra_tp"] = run_mlra_tp(args, rank, world, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(args)
     return out
@@ -412,33 +425,63 @@ def run_prefill(args, lay_device):
     seq = torch.arange(B, dtype=torch.int32, device=lay_device).repeat_interleave(S)
     stream = torch.cuda.current_stream()
 
-    def step():
-        qn, qr = lay.project_latent(x, seq, pos)
-        o = lay.prefill(qn, qr, B, S)
-        return lay.out_proj(o)
+    dt = torch.bfloat16
+    qn = torch.empty(B * S, w.n_heads, w.d_nope, dtype=dt, device=lay_device)
+    qr = torch.empty(B * S, w.n_heads, w.d_rope, dtype=dt, device=lay_device)
+    o = torch.empty(B, S, w.n_heads, w.d_v, dtype=dt, device=lay_device)
+    y = torch.empty(B * S, w.d_model, dtype=dt, device=lay_device)
 
+    def check(st, what):
+        if st != mla.MLA_OK:
+            raise mla.MlaError(st, what)
+
+    def step():
+        check(mla.mla_project_latent(lay.h, lay.w, x, seq, pos, lay.cache, qn, qr, lay.ws), "mla_project_latent")
+        check(mla.mla_prefill(lay.h, lay.w, qn, qr, lay.cache, B, S, None, o, lay.ws), "mla_prefill")
+        check(mla.mla_out_proj(lay.h, lay.w, o.view(B * S, -1), y, lay.ws), "mla_out_proj")
+
+    # Like the decode step: one graph of the layer step without timing hooks
+    # (the step's figure) and one with events around the attention kernel
+    # (its figure), replayed alternately.  The step moves several GB, far
+    # more than L2 holds, so no flush is needed between replays.
     for _ in range(2):
         step()
     torch.cuda.synchronize()
-    K = args.prefill_steps
-    ev = timing_events(K)
-    kev = timing_events(K)
-    for i in range(K):
-        mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, kev[i][0], kev[i][1])
-        ev[i][0].record(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
         step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
+    kb, ke = timing_events(1)[0]
+    mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, kb, ke)
+    g_k = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_k):
+        step()
     mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, None, None)
-    ms = sum(a.elapsed_time(b) for a, b in ev) / K
-    kms = sum(a.elapsed_time(b) for a, b in kev) / K
+    for _ in range(3):
+        g.replay()
+        g_k.replay()
+    torch.cuda.synchronize()
+    K = max(args.prefill_steps, 1)
+    ev = timing_events(K)
+    step_ms, kern_ms = [], []
+    for i in range(K):
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+        g_k.replay()
+        ke.synchronize()
+        kern_ms.append(kb.elapsed_time(ke))
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / K
+    kms = sum(kern_ms) / K
     total, attn = prefill_flops(w)
     tf = total / (ms * 1e-3) / 1e12
     katt = attn / (kms * 1e-3) / 1e12
-    del lay
+    del lay, g, g_k
     torch.cuda.empty_cache()
     return {"workload": "dsv2_prefill", "batch": B, "seq": S, "steps": K,
-            "ms_per_step": round(ms, 4), "tflops": round(tf, 2), "unit": "TFLOP/s",
+            "timing": "graph of the layer step; attention kernel events in a second graph of it",
+            "ms_per_step": round(ms, 4), "step_ms": spread(step_ms), "tflops": round(tf, 2), "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(tf / tf_peak, 4), "flops_per_step": total,
             "roofline": {"bound": "tensor", "kernel": "causal flash attention",
                          "achieved": round(katt, 2), "peak": tf_peak, "unit": "TFLOP/s",
@@ -486,18 +529,164 @@ def run_mlra(args, device):
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     mla.mla_set_profile_events(mla.MLA_PROFILE_DECODE_ATTENTION, None, None)
-    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / K
     kms = sum(a.elapsed_time(b) for a, b in kev) / K
     nbytes = int(np.sum(lens)) * w.r_kv * 2
     del lay
     torch.cuda.empty_cache()
     return {"workload": "mlra_decode", "batch": B, "cache_len": int(lens[0]), "latent_heads": w.n_latent_heads,
-            "steps": K, "ms_per_step": round(ms, 4), "value": round(nbytes / (ms * 1e-3) / 1e9, 2),
+            "steps": K, "ms_per_step": round(ms, 4), "step_ms": spread(step_ms),
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 2),
             "unit": "GB/s", "cache_bytes_per_step": nbytes, "l2": "cache 2.1 GB > L2, no flush",
             "roofline": {"bound": "hbm", "kernel": "MLRA split-KV latent attention",
                          "achieved": round(nbytes / (kms * 1e-3) / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(nbytes / (kms * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": peak_src,
                          "kernel_ms": round(kms, 4)}}
+
+
+def run_small_decode(args, device):
+    """One small-LM decode layer step (latent projection with the cache
+    append, the per-step decompression of each sequence's cached rows into
+    keys (rotated) and values, causal attention of the one new query, output
+    projection): 8 sequences, lengths ~ U[512, 1024].  RoPE sits between W_UK
+    and the query in this form, so nothing can be absorbed; the decompression
+    covers each sequence's rows up to its length.  Graph-captured, L2 flushed
+    between steps."""
+    import torch
+    import head_latent_attention_gb300 as mla
+    hbm_peak, tf_peak, tf_sust, peak_src = peaks()
+    w = syn.WORKLOADS["small_lm_decode"]
+    B = w.batch
+    lens = syn.lengths(w)
+    lay = build_layer(w, device, B, w.seq, B, w.seq)
+    for b in range(B):
+        ls, _ = syn.cache_rows(w, b, int(lens[b]))
+        lay.cache_lat[b, :lens[b]] = to_dev(ls, device)
+    xs, _ = syn.activations(w, B)
+    x = to_dev(xs, device)
+    seq = torch.arange(B, dtype=torch.int32, device=device)
+    pos = torch.from_numpy(lens - 1).to(device)
+    sl = torch.from_numpy(lens).to(device)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    dt = torch.bfloat16
+    qn = torch.empty(B, w.n_heads, w.d_nope, dtype=dt, device=device)
+    o = torch.empty(B, w.n_heads, w.d_v, dtype=dt, device=device)
+    y = torch.empty(B, w.d_model, dtype=dt, device=device)
+
+    def check(st, what):
+        if st != mla.MLA_OK:
+            raise mla.MlaError(st, what)
+
+    def step():
+        check(mla.mla_project_latent(lay.h, lay.w, x, seq, pos, lay.cache, qn, None, lay.ws), "mla_project_latent")
+        check(mla.mla_decode(lay.h, lay.w, qn, None, lay.cache, sl, B, o, lay.ws), "mla_decode")
+        check(mla.mla_out_proj(lay.h, lay.w, o.view(B, -1), y, lay.ws), "mla_out_proj")
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    K = max(args.steps, 1)
+    ev = timing_events(K)
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / K
+    rows = int(np.sum(lens))
+    cache_bytes = rows * w.r_kv * 2
+    # Bytes the step must move in this form: the cached rows read, their keys
+    # and values (fp16) written and read back once, and the weights.
+    kv_bytes = rows * 2 * w.n_heads * w.d_nope * 2
+    weights = sum(int(np.prod(s)) for s in syn.weight_shapes(w).values()) * 2
+    all_bytes = cache_bytes + 2 * kv_bytes + weights
+    del lay, g
+    torch.cuda.empty_cache()
+    return {"workload": "small_lm_decode", "batch": B, "cache_len": "U[512,1024] seed 0", "sum_len": rows,
+            "steps": K, "ms_per_step": round(ms, 5), "step_ms": spread(step_ms),
+            "value": round(cache_bytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "cache_bytes_per_step": cache_bytes,
+            "l2": "flushed between steps (512 MiB write, outside the step events)",
+            "roofline": {"bound": "hbm", "kernel": "whole decode step (latency-bound at this size)",
+                         "bytes": all_bytes,
+                         "bytes_are": "cache rows + fp16 keys/values written and read back + weights",
+                         "achieved": round(all_bytes / (ms * 1e-3) / 1e9, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(all_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": peak_src}}
+
+
+def run_mlra_tp(args, rank, world, device):
+    """MLRA decode layer step with latent sub-head tensor parallelism across
+    the ranks (mlra_attn module docstring: each device loads 1/L of the KV
+    cache): rank s holds latent blocks [s L/n, (s+1) L/n), the heads that read
+    them and the matching columns of W_O; its step appends its latent columns,
+    attends with its heads and projects them, and one all-reduce (sum) of the
+    partial outputs [B, d_model] over NCCL gives the layer's output.  Runs
+    when the number of ranks divides L (= 4); the whole job reads the cache
+    once per step."""
+    import torch
+    import torch.distributed as dist
+    import head_latent_attention_gb300 as mla
+    from head_latent_attention_gb300 import mlra_tp
+    w = MLRA
+    if w.n_latent_heads % world or w.n_heads % world:
+        return {"workload": "mlra_decode", "n_shards": world,
+                "skipped": f"{world} ranks do not divide L = {w.n_latent_heads} latent blocks"}
+    B = w.batch
+    lens = syn.lengths(w)
+    cfg = mla.make_config(w.variant, w.dtype, w.d_model, w.n_heads, w.d_nope, w.d_rope, w.d_v, w.r_kv,
+                          w.r_q, w.n_latent_heads, w.rope_base, B, w.seq)
+    full = {k: to_dev(s, device) for k, (s, _) in syn.weights(w).items()}
+    lay = mla.MlaLayer(cfg, mlra_tp.shard_weights(full, cfg, rank, world), B, device=device, ws_max_len=0,
+                       shard=(rank, world))
+    del full
+    cols = mlra_tp.shard_cache_columns(cfg, rank, world)
+    for b in range(B):
+        ls, _ = syn.cache_rows(w, b, int(lens[b]))
+        lay.cache_lat[b, :lens[b]] = to_dev(np.ascontiguousarray(ls[:, cols]), device)
+    xs, _ = syn.activations(w, B)
+    x = to_dev(xs, device)
+    seq = torch.arange(B, dtype=torch.int32, device=device)
+    pos = torch.from_numpy(lens - 1).to(device)
+    sl = torch.from_numpy(lens).to(device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qn, _ = lay.project_latent(x, seq, pos)
+        o = lay.decode(qn, None, sl)
+        return mlra_tp.all_reduce_partial(lay.out_proj(o))
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    K = args.mlra_steps
+    ev = timing_events(K)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks([sum(step_ms) / K], world, device)[0]
+    nbytes = int(np.sum(lens)) * w.r_kv * 2  # the whole job's cache bytes per step
+    del lay
+    torch.cuda.empty_cache()
+    return {"workload": "mlra_decode", "n_shards": world, "batch": B, "cache_len": int(lens[0]),
+            "steps": K, "ms_per_step": round(ms, 4), "step_ms": spread(step_ms),
+            "value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "cache_bytes_per_step": nbytes, "cache_bytes_per_gpu": nbytes // world,
+            "collective": "NCCL all-reduce (sum) of the bf16 partial outputs [B, d_model] per step"}
 
 
 # ---------------------------------------------------------------------------
@@ -534,11 +723,24 @@ def cpu_baseline(args):
         if secs >= args.cpu_seconds:
             break
     nbytes = decode_bytes(lens[bs])
+    # The same oracle on one thread, over the shortest sequences until about
+    # a third of the budget is spent.
+    order = [int(b) for b in np.argsort(lens, kind="stable")]
+    secs1, bs1 = 0.0, []
+    for b in order:
+        secs1 += oracle_decode_sample([b], lens, Wx, 1)
+        bs1.append(b)
+        if secs1 >= args.cpu_seconds / 3:
+            break
+    nbytes1 = decode_bytes(lens[bs1])
     return {"value": round(nbytes / secs / 1e9, 5), "unit": "GB/s", "cores": n_threads,
             "kind": "oracle",
             "sample": f"oracle decode step (projection, absorbed attention, W_UV, W_O; fp64) "
                       f"for sequences 0..{len(bs) - 1} of the dsv2_decode workload "
-                      f"({int(np.sum(lens[bs]))} cached tokens, {secs:.1f} s)"}
+                      f"({int(np.sum(lens[bs]))} cached tokens, {secs:.1f} s)",
+            "single_thread": {"value": round(nbytes1 / secs1 / 1e9, 6), "unit": "GB/s", "cores": 1,
+                              "sample": f"the same oracle step on one thread for the {len(bs1)} shortest "
+                                        f"sequences ({int(np.sum(lens[bs1]))} cached tokens, {secs1:.1f} s)"}}
 
 
 def run_reference(args):
@@ -579,9 +781,10 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--prefill-steps", type=int, default=3)
+    ap.add_argument("--prefill-steps", type=int, default=20)
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--no-mlra", dest="mlra", action="store_false")
+    ap.add_argument("--no-small", dest="small", action="store_false")
     ap.add_argument("--mlra-steps", type=int, default=5)
     ap.add_argument("--mlra-only", action="store_true", help="time only the MLRA decode layer (profiling aid)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -27,6 +27,9 @@ MLA_ERR_CUDA = 5
 MLA_ERR_TIMEOUT = 6
 MLA_ERR_DEVICE_DATA = 7
 
+# Bits of the device status word (mla_get_device_status).
+STATUS_POS, STATUS_SEQ, STATUS_LEN, STATUS_TIMEOUT, STATUS_F16_RANGE = 1, 2, 4, 8, 16
+
 VARIANT_DECOUPLED, VARIANT_SMALL, VARIANT_MLRA = 0, 1, 2
 DTYPE_F32, DTYPE_BF16 = 0, 1
 TORCH_DTYPE = {DTYPE_F32: torch.float32, DTYPE_BF16: torch.bfloat16}
@@ -35,7 +38,7 @@ TORCH_DTYPE = {DTYPE_F32: torch.float32, DTYPE_BF16: torch.bfloat16}
 EXPORTS = ("mla_check_config", "mla_create", "mla_destroy", "mla_workspace_size",
            "mla_project_latent", "mla_prefill", "mla_decode", "mla_out_proj",
            "mla_get_device_status", "mla_status_string", "mla_launch_count",
-           "mla_set_profile_events", "mla_out_proj_static")
+           "mla_set_profile_events", "mla_out_proj_static", "mla_set_wait_limit", "mla_create_shard")
 MLA_PROFILE_DECODE_ATTENTION = 0
 MLA_PROFILE_PREFILL_ATTENTION = 1
 MLA_PROFILE_DECODE_CALL = 2
@@ -81,6 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     sig = {
         "mla_check_config": (I, [P]),
         "mla_create": (I, [P, ctypes.POINTER(P)]),
+        "mla_create_shard": (I, [P, I, I, ctypes.POINTER(P)]),
         "mla_destroy": (None, [P]),
         "mla_workspace_size": (S, [P, I, I, L]),
         "mla_project_latent": (I, [P, P, P, L, P, P, P, P, P, P, S, P]),
@@ -92,6 +96,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mla_status_string": (ctypes.c_char_p, [I]),
         "mla_launch_count": (ctypes.c_uint64, []),
         "mla_set_profile_events": (I, [I, P, P]),
+        "mla_set_wait_limit": (I, [L]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -179,6 +184,24 @@ def mla_create(cfg: MlaConfig) -> Handle:
     return Handle(out, cfg)
 
 
+def shard_config(cfg: MlaConfig, n_shards: int) -> MlaConfig:
+    """The part of an MLRA layer that one of n_shards shards computes: H/n
+    heads, rank r_kv/n in L/n latent blocks, the same d_model (the shape of a
+    shard handle's weights, cache and outputs)."""
+    return MlaConfig(cfg.variant, cfg.dtype, cfg.d_model, cfg.n_heads // n_shards, cfg.d_nope, cfg.d_rope,
+                     cfg.d_v, cfg.r_kv // n_shards, cfg.r_q, cfg.n_latent_heads // n_shards, cfg.rope_base,
+                     cfg.max_batch, cfg.max_seq)
+
+
+def mla_create_shard(cfg: MlaConfig, shard: int, n_shards: int) -> Handle:
+    """Handle for shard `shard` of `n_shards` of an MLRA layer (latent
+    sub-head tensor parallelism); its cfg is the shard's own part."""
+    out = ctypes.c_void_p()
+    _check(load_library().mla_create_shard(ctypes.byref(cfg), int(shard), int(n_shards), ctypes.byref(out)),
+           "mla_create_shard")
+    return Handle(out, shard_config(cfg, n_shards))
+
+
 def mla_destroy(h: Handle):
     if h.ptr:
         load_library().mla_destroy(h.ptr)
@@ -219,8 +242,24 @@ def mla_decode(h: Handle, w: MlaWeights, q_nope: torch.Tensor, q_rope: Optional[
         B, _ptr(o), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
+def _check_out_proj_args(h: Handle, o: torch.Tensor, y: torch.Tensor):
+    """o [T, H*d_v] and y [T, d_model], contiguous, in the handle's dtype:
+    the C call trusts T and the row widths it derives from the config."""
+    c = h.cfg
+    dt = TORCH_DTYPE[c.dtype]
+    T = o.shape[0]
+    if o.dim() != 2 or o.shape[1] != c.n_heads * c.d_v:
+        raise ValueError(f"o must be [T, {c.n_heads * c.d_v}], got {tuple(o.shape)}")
+    if y.dim() != 2 or tuple(y.shape) != (T, c.d_model):
+        raise ValueError(f"y must be [{T}, {c.d_model}], got {tuple(y.shape)}")
+    for name, t in (("o", o), ("y", y)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dt} tensor")
+
+
 def mla_out_proj(h: Handle, w: MlaWeights, o: torch.Tensor, y: torch.Tensor, ws: torch.Tensor,
                  stream=None) -> int:
+    _check_out_proj_args(h, o, y)
     return load_library().mla_out_proj(h.ptr, ctypes.byref(w), _ptr(o), o.shape[0], _ptr(y),
                                        _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
@@ -230,6 +269,7 @@ def mla_out_proj_static(h: Handle, w: MlaWeights, o: torch.Tensor, y: torch.Tens
     """mla_out_proj without a workspace: for callers that cannot allocate
     device memory (the scratch is a fixed buffer owned by the library; see
     include/mla.h for its size limit and sharing rules)."""
+    _check_out_proj_args(h, o, y)
     return load_library().mla_out_proj_static(h.ptr, ctypes.byref(w), _ptr(o), o.shape[0], _ptr(y),
                                               _stream(stream))
 
@@ -242,6 +282,12 @@ def mla_get_device_status(h: Handle, ws: Optional[torch.Tensor], stream=None):
 
 def mla_launch_count() -> int:
     return load_library().mla_launch_count()
+
+
+def mla_set_wait_limit(cycles: int) -> int:
+    """Give-up limit (SM clock cycles) of the projection GEMM's bounded waits;
+    0 restores the default (a test hook for the timeout path)."""
+    return load_library().mla_set_wait_limit(int(cycles))
 
 
 def mla_set_profile_events(which: int, begin: Optional[torch.cuda.Event],
@@ -264,9 +310,17 @@ class MlaLayer:
 
     def __init__(self, cfg: MlaConfig, weights: Dict[str, torch.Tensor], max_tokens: int,
                  device: str = "cuda", cache_lat: Optional[torch.Tensor] = None,
-                 cache_rope: Optional[torch.Tensor] = None, ws_max_len: Optional[int] = None):
+                 cache_rope: Optional[torch.Tensor] = None, ws_max_len: Optional[int] = None,
+                 shard: Optional[Sequence[int]] = None):
+        # shard = (s, n): this layer is shard s of n of an MLRA layer (cfg
+        # describes the whole layer; weights are the shard's, see
+        # mla_create_shard), and its outputs of out_proj are partial sums.
+        if shard is not None:
+            self.h = mla_create_shard(cfg, shard[0], shard[1])
+            cfg = self.h.cfg
+        else:
+            self.h = mla_create(cfg)
         self.cfg = cfg
-        self.h = mla_create(cfg)
         self.w = make_weights(weights)
         dt = TORCH_DTYPE[cfg.dtype]
         if cache_lat is None:

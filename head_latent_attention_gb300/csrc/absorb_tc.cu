@@ -47,6 +47,7 @@ struct AbsCfg {
 struct AbsParams {
     int B, H;
     bf16 *q_abs;  // [B, H, R], or head-interleaved (see AbsorbArgs)
+    const bf16 *q_rope;  // [B, H, 64], copied into chunks 64..71 when interleaved
     bool interleave;
     uint32_t *status;
 };
@@ -125,7 +126,8 @@ __global__ void __launch_bounds__(kThreads, 1) absorb_kernel(const __grid_consta
     // Chain m, tensor-memory lane l: latent column 128 m + l; column t of the
     // chain: sequence b0 + t.  Warps w and w + 4 share lane quadrant w % 4 and
     // take sequence halves.
-    if (ptx::mbar_wait(mma_done, 0, abort_flag)) {
+    // (Warp-uniform outcome: the tensor-memory loads below are warp-wide.)
+    if (__all_sync(0xffffffffu, ptx::mbar_wait(mma_done, 0, abort_flag))) {
         ptx::tc_fence_after();
         const int quad = warp % 4, half = warp / 4;
         const int nt = min(32, p.B - b0 - half * 32);
@@ -136,11 +138,22 @@ __global__ void __launch_bounds__(kThreads, 1) absorb_kernel(const __grid_consta
             ptx::tmem_ld_wait();
             const int col = m * 128 + quad * 32 + lane;  // latent column
             bf16 *dst = p.interleave
-                            ? p.q_abs + (((int64_t)(b0 + half * 32) * (R / 8) + col / 8) * p.H + h) * 8 + col % 8
+                            ? p.q_abs + (((int64_t)(b0 + half * 32) * kQChunks + col / 8) * kQRows + h) * 8 + col % 8
                             : p.q_abs + ((int64_t)(b0 + half * 32) * p.H + h) * R + col;
+            const int64_t tstride = p.interleave ? (int64_t)kQChunks * kQRows * 8 : (int64_t)p.H * R;
 #pragma unroll
             for (int t = 0; t < 32; ++t)
-                if (t < nt) dst[(int64_t)t * p.H * R] = __float2bfloat16_rn(__uint_as_float(r[t]));
+                if (t < nt) dst[(int64_t)t * tstride] = __float2bfloat16_rn(__uint_as_float(r[t]));
+        }
+        if (p.interleave) {
+            // The rope query of head h for the group's sequences, as chunks
+            // 64..71 (one 16-byte chunk per thread and step).
+            for (int i = threadIdx.x; i < kTok * 8; i += kThreads) {
+                const int t = i / 8, c = i % 8;
+                if (b0 + t < p.B)
+                    *reinterpret_cast<uint4 *>(p.q_abs + (((int64_t)(b0 + t) * kQChunks + 64 + c) * kQRows + h) * 8) =
+                        *reinterpret_cast<const uint4 *>(p.q_rope + ((int64_t)(b0 + t) * p.H + h) * 64 + c * 8);
+            }
         }
     } else {
         *abort_flag = 1;
@@ -176,6 +189,7 @@ cudaError_t launch_absorb(const AbsorbArgs &a, cudaStream_t s)
     AbsParams p;
     p.B = a.B; p.H = a.H;
     p.q_abs = (bf16 *)a.q_abs;
+    p.q_rope = (const bf16 *)a.q_rope;
     p.interleave = a.interleave;
     p.status = a.status;
     e = launch_ex(absorb_kernel<R>, dim3(a.H, (a.B + kTok - 1) / kTok), dim3(kThreads), C::kSmem, s, 1, tw, tq, p);
@@ -191,6 +205,7 @@ cudaError_t absorb(const AbsorbArgs &a, cudaStream_t s)
 {
     if (a.B == 0) return cudaSuccess;
     if (!absorb_supported(a.r_lat, a.d_nope)) return cudaErrorInvalidValue;
+    if (a.interleave && (a.r_lat != 512 || a.H > kQRows || !a.q_rope)) return cudaErrorInvalidValue;
     return a.r_lat == 512 ? launch_absorb<512>(a, s) : launch_absorb<256>(a, s);
 }
 

@@ -28,6 +28,13 @@ bool pdl_enabled()
 
 void note_launch(int n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
 
+static long long g_gemm_wait_cycles = 0;  // 0: the default limit
+long long gemm_wait_cycles()
+{
+    const long long v = __atomic_load_n(&g_gemm_wait_cycles, __ATOMIC_RELAXED);
+    return v > 0 ? v : ptx_default_wait_cycles();
+}
+
 // Inside stream capture the record is made external, so that it becomes an
 // event-record node of the graph the caller can time; outside capture it is a
 // plain record.  A failed diagnostic record must not surface as the error of
@@ -235,11 +242,14 @@ DecodeWs decode_ws(const mla_handle *h, int B)
     const mla_config &c = h->cfg;
     DecodeWs w;
     size_t lat = (size_t)B * c.n_heads * r_lat_of(c);
+    // The tensor-core MLA decode reads the absorbed query (and the rope
+    // query) head-interleaved, 128 head rows per chunk.
+    size_t qsz = use_tc_decode(h) ? (size_t)B * kQChunks * kQRows * 8 : lat;
     size_t parts = use_tc_decode(h)  ? (size_t)(h->decode_clusters + B) * c.n_heads
                    : use_mlra_tc(h) ? (size_t)(mlra_tc_ctas() + B) * c.n_heads
                                      : (size_t)B * decode_splits(c) * c.n_heads;
     w.q_abs = kWsHeader;
-    w.o_lat = round_up(w.q_abs + lat * esize(c), 256);
+    w.o_lat = round_up(w.q_abs + qsz * esize(c), 256);
     w.o_part = round_up(w.o_lat + lat * esize(c), 256);
     w.ml_part = round_up(w.o_part + parts * r_lat_of(c) * 4, 256);
     w.prefix = round_up(w.ml_part + parts * 2 * 4, 256);
@@ -353,15 +363,14 @@ mla_status mla_check_config(const mla_config *c)
     return MLA_OK;
 }
 
-mla_status mla_create(const mla_config *cfg, mla_handle **out)
+// A handle computing the layer described by cfg (already validated).
+static mla_status create_handle(const mla_config *cfg, int shard, int n_shards, mla_handle **out)
 {
-    if (!out) return MLA_ERR_INVALID_ARG;
-    *out = nullptr;
-    mla_status st = mla_check_config(cfg);
-    if (st != MLA_OK) return st;
     mla_handle *h = new (std::nothrow) mla_handle();
     if (!h) return MLA_ERR_CUDA;
     h->cfg = *cfg;
+    h->shard = shard;
+    h->n_shards = n_shards;
     h->rope_dim = rope_dim_of(*cfg);
     h->rope_table = nullptr;
     h->status = nullptr;
@@ -399,6 +408,37 @@ mla_status mla_create(const mla_config *cfg, mla_handle **out)
     }
     *out = h;
     return MLA_OK;
+}
+
+mla_status mla_create(const mla_config *cfg, mla_handle **out)
+{
+    if (!out) return MLA_ERR_INVALID_ARG;
+    *out = nullptr;
+    mla_status st = mla_check_config(cfg);
+    if (st != MLA_OK) return st;
+    return create_handle(cfg, 0, 1, out);
+}
+
+mla_status mla_create_shard(const mla_config *cfg, int shard, int n_shards, mla_handle **out)
+{
+    if (!out) return MLA_ERR_INVALID_ARG;
+    *out = nullptr;
+    mla_status st = mla_check_config(cfg);
+    if (st != MLA_OK) return st;
+    if (cfg->variant != MLA_VARIANT_MLRA) return MLA_ERR_UNSUPPORTED;
+    const int L = cfg->n_latent_heads;
+    if (n_shards < 1 || shard < 0 || shard >= n_shards || L % n_shards || cfg->n_heads % n_shards)
+        return MLA_ERR_INVALID_ARG;
+    // mlra_attn module docstring: device i loads 1/L of the cache.  The shard
+    // is the MLRA layer restricted to its latent blocks and the heads that
+    // read them (contiguous ranges, since head h reads block h L / H); its
+    // output projection takes W_O's columns of those heads, so the layer's
+    // output is the sum of the shards' partial outputs.
+    mla_config eff = *cfg;
+    eff.n_heads = cfg->n_heads / n_shards;
+    eff.r_kv = cfg->r_kv / n_shards;
+    eff.n_latent_heads = L / n_shards;
+    return create_handle(&eff, shard, n_shards, out);
 }
 
 void mla_destroy(mla_handle *h)
@@ -499,6 +539,8 @@ static mla_status prefill_core(mla_handle *h, const mla_weights *w, const void *
         gk.epi.ldc = ldk;
         gk.epi.batch_stride = kv_rows * ldk;
         gk.epi.out_f16 = tc;
+        gk.epi.range_start = d_sp;
+        gk.epi.range_len = S;
         if (c.variant == MLA_VARIANT_SMALL) {
             gk.epi.rope_mode = kRopeHalf; gk.epi.rope_dim = c.d_nope;
             gk.epi.rope_table = h->rope_table; gk.epi.max_seq = c.max_seq;
@@ -513,6 +555,8 @@ static mla_status prefill_core(mla_handle *h, const mla_weights *w, const void *
         gv.epi.ldc = ldv;
         gv.epi.batch_stride = kv_rows * ldv;
         gv.epi.out_f16 = tc;
+        gv.epi.range_start = d_sp;
+        gv.epi.range_len = S;
         MLA_TRY(run_gemm(h, gv, (uint32_t *)ws, s));
     }
     const float scale_log2 = (float)(kLog2e / sqrt((double)(c.d_nope + (dec ? c.d_rope : 0))));
@@ -612,6 +656,7 @@ static mla_status decode_launch(mla_handle *h, const mla_weights *w, const void 
         AbsorbArgs ab;
         ab.B = B; ab.H = H; ab.r_lat = r_lat; ab.d_nope = c.d_nope;
         ab.q_nope = q_nope;
+        ab.q_rope = tc_mla ? q_rope : nullptr;
         ab.W_UK = w->W_UK;
         ab.q_abs = q_abs;
         ab.interleave = tc_mla;  // the tensor-core MLA decode reads it head-interleaved
@@ -800,6 +845,13 @@ mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t
 }
 
 uint64_t mla_launch_count(void) { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+mla_status mla_set_wait_limit(int64_t cycles)
+{
+    if (cycles < 0) return MLA_ERR_INVALID_ARG;
+    __atomic_store_n(&g_gemm_wait_cycles, (long long)cycles, __ATOMIC_RELAXED);
+    return MLA_OK;
+}
 
 mla_status mla_set_profile_events(int which, void *begin, void *end)
 {

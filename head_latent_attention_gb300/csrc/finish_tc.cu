@@ -266,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_finish_kernel(const __grid
     // 4. Accumulator row d (tensor-memory lane d) holds o[b0 + t, h, d] in
     // column t; warps w and w + 4 share lane quadrant w % 4 and take token
     // halves.
-    if (ptx::mbar_wait(mma_done, 0, abort_flag)) {
+    // (Warp-uniform outcome: the tensor-memory loads below are warp-wide.)
+    if (__all_sync(0xffffffffu, ptx::mbar_wait(mma_done, 0, abort_flag))) {
         ptx::tc_fence_after();
         const int quad = warp % 4, half = warp / 4;
         const int d = quad * 32 + lane;

@@ -37,6 +37,7 @@ struct TcGemmParams {
     int seg_n0[kMaxSeg + 1];
     Epilogue epi[kMaxSeg];
     uint32_t *status;
+    long long wait_cycles;     // give-up limit of the pipeline waits
 };
 
 template <int BN>
@@ -120,11 +121,18 @@ __device__ __forceinline__ void store_chunk_seg(const TcGemmParams &p, const Epi
         dst = (uint16_t *)e.out + (int64_t)z * e.batch_stride + (int64_t)m * e.ldc + n0;
     }
     if (e.out_f16) {
+        // fp16 operands of the prefill attention: values beyond fp16's range
+        // saturate at 65504 and raise the range flag.
+        bool over = false;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) over |= ptx::beyond_f16(v[i]);
+        if (over && e.range_start && m >= e.range_start[z] + e.range_len) over = false;
+        if (over && e.status) atomicOr(e.status, kStatusF16Range);
 #pragma unroll
         for (int i = 0; i < NC; i += 8)
             *reinterpret_cast<uint4 *>(dst + i) =
-                make_uint4(ptx::pack_f16(v[i], v[i + 1]), ptx::pack_f16(v[i + 2], v[i + 3]),
-                           ptx::pack_f16(v[i + 4], v[i + 5]), ptx::pack_f16(v[i + 6], v[i + 7]));
+                make_uint4(ptx::pack_f16_satfinite(v[i], v[i + 1]), ptx::pack_f16_satfinite(v[i + 2], v[i + 3]),
+                           ptx::pack_f16_satfinite(v[i + 4], v[i + 5]), ptx::pack_f16_satfinite(v[i + 6], v[i + 7]));
     } else {
 #pragma unroll
         for (int i = 0; i < NC; i += 8)
@@ -146,6 +154,15 @@ __device__ __forceinline__ void store_chunk(const TcGemmParams &p, int z, int m,
     else store_chunk_seg<NC>(p, p.epi[2], z, m, ng - p.seg_n0[2], v);
 }
 
+// Row tile mt of batch entry z lies wholly past the rows in use (see
+// Epilogue::range_start): no role loads, multiplies or stores it.  Read after
+// the wait for the previous kernel, which may write the limits.
+__device__ __forceinline__ bool unit_skipped(const TcGemmParams &p, int z, int mt)
+{
+    const Epilogue &e = p.epi[0];
+    return p.nseg == 1 && e.range_start && mt * kBM >= e.range_start[z] + e.range_len;
+}
+
 template <int BN, bool kBMN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -162,7 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
     uint64_t *acc_empty = acc_full + 2;
-    uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
+    uint64_t *mma_drain = acc_empty + 2;  // the MMA thread's issued MMAs completed (give-up path)
+    uint32_t *tmem_slot = (uint32_t *)(mma_drain + 1);
     volatile int *abort_flag = (volatile int *)(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -175,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&acc_full[i], 1);
             ptx::mbar_init(&acc_empty[i], 4);
         }
+        ptx::mbar_init(mma_drain, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -224,7 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // first stages of B go out before the wait for the previous
             // kernel, overlapping its tail.
             int pre = 0;
-            if ((int)blockIdx.x < num_units) {
+            // (Not when tiles may be skipped: whether this one is, is known
+            // only after the wait.)
+            if ((int)blockIdx.x < num_units && !(p.nseg == 1 && p.epi[0].range_start)) {
                 int z, mt, nt;
                 const int u = blockIdx.x;
                 tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
@@ -241,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
                 int z, mt, nt;
                 tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
+                if (unit_skipped(p, z, mt)) continue;
                 const int ks = u / num_tiles;
                 const int kb0 = ks * p.kb_per_split, kb1 = min(nk, kb0 + p.kb_per_split);
                 const int ax = (int)(z * p.a_col_batch), ay = (int)(z * p.a_row_batch) + mt * kBM;
@@ -252,7 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // Stage already armed and holding its weights.
                         --pre;
                     } else {
-                        if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                        if (!ptx::mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.wait_cycles)) {
+                            ok = false;
+                            break;
+                        }
                         ptx::mbar_expect_tx(&full[stage], C::kStageBytes);
                         load_b(stage, tmB, z, brow, kb);
                     }
@@ -276,13 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+                {
+                    int z, mt, nt;
+                    tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
+                    if (unit_skipped(p, z, mt)) continue;
+                }
                 const int ks = u / num_tiles;
                 const int kb0 = ks * p.kb_per_split, kb1 = min(nk, kb0 + p.kb_per_split);
-                if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                if (!ptx::mbar_wait(&acc_empty[acc], acc_phase ^ 1, abort_flag, p.wait_cycles)) { ok = false; break; }
                 ptx::tc_fence_after();
                 const uint32_t d = tmem + acc * BN;
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+                    if (!ptx::mbar_wait(&full[stage], phase, abort_flag, p.wait_cycles)) { ok = false; break; }
                     ptx::tc_fence_after();
                     const uint32_t a0 = ptx::smem_u32(sA + stage * C::kABytes);
                     const uint32_t b0 = ptx::smem_u32(sB + stage * C::kBBytes);
@@ -301,7 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1;
             }
-            if (!ok) *abort_flag = 1;
+            if (!ok) {
+                *abort_flag = 1;
+                // Giving up: the MMAs already issued still read shared memory
+                // and write tensor memory; they complete before the CTA frees
+                // either.
+                ptx::mma_commit(mma_drain);
+                volatile int never = 0;
+                ptx::mbar_wait(mma_drain, 0, &never);
+            }
         }
     } else {
         ptx::pdl_wait();
@@ -311,11 +349,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
             int z, mt, nt;
             tile_coords(u % num_tiles, p.tiles_m, p.tiles_n, z, mt, nt);
+            if (unit_skipped(p, z, mt)) continue;
             const int ks = u / num_tiles;
             const int sg = segment_of(p, nt * BN);
             const bool half_rope = (sg == 0 ? p.epi[0].rope_mode : (sg == 1 ? p.epi[1].rope_mode : p.epi[2].rope_mode)) ==
                                    kRopeHalf;
-            if (!ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag)) { ok = false; break; }
+            // (Warp-uniform outcome: the tensor-memory loads below are warp-wide.)
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&acc_full[acc], acc_phase, abort_flag, p.wait_cycles))) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
             const int m = mt * kBM + quad * 32 + lane;
             const uint32_t tbase = tmem + acc * BN + ((uint32_t)(quad * 32) << 16);
@@ -592,6 +635,7 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     }
     for (int i = ns; i < kMaxSeg; ++i) p.epi[i] = sg[0].epi;
     p.status = sg[0].epi.status;
+    p.wait_cycles = gemm_wait_cycles();
     if (pl.splits > 1 && !a.split_ws) return cudaErrorInvalidValue;
     const int units = p.tiles_m * p.tiles_n * a.batch * p.splits;
     static std::atomic<int> smem_dev{-1};
@@ -611,6 +655,8 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     }
     return e;
 }
+
+long long ptx_default_wait_cycles() { return ptx::kWaitCycles; }
 
 cudaError_t gemm_tc(const GemmArgs &a, int num_sms, cudaStream_t s)
 {

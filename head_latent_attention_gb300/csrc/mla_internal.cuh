@@ -10,7 +10,8 @@
 #include "mla.h"
 
 struct mla_handle {
-    mla_config cfg;
+    mla_config cfg;      // the layer this handle computes (a shard's own part for MLRA shards)
+    int shard, n_shards; // MLRA sub-head tensor parallelism: this handle's part (0 of 1 otherwise)
     int device;
     int num_sms;
     int rope_dim;        // rotated width: d_rope (decoupled), d_nope (small), 0 (MLRA)
@@ -23,6 +24,10 @@ namespace mla {
 
 // Launch bookkeeping and the optional timing hook (api.cu).
 void note_launch(int n = 1);
+// Give-up limit (SM clock cycles) of the projection GEMM's bounded waits:
+// the default (about one second) unless mla_set_wait_limit changed it.
+long long gemm_wait_cycles();
+long long ptx_default_wait_cycles();  // ptx::kWaitCycles, for host code without ptx.cuh
 void profile_begin(int which, cudaStream_t s);
 void profile_end(int which, cudaStream_t s);
 
@@ -82,6 +87,7 @@ constexpr uint32_t kStatusPos = 1u;
 constexpr uint32_t kStatusSeq = 2u;
 constexpr uint32_t kStatusLen = 4u;
 constexpr uint32_t kStatusTimeout = 8u;
+constexpr uint32_t kStatusF16Range = 16u;  // an fp16 operand of prefill was saturated
 
 // Workspace: the first 256 bytes hold the status word; call scratch follows.
 constexpr size_t kWsHeader = 256;
@@ -120,6 +126,13 @@ struct Epilogue {
     const int32_t *rope_pos = nullptr;
     uint32_t *status = nullptr;  // device status word (index flags, timeouts)
     bool out_f16 = false;        // tensor-core path: store fp16 instead of bfloat16
+    // Rows in use: with range_start set, only rows m < range_start[z] +
+    // range_len of batch entry z are needed (the cache rows a prefill's
+    // queries can see; the rest of a sequence's rows may hold anything).  The
+    // tensor-core GEMM skips whole row tiles past that limit (single-segment
+    // products) and checks only rows below it against fp16's range.
+    const int32_t *range_start = nullptr;
+    int range_len = 0;
 };
 
 // Row-major 2-D view of a tensor: rows x cols elements, row stride ld.
@@ -251,11 +264,22 @@ void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const bf16 *
 // Absorbed decode queries (absorb_tc.cu): q_abs[b, h] = W_UK,h^T q_nope[b, h]
 // with W_UK,h = rows [128 h, 128 h + 128) of W_UK viewed as [H * 128, r_lat].
 // bfloat16, d_nope == 128, r_lat in {256, 512}.
+// The absorbed decode query of the tensor-core MLA decode, head-interleaved:
+// per sequence, kQChunks 16-byte chunks of 128 head rows (chunk c of head h
+// at ((b * kQChunks + c) * 128 + h) * 16 bytes): chunks 0..63 are q_abs
+// (8 latent columns each), 64..71 the rope query q_rope.  A chunk is a
+// column of 8-row x 16-byte core matrices, so a contiguous run of chunks is
+// a K-major matrix that a bulk copy brings to shared memory and tcgen05.cp
+// moves to tensor memory as is.  Rows of heads >= H are not written.
+constexpr int kQChunks = 72;
+constexpr int kQRows = 128;
+
 struct AbsorbArgs {
     int B, H, r_lat, d_nope;
     const void *q_nope;  // [B, H * 128]
+    const void *q_rope;  // [B, H, 64] (interleave only)
     const void *W_UK;
-    void *q_abs;         // [B, H, r_lat]; interleave: element (b, h, r) at ((b * r_lat / 8 + r / 8) * H + h) * 8 + r % 8
+    void *q_abs;         // [B, H, r_lat], or the interleaved layout above (r_lat = 512)
     bool interleave;
     uint32_t *status;
 };

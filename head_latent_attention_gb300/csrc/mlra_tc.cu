@@ -378,7 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 softmax_bar();  // red may be reused
                 if (changed) {
                     // O holds every earlier P.V of the unit before it is rescaled.
-                    if (!ptx::mbar_wait(&bar->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag)) {
+                    // (Warp-uniform outcome: the tensor-memory accesses are warp-wide.)
+                    if (!__all_sync(0xffffffffu,
+                                    ptx::mbar_wait(&bar->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, abort_flag))) {
                         ok = false;
                     } else {
                         ptx::tc_fence_after();

@@ -9,6 +9,8 @@
 // device synchronisation is not acceptable.  mla_out_proj_static computes the
 // same projection with its scratch in a fixed buffer that belongs to the
 // library itself, so it allocates nothing.
+#include <atomic>
+
 #include "mla_internal.cuh"
 
 namespace {
@@ -21,8 +23,11 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 // Device address of g_static_scratch per device.  In host code the symbol
 // names a host-side stand-in, not device memory, so the address is looked up
 // with cudaGetSymbolAddress once per device (with that device current).
+// Threads that make their first call on a device at the same time may both
+// look it up; they store the same address, and the atomics keep the cache
+// itself well defined.
 constexpr int kMaxDevices = 64;
-void *g_scratch_addr[kMaxDevices] = {};
+std::atomic<void *> g_scratch_addr[kMaxDevices] = {};
 
 cudaError_t static_scratch(void **out)
 {
@@ -30,13 +35,13 @@ cudaError_t static_scratch(void **out)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
+    void *p = g_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
         e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        g_scratch_addr[dev].store(p, std::memory_order_release);
     }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

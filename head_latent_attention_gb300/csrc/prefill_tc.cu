@@ -246,25 +246,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Query tile: bfloat16 -> fp16 in place (row r of every atom).
             if (!ptx::mbar_wait(&bar->q_full[q], 0, abort_flag)) ok = false;
             if (ok) {
+                // Values beyond fp16's range saturate and raise the range flag.
+                bool over = false;
                 for (int a = 0; a < NQ; ++a) {
                     uint4 *row = reinterpret_cast<uint4 *>(sQ + a * kQ * 128 + r * 128);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         uint4 w = row[j];
-                        w.x = ptx::bf16x2_to_f16x2(w.x);
-                        w.y = ptx::bf16x2_to_f16x2(w.y);
-                        w.z = ptx::bf16x2_to_f16x2(w.z);
-                        w.w = ptx::bf16x2_to_f16x2(w.w);
+                        w.x = ptx::bf16x2_to_f16x2(w.x, over);
+                        w.y = ptx::bf16x2_to_f16x2(w.y, over);
+                        w.z = ptx::bf16x2_to_f16x2(w.z, over);
+                        w.w = ptx::bf16x2_to_f16x2(w.w, over);
                         row[j] = w;
                     }
                 }
+                if (over && p.status) atomicOr(p.status, kStatusF16Range);
                 ptx::fence_proxy_async_smem();
                 ptx::mbar_arrive(&bar->q_ready[q]);
             }
         }
         for (int t = 0; ok && t < n_kt[q]; ++t) {
             const uint32_t sbuf = C::kSCol + (2 * q + (t & 1)) * kBN;
-            if (!ptx::mbar_wait(&bar->s_full[q][t & 1], (t >> 1) & 1, abort_flag)) { ok = false; break; }
+            // (Warp-uniform outcome: the tensor-memory loads below are warp-wide.)
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->s_full[q][t & 1], (t >> 1) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
             uint32_t r0[32], r1[32];
             ptx::tmem_ld32(tmem + lane_off + sbuf, r0);
@@ -327,8 +334,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             m_run = m_new;
             // P.V(t - 1) every tile: keeps the pv_done phases observed in
             // order, and O must hold it before a rescale.
-            if (t > 0 && !ptx::mbar_wait(&bar->pv_done[q], (t - 1) & 1, abort_flag)) { ok = false; break; }
-            if (resc && t > 0 && corr != 1.f) {
+            // (Warp-uniform outcome: the tensor-memory accesses below are warp-wide.)
+            if (t > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->pv_done[q], (t - 1) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
+            // The tensor-memory loads and stores are warp-wide: a warp
+            // rescales when any of its rows needs it (the others multiply by 1).
+            const bool do_resc = resc && t > 0 && corr != 1.f;
+            if (__any_sync(0xffffffffu, do_resc)) {
+                const float cf = do_resc ? corr : 1.f;
                 ptx::tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < NV * 64; c += 32) {
@@ -336,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_ld32(tmem + lane_off + q * C::kOCol + c, o);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * corr);
+                    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * cf);
                     ptx::tmem_st32(tmem + lane_off + q * C::kOCol + c, o);
                 }
             }
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive(&bar->p_full[q]);
         }
         if (ok && n_kt[q] > 0) {
-            if (ptx::mbar_wait(&bar->pv_done[q], (n_kt[q] - 1) & 1, abort_flag)) {
+            if (__all_sync(0xffffffffu, ptx::mbar_wait(&bar->pv_done[q], (n_kt[q] - 1) & 1, abort_flag))) {
                 ptx::tc_fence_after();
                 const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll 1
@@ -416,7 +431,8 @@ __global__ void __launch_bounds__(256) positions_from_lengths_kernel(const int32
 
 // fp16 copy of the rope keys of rows [0, kv_rows) of every sequence.
 __global__ void __launch_bounds__(256) rope_to_f16_kernel(const uint16_t *rope, int64_t stride, int max_seq,
-                                                          int64_t kv_rows, int B, uint16_t *out)
+                                                          int64_t kv_rows, int B, uint16_t *out,
+                                                          const int32_t *start_pos, int S, uint32_t *status)
 {
     ptx::pdl_trigger();
     ptx::pdl_wait();
@@ -426,9 +442,12 @@ __global__ void __launch_bounds__(256) rope_to_f16_kernel(const uint16_t *rope, 
     const int64_t row = i / 8, ch = i % 8;
     const int64_t b = row / kv_rows, j = row % kv_rows;
     const uint4 w = *reinterpret_cast<const uint4 *>(rope + (b * max_seq + j) * stride + ch * 8);
+    bool over = false;
     *reinterpret_cast<uint4 *>(out + row * 64 + ch * 8) =
-        make_uint4(ptx::bf16x2_to_f16x2(w.x), ptx::bf16x2_to_f16x2(w.y), ptx::bf16x2_to_f16x2(w.z),
-                   ptx::bf16x2_to_f16x2(w.w));
+        make_uint4(ptx::bf16x2_to_f16x2(w.x, over), ptx::bf16x2_to_f16x2(w.y, over),
+                   ptx::bf16x2_to_f16x2(w.z, over), ptx::bf16x2_to_f16x2(w.w, over));
+    // Only rows that a query sees count (the others may hold anything).
+    if (over && status && j < start_pos[b] + S) atomicOr(status, kStatusF16Range);
 }
 
 template <int NQ, int NV>
@@ -448,7 +467,7 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
             return cudaErrorInvalidValue;
         cudaError_t e = launch_ex(rope_to_f16_kernel, dim3((unsigned)((KR * 64 / 8 + 255) / 256)), dim3(256), 0, s,
                                   1, (const uint16_t *)a.rope, a.rope_stride, a.max_seq, a.kv_rows, a.B,
-                                  (uint16_t *)a.k_rope16);
+                                  (uint16_t *)a.k_rope16, a.start_pos, a.S, a.status);
         note_launch();
         if (e != cudaSuccess) return e;
     } else {

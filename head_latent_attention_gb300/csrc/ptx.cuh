@@ -118,17 +118,22 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
     return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete; false on timeout or
-// when *abort becomes non-zero (another warp gave up).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
+// Wait for the phase with the given parity to complete; false after `limit`
+// SM clock cycles or when *abort becomes non-zero (another warp gave up).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          long long limit = kWaitCycles)
 {
     const uint32_t addr = smem_u32(bar);
-    if (mbar_try_wait(addr, parity)) return true;
+    // try_wait may suspend the thread until the phase completes; a limit
+    // shorter than the default (the timeout test hook) polls with test_wait
+    // instead, so that the wait can end before the phase does.
+    const bool poll = limit < kWaitCycles;
+    if (poll ? mbar_test(addr, parity) : mbar_try_wait(addr, parity)) return true;
     const long long t0 = clock64();
     for (;;) {
-        if (mbar_try_wait(addr, parity)) return true;
+        if (poll ? mbar_test(addr, parity) : mbar_try_wait(addr, parity)) return true;
         if (*abort) return false;
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
 }
 
@@ -167,6 +172,18 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// Plain (untiled) bulk copy of `bytes` contiguous global bytes into this
+// CTA's shared memory, completing on `bar`.  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
 
@@ -236,6 +253,16 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 }
 
 // Arrive (once) on a CTA-local mbarrier when all prior MMAs of this thread finish.
+// Asynchronous copy of a 128-row x 32-byte matrix from shared memory (a
+// K-major matrix descriptor: rows = tensor-memory lanes) to tensor memory:
+// row i goes to lane i, its 32 bytes to 8 consecutive columns at taddr.
+// Ordered before later tcgen05.mma of the same thread; tcgen05.commit tracks
+// its completion.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -384,11 +411,30 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// Two bfloat16 values (one 32-bit word) to two fp16 values.
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+// Two fp32 values to fp16 (round to nearest even), saturating at fp16's
+// largest finite value (65504) instead of overflowing to infinity.
+__device__ __forceinline__ uint32_t pack_f16_satfinite(float lo, float hi)
 {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// True when an fp32 value lies beyond what fp16 holds as a finite number
+// (|v| >= 65520 rounds to infinity; infinities included, NaN not).
+__device__ __forceinline__ bool beyond_f16(float v) { return fabsf(v) >= 65520.f; }
+
+// bfloat16 magnitude bits beyond fp16's finite range: 65536 (0x4780) up to
+// infinity (0x7f80); NaN patterns lie above and are not counted.
+__device__ __forceinline__ bool bf16_bits_beyond_f16(uint32_t m) { return m >= 0x4780u && m <= 0x7f80u; }
+
+// Two bfloat16 values (one 32-bit word) to two fp16 values, saturating;
+// `over` is set when either lies beyond fp16's finite range.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool &over)
+{
+    over |= bf16_bits_beyond_f16(w & 0x7fffu) || bf16_bits_beyond_f16((w >> 16) & 0x7fffu);
     const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-    return pack_f16(lo, hi);
+    return pack_f16_satfinite(lo, hi);
 }
 
 }  // namespace ptx

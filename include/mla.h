@@ -135,6 +135,26 @@ mla_status mla_check_config(const mla_config *cfg);
  * double precision on the host).  *out is NULL on failure. */
 mla_status mla_create(const mla_config *cfg, mla_handle **out);
 
+/* A handle for one shard of MLRA latent sub-head tensor parallelism
+ * ("frankenstein-transformer", latent/mlra_attn.py, module docstring: with
+ * the latent split into L sub-heads, each device loads 1/L of the KV cache).
+ * cfg describes the whole MLRA layer (H heads, latent rank r_kv split into
+ * L blocks); shard s of n_shards (n_shards divides L and H) owns latent
+ * blocks [s L/n, (s+1) L/n) and the heads that read them, [s H/n, (s+1) H/n)
+ * (head h reads block h L / H).  Every entry point then works on the shard's
+ * part, as for an MLRA layer of H/n heads, rank r_kv/n and L/n blocks with
+ * the same d_model:
+ *  - weights: W_Q rows of its heads [H/n * d_nope, d_model], W_DKV rows of
+ *    its latent columns [r_kv/n, d_model], W_UK / W_UV its L/n stacked
+ *    blocks, W_O the columns of its heads [d_model, H/n * d_v] (contiguous);
+ *  - cache: its latent columns only (r_kv/n wide);
+ *  - mla_out_proj gives the shard's partial output W_O,s o_s [T, d_model];
+ *    the layer's output is the sum of the partials over all shards (an
+ *    all-reduce across the devices, made by the caller).
+ * Returns MLA_ERR_UNSUPPORTED for other variants, MLA_ERR_INVALID_ARG for a
+ * bad shard index or count. */
+mla_status mla_create_shard(const mla_config *cfg, int shard, int n_shards, mla_handle **out);
+
 /* Release a handle and its table (NULL is allowed).  Synchronises nothing;
  * the caller must not destroy a handle with work still in flight. */
 void mla_destroy(mla_handle *h);
@@ -170,7 +190,11 @@ mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x
  * q_nope [B, S, H, d_nope], q_rope [B, S, H, d_rope] (DECOUPLED, else NULL),
  * o [B, S, H, d_v].  start_pos: HOST int32 [B] (NULL means all zero);
  * start_pos[b] + S > max_seq returns MLA_ERR_CACHE_OVERFLOW.  The keys and
- * values of every cached row in use are up-projected into the workspace. */
+ * values of every cached row in use are up-projected into the workspace.
+ * bfloat16 runs both attention contractions with fp16 operands (finer
+ * rounding than bfloat16, same tensor-core rate): query elements and
+ * up-projected keys and values must lie within fp16's range (|v| < 65520);
+ * larger ones are saturated to +-65504 and flagged (status bit 16). */
 mla_status mla_prefill(mla_handle *h, const mla_weights *w, const void *q_nope,
                        const void *q_rope, const mla_cache *cache, int B, int S,
                        const int32_t *start_pos, void *o, void *ws, size_t ws_bytes,
@@ -207,8 +231,12 @@ mla_status mla_out_proj(mla_handle *h, const mla_weights *w, const void *o, int6
  * (ws may be NULL) and of the handle (used by calls without a workspace).
  * *bits receives the flags OR-ed together (1: position out of range,
  * 2: sequence index out of range, 4: decode length out of range, 8: a bounded
- * device wait timed out and the kernel gave up).  Returns MLA_OK when no flag
- * was set, MLA_ERR_TIMEOUT when bit 8 was, MLA_ERR_DEVICE_DATA otherwise. */
+ * device wait timed out and the kernel gave up, 16: a value that the
+ * bfloat16 tensor-core prefill hands to its fp16 operands (a query element,
+ * an up-projected key or value, or a rope key of a cache row some query
+ * sees) lay beyond fp16's finite range, |v| >= 65520, and was saturated to
+ * +-65504).  Returns MLA_OK when no flag was set, MLA_ERR_TIMEOUT when bit 8
+ * was, MLA_ERR_DEVICE_DATA otherwise. */
 mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t *bits);
 
 /* Output projection that allocates nothing: the same y = W_O [o_1 ‖ ... ‖ o_H]
@@ -242,6 +270,18 @@ const char *mla_status_string(mla_status s);
 
 /* Number of kernels this library has launched in this process so far. */
 uint64_t mla_launch_count(void);
+
+/* Test hook for the give-up path of the bounded device waits: the pipeline
+ * waits of the projection GEMM (used by every bfloat16 projection, the
+ * prefill key/value up-projection and mla_out_proj) give up after `cycles`
+ * SM clock cycles instead of the default of about one second; 0 restores the
+ * default.  A wait that gives up stops the kernel's issue, lets the copies and
+ * MMAs it already issued complete, frees its tensor memory and sets the
+ * timeout bit (mla_get_device_status then returns MLA_ERR_TIMEOUT and the
+ * call's outputs are undefined).  Process-wide and read at each launch: set it
+ * only while no other thread is calling into the library.  Negative values
+ * return MLA_ERR_INVALID_ARG. */
+mla_status mla_set_wait_limit(int64_t cycles);
 
 typedef enum {
     MLA_PROFILE_DECODE_ATTENTION = 0,  /* the split-KV latent attention kernel */

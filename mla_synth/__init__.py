@@ -85,8 +85,9 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads: a tiny fp32 prefill, a small-LM prefill (RoPE on the
-# decompressed Q/K), a DeepSeek-V2-shaped decode and prefill, and an MLRA decode.
+# The five workloads of the method's statement: a tiny fp32 prefill, a
+# small-LM prefill (RoPE on the decompressed Q/K), a DeepSeek-V2-shaped decode
+# and prefill, and an MLRA decode; plus a small-LM decode step (below).
 WORKLOADS: Dict[str, Workload] = {
     "tiny_fp32_prefill": Workload(
         "tiny_fp32_prefill", VARIANT_DECOUPLED, DTYPE_F32, d_model=64, n_heads=4,
@@ -108,6 +109,14 @@ WORKLOADS: Dict[str, Workload] = {
         "mlra_decode", VARIANT_MLRA, DTYPE_BF16, d_model=2048, n_heads=16,
         d_nope=128, d_rope=0, d_v=128, r_kv=1024, r_q=0, n_latent_heads=4,
         batch=128, seq=8192, mode="decode", len_lo=8192, len_hi=8192),
+    # A decode step of the small-LM layer (the shape of its prefill: 8
+    # sequences of up to 1024 cached tokens), cache lengths ~ U[512, 1024].
+    # The pages give no decode workload for this form; this one times the
+    # per-step decompression that its RoPE placement forces.
+    "small_lm_decode": Workload(
+        "small_lm_decode", VARIANT_SMALL, DTYPE_BF16, d_model=512, n_heads=8,
+        d_nope=64, d_rope=0, d_v=64, r_kv=256, r_q=0, n_latent_heads=1,
+        batch=8, seq=1024, mode="decode", len_lo=512, len_hi=1024),
 }
 
 

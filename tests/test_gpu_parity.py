@@ -156,10 +156,15 @@ def test_mlra_prefill_e2e(mla, oracle_mod):
 # Decode stage: synthetic q and caches -> o
 # ---------------------------------------------------------------------------
 
-def decode_stage(mla, oracle_mod, w, lens, check_b=None, heads=None, absorbed=True):
+def decode_stage(mla, oracle_mod, w, lens, check_b=None, heads=None, absorbed=True, poison=False):
     B = len(lens)
     dev_w, ex_w = weights_of(w)
     lay = make_layer(mla, w, dev_w, B, max_batch=B, ws_max_len=0)
+    if poison:
+        # Cache rows past each sequence's length hold NaN: they must reach no output.
+        lay.cache_lat.fill_(float("nan"))
+        if w.d_rope:
+            lay.cache_rope.fill_(float("nan"))
     H = w.n_heads
     qs, qe = syn.stage_inputs(w, "q_nope", (B, H, w.d_nope))
     q_rope = None
@@ -216,6 +221,19 @@ def test_small_lm_decode_stage(mla, oracle_mod):
     # The small-model form decodes by decompressing the cache each step.
     w = W["small_lm_prefill"].replace(seq=600)
     decode_stage(mla, oracle_mod, w, [1, 2, 63, 64, 65, 300, 600, 129], absorbed=False)
+
+
+def test_small_lm_decode_stage_unwritten_rows_nan(mla, oracle_mod):
+    # Only each sequence's rows up to its length are decompressed; the rest
+    # (NaN here, several 128-row tiles of them for the short sequences) are
+    # neither computed nor read.
+    w = W["small_lm_decode"].replace(seq=700)
+    decode_stage(mla, oracle_mod, w, [1, 129, 700, 255, 256, 257, 400, 5], absorbed=False, poison=True)
+
+
+def test_dsv2_decode_stage_unwritten_rows_nan(mla, oracle_mod):
+    decode_stage(mla, oracle_mod, W["dsv2_decode"].replace(seq=1000), [1, 47, 48, 49, 1000, 333],
+                 poison=True)
 
 
 def test_mlra_decode_stage(mla, oracle_mod):
