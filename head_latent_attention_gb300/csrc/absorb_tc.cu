@@ -47,7 +47,6 @@ struct AbsCfg {
 struct AbsParams {
     int B, H;
     bf16 *q_abs;  // [B, H, R], or head-interleaved (see AbsorbArgs)
-    const bf16 *q_rope;  // [B, H, 64], copied into chunks 64..71 when interleaved
     bool interleave;
     uint32_t *status;
 };
@@ -145,16 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1) absorb_kernel(const __grid_consta
             for (int t = 0; t < 32; ++t)
                 if (t < nt) dst[(int64_t)t * tstride] = __float2bfloat16_rn(__uint_as_float(r[t]));
         }
-        if (p.interleave) {
-            // The rope query of head h for the group's sequences, as chunks
-            // 64..71 (one 16-byte chunk per thread and step).
-            for (int i = threadIdx.x; i < kTok * 8; i += kThreads) {
-                const int t = i / 8, c = i % 8;
-                if (b0 + t < p.B)
-                    *reinterpret_cast<uint4 *>(p.q_abs + (((int64_t)(b0 + t) * kQChunks + 64 + c) * kQRows + h) * 8) =
-                        *reinterpret_cast<const uint4 *>(p.q_rope + ((int64_t)(b0 + t) * p.H + h) * 64 + c * 8);
-            }
-        }
     } else {
         *abort_flag = 1;
     }
@@ -189,7 +178,6 @@ cudaError_t launch_absorb(const AbsorbArgs &a, cudaStream_t s)
     AbsParams p;
     p.B = a.B; p.H = a.H;
     p.q_abs = (bf16 *)a.q_abs;
-    p.q_rope = (const bf16 *)a.q_rope;
     p.interleave = a.interleave;
     p.status = a.status;
     e = launch_ex(absorb_kernel<R>, dim3(a.H, (a.B + kTok - 1) / kTok), dim3(kThreads), C::kSmem, s, 1, tw, tq, p);
@@ -205,7 +193,7 @@ cudaError_t absorb(const AbsorbArgs &a, cudaStream_t s)
 {
     if (a.B == 0) return cudaSuccess;
     if (!absorb_supported(a.r_lat, a.d_nope)) return cudaErrorInvalidValue;
-    if (a.interleave && (a.r_lat != 512 || a.H > kQRows || !a.q_rope)) return cudaErrorInvalidValue;
+    if (a.interleave && (a.r_lat != 512 || a.H > kQRows)) return cudaErrorInvalidValue;
     return a.r_lat == 512 ? launch_absorb<512>(a, s) : launch_absorb<256>(a, s);
 }
 

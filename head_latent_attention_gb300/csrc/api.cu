@@ -242,8 +242,8 @@ DecodeWs decode_ws(const mla_handle *h, int B)
     const mla_config &c = h->cfg;
     DecodeWs w;
     size_t lat = (size_t)B * c.n_heads * r_lat_of(c);
-    // The tensor-core MLA decode reads the absorbed query (and the rope
-    // query) head-interleaved, 128 head rows per chunk.
+    // The tensor-core MLA decode reads the absorbed query head-interleaved,
+    // 128 head rows per chunk.
     size_t qsz = use_tc_decode(h) ? (size_t)B * kQChunks * kQRows * 8 : lat;
     size_t parts = use_tc_decode(h)  ? (size_t)(h->decode_clusters + B) * c.n_heads
                    : use_mlra_tc(h) ? (size_t)(mlra_tc_ctas() + B) * c.n_heads
@@ -656,7 +656,6 @@ static mla_status decode_launch(mla_handle *h, const mla_weights *w, const void 
         AbsorbArgs ab;
         ab.B = B; ab.H = H; ab.r_lat = r_lat; ab.d_nope = c.d_nope;
         ab.q_nope = q_nope;
-        ab.q_rope = tc_mla ? q_rope : nullptr;
         ab.W_UK = w->W_UK;
         ab.q_abs = q_abs;
         ab.interleave = tc_mla;  // the tensor-core MLA decode reads it head-interleaved

@@ -81,17 +81,7 @@ constexpr int kPGroup = (kBKV / 8) * 128;
 constexpr int kOffP = kOffX + kXBuf * kXBytes;
 static_assert(kXWarpBytes == 4 * kPGroup, "a warp's staging block is its P rows");
 constexpr int kOffRed = kOffP + 2 * kPBytes;          // reference maxima, segment-end (max, sum)
-constexpr int kESlots = 3;                            // segment-end (max, sum) hand-over ring
-constexpr int kOffBar = kOffRed + (2 + 2 * kESlots) * kH * 4;
-// A segment's absorbed query travels through the KV ring: this CTA's 36
-// chunks of it (32 latent, 4 rope; 2 KB each: 128 head rows x 16 bytes) take
-// kQSlots ring uses of 12 chunks, whole chunk pairs each, since one
-// tcgen05.cp moves a pair (a 128-row x 32-byte matrix) to tensor memory.
-constexpr int kQSlots = 3;
-constexpr int kQChunkBytes = kQRows * 16;
-constexpr int kQSlotChunks = 12;
-constexpr int kQSlotBytes = kQSlotChunks * kQChunkBytes;
-static_assert(kQSlotBytes <= kStageBytes && kQSlots * kQSlotChunks == 36, "query slots");
+constexpr int kOffBar = kOffRed + 6 * kH * 4;
 // The cluster's view of the schedule: its range [start, end) of the
 // concatenated keys and the prefix sums of the sequences from the range's
 // first one on (kWin + 1 entries; later ones are read from global memory).
@@ -125,7 +115,7 @@ struct DecTcParams {
 };
 
 struct Bars {
-    uint64_t q_empty;  // the segment's last Q K^T completed (its query may be replaced)
+    uint64_t q_full, q_empty;  // query written to tensor memory by the softmax warps; consumed
     uint64_t kv_full[kStages], kv_empty[kStages];
     uint64_t s_full[kSBuf], s_free[kSBuf];
     uint64_t p_full[2], pv_done[2];
@@ -133,17 +123,12 @@ struct Bars {
     uint64_t x_full[kXBuf], x_free[kXBuf];
     // Softmax groups: reference-max handoff from group i, per lane quarter
     // (one arrival per thread of the producing warp), and the segment-end
-    // (max, sum) of the group that did not run the segment's last tile, per
-    // hand-over slot and lane quarter.
-    uint64_t hand[2][4], ml_full[kESlots][4];
+    // meeting of the two warps of a lane quarter.
+    uint64_t hand[2][4], seg[4];
     int abort;
     uint32_t tmem;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block");
-
-// Ring use of tile g of segment nseg: every segment's query takes kQSlots
-// uses before the segment's first tile.
-__device__ __forceinline__ int ring_use(int g, int nseg) { return g + kQSlots * (nseg + 1); }
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -184,17 +169,19 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
-// Asynchronous 16-byte store into the peer CTA's shared memory that
-// completes its bytes on the peer's mbarrier (both peer addresses already
-// mapped): no local staging, no fence; the receiver's wait on that barrier
-// makes the data visible.
-__device__ __forceinline__ void st_async_peer(uint32_t peer_dst, uint4 v, uint32_t peer_bar)
+// Bulk copy of `bytes` from this CTA's shared memory into the peer's, completing
+// the bytes on the peer's mbarrier (both peer addresses already mapped).
+__device__ __forceinline__ void bulk_to_peer(uint32_t peer_dst, const void *src, uint32_t bytes, uint32_t peer_bar)
 {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-                     peer_dst),
-                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(peer_bar)
-                 : "memory");
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t"
+        "cp.async.bulk.commit_group;" ::"r"(peer_dst),
+        "r"(ptx::smem_u32(src)), "r"(bytes), "r"(peer_bar)
+        : "memory");
 }
+// The bulk copies this thread issued have finished reading their source.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Arrive on the peer's mbarrier without ordering earlier memory operations
 // (a release at cluster scope waits for this thread's outstanding remote
 // stores, which costs thousands of cycles); callers order what they must
@@ -329,67 +316,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cid = (int)cluster_id();
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
-    // Ring loads are issued by thread 0: the first segment's first tiles
-    // right after the barriers exist (before the CTA and cluster syncs, and
-    // before the wait for the previous kernel, so the first HBM round trip
-    // overlaps both), the rest from the producer loop.  The schedule and the
-    // cache rows are complete when this kernel starts: the scheduler runs
-    // before the kernel that precedes this one and does not let it start
-    // early, and it waits for every earlier kernel itself.  Only the queries
-    // come from the previous kernel: each segment's goes out after the wait,
-    // ahead of its tiles, through the same ring.
+    // KV loads are issued by thread 0: the first kStages right after the
+    // barriers exist (before the CTA and cluster syncs, and before the wait
+    // for the previous kernel, so the first HBM round trip overlaps both),
+    // the rest from the producer loop.  The schedule and the cache rows are
+    // complete when this kernel starts: the scheduler runs before the
+    // kernel that precedes this one and does not let it start early, and it
+    // waits for every earlier kernel itself.  Only the queries come from the
+    // previous kernel.
     TileCursor ld;
-    int first_b = -1;  // sequence of the first segment (-1: the range is empty)
     int pending[kStages];
     uint64_t evict_first = 0;
-    int q_issued = -1;  // last segment whose query went out
-    // Ring use u: wait until its slot is free, arm its full barrier.
-    auto claim = [&](int u, uint32_t bytes) -> uint8_t * {
-        const int st = u % kStages;
-        const uint32_t ph = (uint32_t)(u / kStages) & 1;
-        if (!ptx::mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag)) return nullptr;
-        ptx::mbar_expect_tx(&bar->kv_full[st], bytes);
-        pending[st] = (int)ph;
-        return sKV + st * kStageBytes;
-    };
-    auto issue_tile = [&]() -> bool {
-        const int u = ring_use(ld.g, ld.nseg);
-        uint8_t *dst = claim(u, kStageBytes);
-        if (!dst) return false;
-        uint64_t *fb = &bar->kv_full[u % kStages];
+    auto issue_load = [&]() -> bool {
+        const int st = ld.g % kStages;
+        const uint32_t ph = (uint32_t)(ld.g / kStages) & 1;
+        if (!ptx::mbar_wait(&bar->kv_empty[st], ph ^ 1, abort_flag)) return false;
+        ptx::mbar_expect_tx(&bar->kv_full[st], kStageBytes);
         const int row = ld.b * p.max_seq + ld.k0 + ld.t * kBKV;
+        uint8_t *dst = sKV + st * kStageBytes;
         for (int a = 0; a < kLA; ++a)
-            ptx::tma_load_2d_hint(dst + a * kAtom, &tmL, fb, (int)rank * kLA * 64 + a * 64, row, evict_first);
-        ptx::tma_load_2d_hint(dst + kLA * kAtom, &tmR, fb, (int)rank * 32, row, evict_first);
+            ptx::tma_load_2d_hint(dst + a * kAtom, &tmL, &bar->kv_full[st], (int)rank * kLA * 64 + a * 64, row,
+                                  evict_first);
+        ptx::tma_load_2d_hint(dst + kLA * kAtom, &tmR, &bar->kv_full[st], (int)rank * 32, row, evict_first);
+        pending[st] = (int)ph;
         ld.step();
-        return true;
-    };
-    // The query of segment nseg (sequence b, first tile g): this CTA's 32
-    // latent chunks [32 rank, 32 rank + 32) and 4 rope chunks
-    // [64 + 4 rank, 68 + 4 rank) of the sequence's interleaved query, 12 per
-    // ring use.
-    auto issue_q = [&](int b, int g, int nseg) -> bool {
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(q_abs) + (int64_t)b * kQChunks * kQChunkBytes;
-        const uint8_t *lat = src + (int64_t)rank * 32 * kQChunkBytes;
-        const uint8_t *rq = src + (int64_t)(64 + rank * 4) * kQChunkBytes;
-        const int u0 = ring_use(g, nseg) - kQSlots;
-        for (int j = 0; j < kQSlots; ++j) {
-            uint8_t *dst = claim(u0 + j, kQSlotBytes);
-            if (!dst) return false;
-            uint64_t *fb = &bar->kv_full[(u0 + j) % kStages];
-            if (j < kQSlots - 1) {
-                ptx::bulk_load(dst, lat + j * kQSlotBytes, kQSlotBytes, fb);
-            } else {
-                ptx::bulk_load(dst, lat + j * kQSlotBytes, 8 * kQChunkBytes, fb);
-                ptx::bulk_load(dst + 8 * kQChunkBytes, rq, 4 * kQChunkBytes, fb);
-            }
-        }
-        q_issued = nseg;
         return true;
     };
 
     if (threadIdx.x == 0) {
         ptx::pdl_trigger();
+        ptx::mbar_init(&bar->q_full, kSoftmaxThreads / 2);  // the group that sends a segment's first tile
         ptx::mbar_init(&bar->q_empty, 1);
         for (int i = 0; i < kStages; ++i) {
             ptx::mbar_init(&bar->kv_full[i], 1);
@@ -407,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&bar->x_full[i], 1);
             ptx::mbar_init(&bar->x_free[i], kSoftmaxThreads / 64);  // one arrival per warp of a peer group
         }
-        ptx::mbar_init(&bar->o_empty, kSoftmaxThreads / 2);  // the group that stores a segment
+        ptx::mbar_init(&bar->o_empty, kSoftmaxThreads);
         for (int q = 0; q < 4; ++q) {
             ptx::mbar_init(&bar->hand[0][q], 32);
             ptx::mbar_init(&bar->hand[1][q], 32);
-            for (int k = 0; k < kESlots; ++k) ptx::mbar_init(&bar->ml_full[k][q], 32);
+            ptx::mbar_init(&bar->seg[q], 64);
         }
         bar->abort = 0;
         ptx::fence_mbar_init();
@@ -425,9 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kStages; ++i) pending[i] = -1;
         ld.init(win, p.sc.prefix, p.B);
-        if (ld.valid) first_b = ld.b;
-        // Fresh ring uses: the waits pass at once.
-        while (ld.valid && ld.nseg == 0 && ring_use(ld.g, 0) < kStages) issue_tile();
+        for (int i = 0; i < kStages && ld.valid; ++i) issue_load();  // fresh ring: no waits
         ptx::pdl_wait();
     }
     if (warp == 1) ptx::tmem_alloc(&bar->tmem, 512);
@@ -446,13 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         if (threadIdx.x == 0) {
-            // The first segment's query (fresh ring uses 0..kQSlots-1), then
-            // the stream: each later segment's query ahead of its tiles.
-            if (first_b >= 0 && !issue_q(first_b, 0, 0)) fail();
-            while (ok && ld.valid) {
-                if (ld.t == 0 && ld.nseg > q_issued && !issue_q(ld.b, ld.g, ld.nseg)) { fail(); break; }
-                if (!issue_tile()) { fail(); break; }
-            }
+            while (ok && ld.valid)
+                if (!issue_load()) { fail(); break; }
             // Copies still in flight land before the CTA may exit.
             volatile int never = 0;
             for (int i = 0; i < kStages; ++i)
@@ -469,7 +418,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             TileCursor qk, pv;
             qk.init(win, p.sc.prefix, p.B);
             pv.init(win, p.sc.prefix, p.B);
-            int q_done = -1;  // last segment whose query is in tensor memory
             long long last = clock64();
             while (ok && pv.valid) {
                 bool progressed = false;
@@ -479,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ready = ptx::mbar_test(ptx::smem_u32(&bar->o_empty), (pv.nseg - 1) & 1);
                     if (ready) {
                         ptx::tc_fence_after();
-                        const int st = ring_use(pv.g, pv.nseg) % kStages;
+                        const int st = pv.g % kStages;
                         const uint32_t vb = kv0 + st * kStageBytes;
                         const uint32_t pa = p0 + (pv.g & 1) * kPBytes;
 #pragma unroll
@@ -496,39 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Q K^T runs at most kQKAhead tiles ahead of the next P.V: the
                 // tensor pipe executes in issue order, and a Q K^T queued
                 // early would delay the P.V that frees a KV stage.
-                if (qk.valid && qk.g <= pv.g + kQKAhead && q_done < qk.nseg) {
-                    // The segment's query into tensor memory, once its ring
-                    // uses have landed and the previous segment's last Q K^T
-                    // (which read the old query) has completed.  tcgen05.cp
-                    // is ordered before the Q K^T issued after it.
-                    const int u0 = ring_use(qk.g, qk.nseg) - kQSlots;
-                    bool ready = qk.nseg == 0 || ptx::mbar_test(ptx::smem_u32(&bar->q_empty), (qk.nseg - 1) & 1);
-#pragma unroll
-                    for (int j = 0; j < kQSlots; ++j)
-                        ready = ready && ptx::mbar_test(ptx::smem_u32(&bar->kv_full[(u0 + j) % kStages]),
-                                                        ((u0 + j) / kStages) & 1);
-                    if (ready) {
-                        ptx::tc_fence_after();
-#pragma unroll
-                        for (int pr = 0; pr < kQSlots * kQSlotChunks / 2; ++pr) {
-                            const int u = u0 + pr / (kQSlotChunks / 2);
-                            const uint32_t src =
-                                kv0 + (u % kStages) * kStageBytes + (pr % (kQSlotChunks / 2)) * 2 * kQChunkBytes;
-                            // Chunk pair (2 pr, 2 pr + 1): core matrices 16
-                            // bytes wide, the next chunk kQChunkBytes on, 8-row
-                            // groups 128 bytes apart.
-                            ptx::tmem_cp_128x256b(tmem + kQCol + pr * 8, sdesc_plain(src, kQChunkBytes, 128));
-                        }
-#pragma unroll
-                        for (int j = 0; j < kQSlots; ++j) ptx::mma_commit(&bar->kv_empty[(u0 + j) % kStages]);
-                        q_done = qk.nseg;
-                        progressed = true;
-                    }
-                }
-                if (qk.valid && qk.g <= pv.g + kQKAhead && q_done == qk.nseg) {
-                    const int u = ring_use(qk.g, qk.nseg);
-                    const int st = u % kStages, sb = qk.g % kSBuf;
-                    bool ready = ptx::mbar_test(ptx::smem_u32(&bar->kv_full[st]), (u / kStages) & 1);
+                if (qk.valid && qk.g <= pv.g + kQKAhead) {
+                    const int st = qk.g % kStages, sb = qk.g % kSBuf;
+                    bool ready = qk.t > 0 || ptx::mbar_test(ptx::smem_u32(&bar->q_full), qk.nseg & 1);
+                    ready = ready && ptx::mbar_test(ptx::smem_u32(&bar->kv_full[st]), (qk.g / kStages) & 1);
                     // Score buffer sb held tile g - 2: the softmax must have read it.
                     ready = ready && (qk.g < kSBuf ||
                                       ptx::mbar_test(ptx::smem_u32(&bar->s_free[sb]), ((qk.g / kSBuf) - 1) & 1));
@@ -570,22 +489,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         float *mslot = reinterpret_cast<float *>(smem + kOffRed);  // [2][kH] reference max after tile g (slot g & 1)
-        uint32_t hand_in = 0;                                      // handoffs received
-        int seg_idx = 0;                                           // segment being walked
-        float *eslot = mslot + 2 * kH;                             // [kESlots][2][kH] (max, sum) at a segment end
-        // Rows of heads >= H hold no query (their scores are sent as 0).
-        const bool row_ok = h < p.H;
+        uint32_t hand_in = 0, nseg_done = 0;                       // handoffs received, segments finished
+        float *eslot = mslot + 2 * kH;                             // [2 groups][2][kH] (max, sum) at a segment end
         const int xblk = quad * kXWarpBytes;                       // this warp's block of an exchange buffer
-        // Row h of the peer's exchange buffer grp, and its full barrier.
-        const uint32_t peer_xrow = map_peer(smem + kOffX + grp * kXBytes + h * kXRowBytes, peer);
+        uint8_t *wstage = smem + kOffP + grp * kPBytes + xblk;
+        uint32_t *my_stage = reinterpret_cast<uint32_t *>(wstage + lane * kXRowBytes);
+        const uint32_t peer_xbuf = map_peer(smem + kOffX + grp * kXBytes + xblk, peer);
         const uint32_t peer_xfull = map_peer(&bar->x_full[grp], peer);
         const uint32_t peer_xfree = map_peer(&bar->x_free[grp], peer);
+        // This CTA's 288 query columns of row h into tensor memory (lanes =
+        // heads, bf16 pairs per 32-bit column, lower column in the low half,
+        // which is how consecutive bf16 values sit in memory), written by the
+        // group that sends the segment's first tile.
+        auto load_q = [&](int b, int nseg) -> bool {
+            if (nseg > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)))
+                return false;
+            ptx::tc_fence_after();
+            const bool row_ok = h < p.H;
+            // q_abs is stored head-interleaved: 16-byte chunk c of row (b, h) at
+            // ((b * kQChunks + c) * kQRows + h) * 16 bytes, so that a warp's
+            // load of one chunk for its 32 heads is 512 contiguous bytes.
+            const uint4 *src = reinterpret_cast<const uint4 *>(q_abs) + ((int64_t)b * kQChunks + rank * 32) * kQRows + h;
+            const uint4 *rs = reinterpret_cast<const uint4 *>(q_rope + ((int64_t)b * p.H + h) * 64 + rank * 32);
+            // Two 128-byte groups of the row in flight at a time.
+            uint4 va[8], vb[8], vr[4];
+            auto fetch = [&](uint4 (&v)[8], int c) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = row_ok ? src[(int64_t)(c * 8 + i) * kQRows] : make_uint4(0, 0, 0, 0);
+            };
+            auto put = [&](const uint4 (&v)[8], int c) {
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    w[4 * i] = v[i].x; w[4 * i + 1] = v[i].y; w[4 * i + 2] = v[i].z; w[4 * i + 3] = v[i].w;
+                }
+                ptx::tmem_st32(tmem + lane_off + kQCol + c * 32, w);
+            };
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vr[i] = row_ok ? rs[i] : make_uint4(0, 0, 0, 0);
+            fetch(va, 0);
+            fetch(vb, 1);
+            put(va, 0);
+            fetch(va, 2);
+            put(vb, 1);
+            fetch(vb, 3);
+            put(va, 2);
+            put(vb, 3);
+            {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    w[4 * i] = vr[i].x; w[4 * i + 1] = vr[i].y; w[4 * i + 2] = vr[i].z; w[4 * i + 3] = vr[i].w;
+                }
+                ptx::tmem_st16(tmem + lane_off + kQRCol, w);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar->q_full);
+            return true;
+        };
         // Row h of the partial scores of this group's tiles, scaled to log2
         // units and rounded to fp16: the current tile's and the one sent ahead.
         uint32_t own[kBKV / 2], own_next[kBKV / 2];
-        // Read the partial of tile g into own_next, free its score buffer and
-        // store the row into the peer's exchange buffer grp.
-        int last_sent = -1;  // this group's last tile sent to the peer
+        // Read the partial of tile g into own_next, free its score buffer,
+        // stage it and copy the warp's block into the peer's buffer grp.
         auto send = [&](int g) -> bool {
             const int sb = g % kSBuf;
             // (Warp-uniform outcome: the tensor-memory load below is warp-wide.)
@@ -601,27 +568,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_arrive(&bar->s_free[sb]);  // score buffer sb may take tile g + 2
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                own_next[j] = row_ok ? pack_f16_sat(__uint_as_float(r0[2 * j]) * p.scale_log2,
-                                                    __uint_as_float(r0[2 * j + 1]) * p.scale_log2)
-                                     : 0u;
+                own_next[j] = pack_f16_sat(__uint_as_float(r0[2 * j]) * p.scale_log2,
+                                           __uint_as_float(r0[2 * j + 1]) * p.scale_log2);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                own_next[16 + j] = row_ok ? pack_f16_sat(__uint_as_float(r1[2 * j]) * p.scale_log2,
-                                                         __uint_as_float(r1[2 * j + 1]) * p.scale_log2)
-                                          : 0u;
+                own_next[16 + j] = pack_f16_sat(__uint_as_float(r1[2 * j]) * p.scale_log2,
+                                                __uint_as_float(r1[2 * j + 1]) * p.scale_log2);
+            // Stage the row once the warp's previous copy has read its block,
+            // then one lane copies the warp's block to the peer.
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < kBKV / 8; ++c)
-                st_async_peer(peer_xrow + c * 16,
-                              make_uint4(own_next[4 * c], own_next[4 * c + 1], own_next[4 * c + 2], own_next[4 * c + 3]),
-                              peer_xfull);
-            last_sent = g;
+                *reinterpret_cast<uint4 *>(my_stage + 4 * c) =
+                    make_uint4(own_next[4 * c], own_next[4 * c + 1], own_next[4 * c + 2], own_next[4 * c + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) bulk_to_peer(peer_xbuf, wstage, kXWarpBytes, peer_xfull);
             return true;
         };
         TileCursor nx;  // the next tile of this group to send (sends run two tiles ahead)
         nx.init(win, p.sc.prefix, p.B);
         if (grp == 1 && nx.valid) nx.step();
         if (ok && nx.valid) {
-            if (!send(nx.g)) fail();
+            if ((nx.t == 0 && !load_q(nx.b, nx.nseg)) || !send(nx.g)) fail();
 #pragma unroll
             for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];
             nx.step();
@@ -686,7 +656,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float m_new = (mt > m_prev + kRescaleThreshold) ? mt : m_prev;
                 mslot[(g & 1) * kH + h] = m_new;
                 if (t + 1 < ntiles) ptx::mbar_arrive(&bar->hand[grp][quad]);
-                // 3. P = 2^(s - m_new) (bf16) and the group's row sum.
+                // 3. The group's next tile: its query (at a segment boundary)
+                //    and its partial, staged in P buffer grp once P.V(g - 2)
+                //    has read P(g - 2) from it.  Each pv_done barrier is
+                //    waited on phase by phase, never two phases behind
+                //    (P.V(g) cannot finish before P(g) exists).
+                if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[grp], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                if (nx.valid) {
+                    if (nx.t == 0 && !load_q(nx.b, nx.nseg)) { fail(); break; }
+                    if (!send(nx.g)) { fail(); break; }
+                    nx.step();
+                    if (nx.valid) nx.step();
+                }
+                // 4. P = 2^(s - m_new) (bf16) and the group's row sum.
                 uint32_t pk[kBKV / 2];
                 float psum;
                 {
@@ -705,6 +687,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 l_grp = l_grp * ptx::ex2(m_grp - m_new) + psum;
                 m_grp = m_new;
+#pragma unroll
+                for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];
                 // Raised: O must hold every earlier P.V before it is rescaled
                 // to the new reference.  The tensor-memory loads and stores
                 // are warp-wide, so a warp rescales when any of its rows was
@@ -726,10 +710,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ptx::tmem_st_wait();
                 }
-                // P into buffer grp once P.V(g - 2) has read P(g - 2) from it.
-                // Each pv_done barrier is waited on phase by phase, never two
-                // phases behind (P.V(g) cannot finish before P(g) exists).
-                if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[grp], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                // P over the staged partial once the warp's copy has read it.
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
                 {
                     uint8_t *prow = smem + kOffP + grp * kPBytes + (h >> 3) * kPGroup + (h & 7) * 16;
 #pragma unroll
@@ -740,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (valid < kBKV) {
                     // Rows past the segment may hold arbitrary cache contents;
                     // P is 0 there, but 0 * NaN is not 0: zero those rows.
-                    uint8_t *stg = sKV + (ring_use(g, seg_idx) % kStages) * kStageBytes;
+                    uint8_t *stg = sKV + (g % kStages) * kStageBytes;
                     const int nrow = kBKV - valid;
                     for (int i = h; i < kLA * nrow * 8; i += kH) {
                         const int a = i / (nrow * 8), rr = (i / 8) % nrow, ch = i % 8;
@@ -751,69 +734,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::fence_proxy_async_smem();  // P and zeroed rows visible to the tensor core
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(&bar->p_full[grp]);
-                // 4. The partial of the group's next tile, to the peer.  (After
-                //    P: sending needs that tile's scores, whose ring slot may
-                //    be the one P.V of this tile frees when a query shares the
-                //    ring with short segments.)
-                if (nx.valid) {
-                    if (!send(nx.g)) { fail(); break; }
-                    nx.step();
-                    if (nx.valid) nx.step();
-                }
-#pragma unroll
-                for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];  // the group's next tile's partial
             }
             if (!ok) break;
-            // Segment done.  The group that ran its last tile stores the
-            // accumulator (all of this CTA's columns) once that tile's P.V has
-            // completed; the other group hands it its (max, sum) through a
-            // ring of kESlots slots and goes on with the next segment.  (It
-            // cannot get more than two segments ahead: its second tile after
-            // this segment needs its P buffer back, i.e. a P.V that waits for
-            // the store to have read the accumulator.)
-            const int gl = g - 1;  // last tile of the segment
-            const int ks = seg_idx % kESlots;
-            const uint32_t ks_phase = (uint32_t)(seg_idx / kESlots) & 1;
-            float *es = eslot + ks * 2 * kH;
-            ++seg_idx;
-            if ((gl & 1) != grp) {
-                es[h] = m_grp;
-                es[kH + h] = l_grp;
-                ptx::mbar_arrive(&bar->ml_full[ks][quad]);
-                continue;
-            }
-            bool w = ptx::mbar_wait(&bar->ml_full[ks][quad], ks_phase, abort_flag);
-            // The row sum relative to the final reference max (this group's:
-            // it ran the last tile).
-            const float m_o = es[h], l_o = es[kH + h];
+            // Segment done: the two groups' (max, sum) give the row sum
+            // relative to the final reference max; then each group stores
+            // half of the accumulator's columns once its last P.V completed.
+            eslot[(grp * 2) * kH + h] = m_grp;
+            eslot[(grp * 2 + 1) * kH + h] = l_grp;
+            ptx::mbar_arrive(&bar->seg[quad]);
+            if (!ptx::mbar_wait(&bar->seg[quad], nseg_done & 1, abort_flag)) { fail(); break; }
+            ++nseg_done;
+            const float m_o = eslot[((grp ^ 1) * 2) * kH + h], l_o = eslot[((grp ^ 1) * 2 + 1) * kH + h];
             const float m_fin = fmaxf(m_grp, m_o);
             const float l_tot = l_grp * exp2f(m_grp - m_fin) + (m_o == -INFINITY ? 0.f : l_o * exp2f(m_o - m_fin));
-            w = w && ptx::mbar_wait(&bar->pv_done[gl & 1], (gl >> 1) & 1, abort_flag);
-            if (!__all_sync(0xffffffffu, w)) { fail(); break; }
+            const int gl = g - 1;  // last tile of the segment
+            if (!__all_sync(0xffffffffu, ptx::mbar_wait(&bar->pv_done[gl & 1], (gl >> 1) & 1, abort_flag))) { fail(); break; }
             ptx::tc_fence_after();
             const int slot = cid + b;
             // The normalised latent average in bfloat16, to o_lat for a whole
             // sequence or to the range's partial slot.  Each warp stages 32
             // rows x 64 bytes at a time in its own block of its group's P
-            // buffer (free: every P.V of the segment has completed), so the global stores
+            // buffer (free: every P.V of the segment has completed, and the
+            // warp's last copy to the peer has read it), so the global stores
             // go out as 64-byte row pieces; the 16-byte pieces of a row are
             // rotated by (row / 2) % 4 against bank conflicts.  Two 32-column
-            // chunks are read from tensor memory per wait; the accumulator is
-            // released right after the last read.
+            // chunks are read from tensor memory per wait.
             uint8_t *wst = smem + kOffP + grp * kPBytes + xblk;
+            if (lane == 0) bulk_wait_read();
+            __syncwarp();
             const int rd_row = lane >> 2, rd_piece = lane & 3;
             bf16 *dst_base = whole ? p.o_lat + (int64_t)b * p.H * kRLat : p.o_part + (int64_t)slot * p.H * kRLat;
             const float inv = 1.f / l_tot;
 #pragma unroll 1
-            for (int c2 = 0; c2 < kOCols; c2 += 64) {
+            for (int c2 = grp * (kOCols / 2); c2 < (grp + 1) * (kOCols / 2); c2 += 64) {
                 uint32_t o[2][32];
                 ptx::tmem_ld32(tmem + lane_off + c2, o[0]);
                 ptx::tmem_ld32(tmem + lane_off + c2 + 32, o[1]);
                 ptx::tmem_ld_wait();
-                if (c2 + 64 == kOCols) {
-                    ptx::tc_fence_before();
-                    ptx::mbar_arrive(&bar->o_empty);
-                }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const int c = c2 + 32 * half;
@@ -840,18 +797,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                 }
             }
-            if (row_ok && !whole && rank == 0) {
+            const bool row_ok = h < p.H;
+            if (row_ok && !whole && rank == 0 && grp == 0) {
                 p.ml_part[((int64_t)slot * p.H + h) * 2] = m_fin;
                 p.ml_part[((int64_t)slot * p.H + h) * 2 + 1] = l_tot;
             }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(&bar->o_empty);
         }
-        // The stores into the peer have landed once the peer has consumed
-        // the last tile sent (it then arrives on this CTA's x_free); after a
-        // failure the bounded wait ends all the same.
-        volatile int never = 0;
-        if (last_sent >= 0) ptx::mbar_wait_cluster(&bar->x_free[grp], (last_sent >> 1) & 1, &never);
     }
 
+    if (warp >= 2 && lane == 0) bulk_wait_all();  // copies into the peer have landed
     ptx::tc_fence_before();
     __syncthreads();
     cluster_sync();  // no CTA leaves while its peer may still touch its shared memory

@@ -229,7 +229,7 @@ struct DecodeSched {
 // r_kv == 512, d_rope == 64.
 struct DecodeTcArgs {
     int B, H, r_kv, d_rope, max_batch, max_seq, n_clusters;
-    const void *q_abs;        // [B, r_kv / 8, H, 8] (head-interleaved 16-byte chunks, see AbsorbArgs)
+    const void *q_abs;        // [B, kQChunks, kQRows, 8] (head-interleaved 16-byte chunks, see kQChunks)
     const void *q_rope;       // [B, H, d_rope]
     const void *lat;          // cache latent rows
     int64_t lat_stride;
@@ -265,19 +265,16 @@ void decode_combine(const DecodeSched &sc, int B, int H, int r_lat, const bf16 *
 // with W_UK,h = rows [128 h, 128 h + 128) of W_UK viewed as [H * 128, r_lat].
 // bfloat16, d_nope == 128, r_lat in {256, 512}.
 // The absorbed decode query of the tensor-core MLA decode, head-interleaved:
-// per sequence, kQChunks 16-byte chunks of 128 head rows (chunk c of head h
-// at ((b * kQChunks + c) * 128 + h) * 16 bytes): chunks 0..63 are q_abs
-// (8 latent columns each), 64..71 the rope query q_rope.  A chunk is a
-// column of 8-row x 16-byte core matrices, so a contiguous run of chunks is
-// a K-major matrix that a bulk copy brings to shared memory and tcgen05.cp
-// moves to tensor memory as is.  Rows of heads >= H are not written.
-constexpr int kQChunks = 72;
+// per sequence, kQChunks 16-byte chunks (8 latent columns each) of kQRows
+// head rows, chunk c of head h at ((b * kQChunks + c) * kQRows + h) * 16
+// bytes, so that a warp's load of one chunk for 32 heads is 512 contiguous
+// bytes.  Rows of heads >= H are not written.
+constexpr int kQChunks = 64;
 constexpr int kQRows = 128;
 
 struct AbsorbArgs {
     int B, H, r_lat, d_nope;
     const void *q_nope;  // [B, H * 128]
-    const void *q_rope;  // [B, H, 64] (interleave only)
     const void *W_UK;
     void *q_abs;         // [B, H, r_lat], or the interleaved layout above (r_lat = 512)
     bool interleave;
@@ -331,7 +328,8 @@ struct PrefillTcArgs {
     int B, S, H, d_nope, d_rope, d_v, max_batch, max_seq;
     int64_t kv_rows;
     const void *q_nope, *q_rope;  // [B*S, H*d_nope], [B*S, H*d_rope]
-    const void *k, *v;            // fp16 workspace [B*kv_rows, H*d_nope], [B*kv_rows, H*d_v]
+    const void *k, *v;            // fp16 workspace [B*kv_rows, Hkv*d_nope], [B*kv_rows, Hkv*d_v]
+    int kv_group = 1;             // query heads per key/value head (Hkv = H / kv_group)
     const void *rope;             // rope cache rows (decoupled, bfloat16)
     int64_t rope_stride;
     void *k_rope16;               // fp16 workspace copy of the rope keys [B*kv_rows, 64]

@@ -175,18 +175,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *m
         : "memory");
 }
 
-// Plain (untiled) bulk copy of `bytes` contiguous global bytes into this
-// CTA's shared memory, completing on `bar`.  Both addresses 16-byte aligned,
-// bytes a multiple of 16.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;
@@ -253,16 +241,6 @@ __device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem,
 }
 
 // Arrive (once) on a CTA-local mbarrier when all prior MMAs of this thread finish.
-// Asynchronous copy of a 128-row x 32-byte matrix from shared memory (a
-// K-major matrix descriptor: rows = tensor-memory lanes) to tensor memory:
-// row i goes to lane i, its 32 bytes to 8 consecutive columns at taddr.
-// Ordered before later tcgen05.mma of the same thread; tcgen05.commit tracks
-// its completion.
-__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 __device__ __forceinline__ void mma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
