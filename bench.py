@@ -403,6 +403,9 @@ def run_ours(args, rank, world, device):
         out["prefill"] = pre
     if args.small:
         out["small_lm_decode"] = run_small_decode(args, device)
+    if args.cca:
+        out["cca_prefill"] = run_cca(args, device, "cca_prefill")
+        out["ccgqa_prefill"] = run_cca(args, device, "ccgqa_prefill")
     if args.mlra:
         out["mlra_decode"] = run_mlra(args, device)
         if world > 1:
@@ -625,6 +628,84 @@ def run_small_decode(args, device):
                          "frac": round(all_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 4), "peak_source": peak_src}}
 
 
+def cca_flops(w):
+    """FLOPs of one CCA / CCGQA forward as the page computes it: the
+    down-projections, both convolutions, causal attention in the latent
+    (exact causal pairs) and the output projection."""
+    T = w.batch * w.seq
+    P = w.q_latent + w.kv_latent
+    proj = 2.0 * T * w.d_model * (P + w.kv_latent) + 2.0 * T * w.q_latent * w.d_model
+    conv = (2.0 * T * P * w.conv_kernel_seq if w.conv_layers >= 1 else 0.0) + \
+           (2.0 * T * P * w.d_h * w.conv_kernel_ch if w.conv_layers >= 2 else 0.0)
+    attn = w.batch * w.n_heads * (w.seq * (w.seq + 1) / 2) * 2 * (2 * w.d_h)
+    return proj + conv + attn, attn
+
+
+def run_cca(args, device, name):
+    """One CCA / CCGQA layer forward (compressed convolutional attention,
+    the layer on the same pages): 4 sequences of 2048 tokens, d_model 2048.
+    Graph-captured; the attention kernel's events in a second graph."""
+    import torch
+    import head_latent_attention_gb300 as mla
+    hbm_peak, tf_peak, tf_sust, peak_src = peaks()
+    w = syn.CCA_WORKLOADS[name]
+    cfg = mla.make_cca_config(w.d_model, w.n_heads, w.n_kv_heads, w.q_latent, w.kv_latent, w.conv_layers,
+                              w.conv_kernel_seq, w.conv_kernel_ch, w.qk_mean, w.value_shift, w.rope_base,
+                              w.key_temp, w.seq)
+    lay = mla.CcaLayer(cfg, {k: to_dev(s, device) for k, (s, _) in syn.cca_weights(w).items()}, w.batch,
+                       device=device)
+    xs, _ = syn.cca_activations(w, w.batch * w.seq)
+    x = to_dev(xs, device).view(w.batch, w.seq, w.d_model)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        st = mla.mla_cca_forward(lay.h, lay.w, x, w.batch, w.seq, y, lay.ws)
+        if st != mla.MLA_OK:
+            raise mla.MlaError(st, "mla_cca_forward")
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    kb, ke = timing_events(1)[0]
+    mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, kb, ke)
+    g_k = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_k):
+        step()
+    mla.mla_set_profile_events(mla.MLA_PROFILE_PREFILL_ATTENTION, None, None)
+    for _ in range(3):
+        g.replay()
+        g_k.replay()
+    torch.cuda.synchronize()
+    K = max(args.prefill_steps, 1)
+    ev = timing_events(K)
+    kern_ms = []
+    for i in range(K):
+        ev[i][0].record(stream)
+        g.replay()
+        ev[i][1].record(stream)
+        g_k.replay()
+        ke.synchronize()
+        kern_ms.append(kb.elapsed_time(ke))
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms, kms = sum(step_ms) / K, sum(kern_ms) / K
+    total, attn = cca_flops(w)
+    del lay, g, g_k
+    torch.cuda.empty_cache()
+    return {"workload": name, "batch": w.batch, "seq": w.seq, "heads": w.n_heads, "kv_heads": w.n_kv_heads,
+            "d_h": w.d_h, "steps": K, "ms_per_step": round(ms, 4), "step_ms": spread(step_ms),
+            "tflops": round(total / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "flops_per_step": total,
+            "frac_of_bf16_peak": round(total / (ms * 1e-3) / 1e12 / tf_peak, 4),
+            "roofline": {"bound": "tensor", "kernel": "causal flash attention in the latent",
+                         "achieved": round(attn / (kms * 1e-3) / 1e12, 2), "peak": tf_peak, "unit": "TFLOP/s",
+                         "frac": round(attn / (kms * 1e-3) / 1e12 / tf_peak, 4), "peak_source": peak_src,
+                         "kernel_ms": round(kms, 4)}}
+
+
 def run_mlra_tp(args, rank, world, device):
     """MLRA decode layer step with latent sub-head tensor parallelism across
     the ranks (mlra_attn module docstring: each device loads 1/L of the KV
@@ -785,6 +866,7 @@ def main():
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--no-mlra", dest="mlra", action="store_false")
     ap.add_argument("--no-small", dest="small", action="store_false")
+    ap.add_argument("--no-cca", dest="cca", action="store_false")
     ap.add_argument("--mlra-steps", type=int, default=5)
     ap.add_argument("--mlra-only", action="store_true", help="time only the MLRA decode layer (profiling aid)")
     ap.add_argument("--no-cpu-baseline", action="store_true")

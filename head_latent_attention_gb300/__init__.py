@@ -38,7 +38,9 @@ TORCH_DTYPE = {DTYPE_F32: torch.float32, DTYPE_BF16: torch.bfloat16}
 EXPORTS = ("mla_check_config", "mla_create", "mla_destroy", "mla_workspace_size",
            "mla_project_latent", "mla_prefill", "mla_decode", "mla_out_proj",
            "mla_get_device_status", "mla_status_string", "mla_launch_count",
-           "mla_set_profile_events", "mla_out_proj_static", "mla_set_wait_limit", "mla_create_shard")
+           "mla_set_profile_events", "mla_out_proj_static", "mla_set_wait_limit", "mla_create_shard",
+           "mla_cca_check_config", "mla_cca_create", "mla_cca_destroy", "mla_cca_workspace_size",
+           "mla_cca_forward", "mla_cca_get_device_status")
 MLA_PROFILE_DECODE_ATTENTION = 0
 MLA_PROFILE_PREFILL_ATTENTION = 1
 MLA_PROFILE_DECODE_CALL = 2
@@ -60,6 +62,17 @@ class MlaWeights(ctypes.Structure):
 class MlaCache(ctypes.Structure):
     _fields_ = [("lat", ctypes.c_void_p), ("rope", ctypes.c_void_p),
                 ("lat_stride", ctypes.c_int64), ("rope_stride", ctypes.c_int64)]
+
+
+class MlaCcaConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("d_model", "n_heads", "n_kv_heads", "q_latent", "kv_latent",
+                                              "conv_layers", "conv_kernel_seq", "conv_kernel_ch", "qk_mean",
+                                              "value_shift")] + \
+               [("rope_base", ctypes.c_double), ("key_temp", ctypes.c_double), ("max_seq", ctypes.c_int)]
+
+
+class MlaCcaWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W_QK", "W_V1", "W_V2", "W_V", "conv0", "conv1", "W_O")]
 
 
 class MlaError(RuntimeError):
@@ -97,6 +110,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mla_launch_count": (ctypes.c_uint64, []),
         "mla_set_profile_events": (I, [I, P, P]),
         "mla_set_wait_limit": (I, [L]),
+        "mla_cca_check_config": (I, [P]),
+        "mla_cca_create": (I, [P, ctypes.POINTER(P)]),
+        "mla_cca_destroy": (None, [P]),
+        "mla_cca_workspace_size": (S, [P, I, I]),
+        "mla_cca_forward": (I, [P, P, P, I, I, P, P, S, P]),
+        "mla_cca_get_device_status": (I, [P, P, P, ctypes.POINTER(ctypes.c_uint32)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -366,3 +385,89 @@ class MlaLayer:
 
     def device_status(self, stream=None):
         return mla_get_device_status(self.h, self.ws, stream)
+
+
+# ---------------------------------------------------------------------------
+# Compressed convolutional attention (CCA / CCGQA)
+# ---------------------------------------------------------------------------
+
+def make_cca_config(d_model: int, n_heads: int, n_kv_heads: int, q_latent: int, kv_latent: int,
+                    conv_layers: int = 2, conv_kernel_seq: int = 4, conv_kernel_ch: int = 3, qk_mean: bool = True,
+                    value_shift: bool = True, rope_base: float = 10000.0, key_temp: float = 0.0,
+                    max_seq: int = 4096) -> MlaCcaConfig:
+    return MlaCcaConfig(d_model, n_heads, n_kv_heads, q_latent, kv_latent, conv_layers, conv_kernel_seq,
+                        conv_kernel_ch, int(qk_mean), int(value_shift), float(rope_base), float(key_temp), max_seq)
+
+
+class CcaHandle:
+    """Owner of an ``mla_cca_handle*``."""
+
+    def __init__(self, ptr: ctypes.c_void_p, cfg: MlaCcaConfig):
+        self.ptr = ptr
+        self.cfg = cfg
+
+    def __del__(self):
+        if getattr(self, "ptr", None) and _lib is not None:
+            _lib.mla_cca_destroy(self.ptr)
+            self.ptr = None
+
+
+def mla_cca_check_config(cfg: MlaCcaConfig) -> int:
+    return load_library().mla_cca_check_config(ctypes.byref(cfg))
+
+
+def mla_cca_create(cfg: MlaCcaConfig) -> CcaHandle:
+    out = ctypes.c_void_p()
+    _check(load_library().mla_cca_create(ctypes.byref(cfg), ctypes.byref(out)), "mla_cca_create")
+    return CcaHandle(out, cfg)
+
+
+def mla_cca_workspace_size(h: CcaHandle, B: int, S: int) -> int:
+    return load_library().mla_cca_workspace_size(h.ptr, B, S)
+
+
+def make_cca_weights(w: Dict[str, torch.Tensor]) -> MlaCcaWeights:
+    mw = MlaCcaWeights()
+    for name, _ in MlaCcaWeights._fields_:
+        t = w.get(name)
+        setattr(mw, name, t.data_ptr() if t is not None else None)
+    mw._keep = dict(w)
+    return mw
+
+
+def mla_cca_forward(h: CcaHandle, w: MlaCcaWeights, x: torch.Tensor, B: int, S: int, y: torch.Tensor,
+                    ws: torch.Tensor, stream=None) -> int:
+    c = h.cfg
+    for name, t in (("x", x), ("y", y)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.numel() != B * S * c.d_model:
+            raise ValueError(f"{name} must be a contiguous bfloat16 [B, S, d_model] tensor")
+    return load_library().mla_cca_forward(h.ptr, ctypes.byref(w), _ptr(x), B, S, _ptr(y), _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(stream))
+
+
+def mla_cca_get_device_status(h: CcaHandle, ws: Optional[torch.Tensor], stream=None):
+    bits = ctypes.c_uint32(0)
+    st = load_library().mla_cca_get_device_status(h.ptr, _ptr(ws), _stream(stream), ctypes.byref(bits))
+    return st, bits.value
+
+
+class CcaLayer:
+    """A CCA / CCGQA layer: handle, weights (bfloat16 device tensors named as
+    in ``mla_cca_weights``) and a workspace for up to max_batch sequences of
+    the config's max_seq tokens."""
+
+    def __init__(self, cfg: MlaCcaConfig, weights: Dict[str, torch.Tensor], max_batch: int, device: str = "cuda"):
+        self.cfg = cfg
+        self.h = mla_cca_create(cfg)
+        self.w = make_cca_weights(weights)
+        self.ws = torch.zeros(mla_cca_workspace_size(self.h, max_batch, cfg.max_seq), dtype=torch.uint8,
+                              device=device)
+
+    def forward(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        B, S = x.shape[0], x.shape[1]
+        y = torch.empty_like(x)
+        _check(mla_cca_forward(self.h, self.w, x, B, S, y, self.ws, stream), "mla_cca_forward")
+        return y
+
+    def device_status(self, stream=None):
+        return mla_cca_get_device_status(self.h, self.ws, stream)

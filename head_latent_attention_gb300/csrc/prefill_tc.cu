@@ -53,6 +53,7 @@ struct PCfg {
 
 struct PreTcParams {
     int B, S, H, max_seq, d_nope;
+    int kv_group;              // query heads per key/value head (head h reads key/value head h / kv_group)
     int64_t kv_rows;
     bool rope;                 // decoupled: last q/k atom from q_rope / rope keys
     const int32_t *start_pos;  // device [B]
@@ -154,10 +155,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *dst = sKV + st * C::kStageBytes;
                 const int krow = (int)(b * p.kv_rows) + t * kBN;
                 for (int a = 0; a < nk_nope; ++a)
-                    ptx::tma_load_2d(dst + a * C::kAtom, &tK, &bar->kv_full[st], h * p.d_nope + a * 64, krow);
+                    ptx::tma_load_2d(dst + a * C::kAtom, &tK, &bar->kv_full[st], (h / p.kv_group) * p.d_nope + a * 64,
+                                     krow);
                 if (p.rope) ptx::tma_load_2d(dst + (NQ - 1) * C::kAtom, &tKR, &bar->kv_full[st], 0, krow);
                 for (int a = 0; a < NV; ++a)
-                    ptx::tma_load_2d(dst + (NQ + a) * C::kAtom, &tV, &bar->kv_full[st], h * p.d_v + a * 64, krow);
+                    ptx::tma_load_2d(dst + (NQ + a) * C::kAtom, &tV, &bar->kv_full[st], (h / p.kv_group) * p.d_v + a * 64,
+                                     krow);
                 pending[st] = (int)ph;
             }
             if (!ok) *abort_flag = 1;
@@ -454,12 +457,15 @@ template <int NQ, int NV>
 cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
 {
     using C = PCfg<NQ, NV>;
+    const int kvg = a.kv_group > 0 ? a.kv_group : 1;
+    if (a.H % kvg) return cudaErrorInvalidValue;
+    const int Hkv = a.H / kvg;
     CUtensorMap tq, tqr, tk, tkr, tv;
     const int64_t T = (int64_t)a.B * a.S;
     const int64_t KR = (int64_t)a.B * a.kv_rows;
     if (!make_tmap_bf16(&tq, a.q_nope, T, (int64_t)a.H * a.d_nope, (int64_t)a.H * a.d_nope, 64, kQ) ||
-        !make_tmap_bf16(&tk, a.k, KR, (int64_t)a.H * a.d_nope, (int64_t)a.H * a.d_nope, 64, kBN) ||
-        !make_tmap_bf16(&tv, a.v, KR, (int64_t)a.H * a.d_v, (int64_t)a.H * a.d_v, 64, kBN))
+        !make_tmap_bf16(&tk, a.k, KR, (int64_t)Hkv * a.d_nope, (int64_t)Hkv * a.d_nope, 64, kBN) ||
+        !make_tmap_bf16(&tv, a.v, KR, (int64_t)Hkv * a.d_v, (int64_t)Hkv * a.d_v, 64, kBN))
         return cudaErrorInvalidValue;
     if (a.d_rope) {
         if (!make_tmap_bf16(&tqr, a.q_rope, T, (int64_t)a.H * 64, (int64_t)a.H * 64, 64, kQ) ||
@@ -480,6 +486,7 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs &a, cudaStream_t s)
     PreTcParams p;
     p.B = a.B; p.S = a.S; p.H = a.H; p.max_seq = a.max_seq; p.d_nope = a.d_nope;
     p.kv_rows = a.kv_rows;
+    p.kv_group = kvg;
     p.rope = a.d_rope != 0;
     p.start_pos = a.start_pos;
     p.scale_log2 = a.scale_log2;

@@ -263,6 +263,80 @@ mla_status mla_get_device_status(mla_handle *h, void *ws, void *stream, uint32_t
 mla_status mla_out_proj_static(mla_handle *h, const mla_weights *w, const void *o, int64_t T,
                                void *y, void *stream);
 
+/* ---- Compressed convolutional attention (CCA) and its grouped form ----
+ *
+ * "frankenstein-transformer", latent/cca_attn.py (CCAAttention,
+ * CCGQAAttention): q, k and v are down-projected into a compressed latent and
+ * the whole attention runs there; only the output projection returns to
+ * d_model.  Per token, in the page's order:
+ *  - qk = W_QK x (query latent q_latent = n_heads * d_h, key latent
+ *    kv_latent = n_kv_heads * d_h, packed);
+ *  - causal convolutions over the sequence on the packed qk (conv_layers of
+ *    them): depth-wise with conv_kernel_seq taps, then grouped (one group of
+ *    d_h channels per head) with conv_kernel_ch taps, both left-padded;
+ *  - q-k-mean (qk_mean != 0): query head h adds (q_pre,h + k_pre,g(h)) / 2,
+ *    key head g the average of that over its query heads (g(h) = h / (n_heads
+ *    / n_kv_heads));
+ *  - values v = W_V x, or with value_shift != 0 [W_V1 x_t | W_V2 x_{t-1}]
+ *    (x_{-1} = 0), the two halves concatenated before the split into heads;
+ *  - q and k L2-normalised to norm sqrt(d_h) (norms clamped at 1e-6), k
+ *    times exp(key_temp);
+ *  - RoPE with half-split pairs at positions 0..S-1 in the latent;
+ *  - causal softmax attention, scale 1/sqrt(d_h), query head h reading
+ *    key/value head g(h); y = W_O o.
+ * CCA is the case n_kv_heads == n_heads.  bfloat16 only (tensor cores for the
+ * projections and the attention, CUDA cores for the convolutions and the
+ * normalisation); d_h in {64, 128}. */
+typedef struct {
+    int d_model, n_heads, n_kv_heads, q_latent, kv_latent;
+    int conv_layers;      /* 0, 1 or 2 */
+    int conv_kernel_seq;  /* depth-wise sequence convolution taps (1..8) */
+    int conv_kernel_ch;   /* grouped channel convolution taps (1..4) */
+    int qk_mean, value_shift;
+    double rope_base;
+    double key_temp;      /* the key temperature beta (its exponential scales k) */
+    int max_seq;          /* longest sequence a forward call may take */
+} mla_cca_config;
+
+/* Device bfloat16 weights, nn.Linear layout [out, in]: W_QK [q_latent +
+ * kv_latent, d_model]; value_shift: W_V1, W_V2 [kv_latent / 2, d_model],
+ * otherwise W_V [kv_latent, d_model]; conv0 [q_latent + kv_latent,
+ * conv_kernel_seq] (conv_layers >= 1); conv1 [q_latent + kv_latent, d_h,
+ * conv_kernel_ch] (conv_layers == 2); W_O [d_model, q_latent].  Unused NULL. */
+typedef struct {
+    const void *W_QK, *W_V1, *W_V2, *W_V, *conv0, *conv1, *W_O;
+} mla_cca_weights;
+
+typedef struct mla_cca_handle mla_cca_handle;
+
+/* Checks of the page's constructors: positive sizes; n_kv_heads | n_heads;
+ * n_heads | q_latent, n_kv_heads | kv_latent, equal and even d_h;
+ * kv_latent <= q_latent; conv_layers in {0, 1, 2}; value_shift needs even
+ * n_kv_heads and kv_latent.  MLA_ERR_UNSUPPORTED for shapes the kernels do
+ * not run (d_h not 64 or 128; latent widths, or the value halves, not
+ * multiples of 64; more taps than the limits above). */
+mla_status mla_cca_check_config(const mla_cca_config *cfg);
+
+/* Handle on the current device: validates cfg and builds the float32 RoPE
+ * table for positions [0, max_seq) (angles in double precision). */
+mla_status mla_cca_create(const mla_cca_config *cfg, mla_cca_handle **out);
+void mla_cca_destroy(mla_cca_handle *h);
+
+/* Workspace bytes of a forward call on B sequences of S tokens (0 on bad
+ * arguments). */
+size_t mla_cca_workspace_size(const mla_cca_handle *h, int B, int S);
+
+/* y = CCA(x) for B sequences of S tokens each (causal, positions from 0):
+ * x [B, S, d_model], y [B, S, d_model], device bfloat16, 16-byte aligned.
+ * S <= max_seq.  Scratch from ws (status word in its first 256 bytes, as for
+ * the MLA calls); keys and values beyond fp16's range are saturated and
+ * flagged (status bit 16).  Asynchronous on stream. */
+mla_status mla_cca_forward(mla_cca_handle *h, const mla_cca_weights *w, const void *x, int B, int S, void *y,
+                           void *ws, size_t ws_bytes, void *stream);
+
+/* As mla_get_device_status, for a CCA workspace. */
+mla_status mla_cca_get_device_status(mla_cca_handle *h, void *ws, void *stream, uint32_t *bits);
+
 /* Static English text for a status code. */
 const char *mla_status_string(mla_status s);
 

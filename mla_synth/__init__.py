@@ -227,3 +227,91 @@ def stage_inputs(w: Workload, name: str, shape: Sequence[int]) -> Tuple[np.ndarr
     """A stage-level input (``q_nope``, ``q_rope`` or ``o``) ~ N(0, 1)."""
     return store(normal(w.seed, name, shape), w.dtype)
 
+
+
+# ---------------------------------------------------------------------------
+# Compressed convolutional attention (CCA) and its grouped form (CCGQA)
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class CcaWorkload:
+    """Shape of a CCA / CCGQA layer and its batch.  CCA is the case
+    n_kv_heads == n_heads (q_latent == kv_latent)."""
+
+    name: str
+    d_model: int
+    n_heads: int          # query heads
+    n_kv_heads: int       # key/value heads (groups of n_heads / n_kv_heads)
+    q_latent: int         # query latent width (n_heads * d_h)
+    kv_latent: int        # key/value latent width (n_kv_heads * d_h)
+    batch: int
+    seq: int
+    conv_layers: int = 2
+    conv_kernel_seq: int = 4
+    conv_kernel_ch: int = 3
+    qk_mean: bool = True
+    value_shift: bool = True
+    key_temp: float = 0.0  # the learnable key temperature beta (the page initialises it to 0)
+    rope_base: float = 10000.0
+    seed: int = 0
+
+    @property
+    def d_h(self) -> int:
+        return self.q_latent // self.n_heads
+
+    def replace(self, **kw) -> "CcaWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+CCA_TENSOR_IDS: Dict[str, int] = {"W_QK": 20, "W_V1": 21, "W_V2": 22, "W_V": 23, "conv0": 24, "conv1": 25,
+                                  "W_O": 26, "x": 27}
+
+# CCA at compression 4 (d_model 2048 -> latent 512, 8 heads of 64) and CCGQA
+# with the page's default rates (query latent E/2 in 16 heads, key/value
+# latent E/8 in 4 heads, d_h 64 for both).
+CCA_WORKLOADS: Dict[str, CcaWorkload] = {
+    "cca_prefill": CcaWorkload("cca_prefill", d_model=2048, n_heads=8, n_kv_heads=8, q_latent=512,
+                               kv_latent=512, batch=4, seq=2048),
+    "ccgqa_prefill": CcaWorkload("ccgqa_prefill", d_model=2048, n_heads=16, n_kv_heads=4, q_latent=1024,
+                                 kv_latent=256, batch=4, seq=2048),
+}
+
+
+def cca_weight_shapes(w: CcaWorkload) -> Dict[str, Tuple[int, ...]]:
+    """nn.Linear layout [out, in]; conv0 [channels, k_seq] (depth-wise),
+    conv1 [channels, d_h, k_ch] (one group of d_h channels per head)."""
+    P = w.q_latent + w.kv_latent
+    out = {"W_QK": (P, w.d_model)}
+    if w.value_shift:
+        out["W_V1"] = (w.kv_latent // 2, w.d_model)
+        out["W_V2"] = (w.kv_latent // 2, w.d_model)
+    else:
+        out["W_V"] = (w.kv_latent, w.d_model)
+    if w.conv_layers >= 1:
+        out["conv0"] = (P, w.conv_kernel_seq)
+    if w.conv_layers >= 2:
+        out["conv1"] = (P, w.d_h, w.conv_kernel_ch)
+    out["W_O"] = (w.d_model, w.q_latent)
+    return out
+
+
+def _cca_normal(w: CcaWorkload, name: str, shape, std: float = 1.0) -> np.ndarray:
+    ss = np.random.SeedSequence([int(w.seed), CCA_TENSOR_IDS[name]])
+    a = np.random.Generator(np.random.PCG64(ss)).standard_normal(size=tuple(shape), dtype=np.float64)
+    return a * std if std != 1.0 else a
+
+
+def cca_weights(w: CcaWorkload) -> Dict[str, Tuple[np.ndarray, np.ndarray]]:
+    """All CCA weights as ``name -> (stored bf16 bits, exact)``; std
+    1/sqrt(fan_in) (a convolution's fan-in is its taps times its input
+    channels per group)."""
+    out = {}
+    for name, shape in cca_weight_shapes(w).items():
+        fan_in = shape[-1] if name != "conv1" else shape[1] * shape[2]
+        out[name] = store(_cca_normal(w, name, shape, fan_in ** -0.5), DTYPE_BF16)
+    return out
+
+
+def cca_activations(w: CcaWorkload, n_tokens: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Layer input x [n_tokens, d_model] ~ N(0, 1), bf16."""
+    return store(_cca_normal(w, "x", (n_tokens, w.d_model)), DTYPE_BF16)
