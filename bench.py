@@ -37,6 +37,7 @@ DECODE = syn.WORKLOADS["dsv2_decode"]
 PREFILL = syn.WORKLOADS["dsv2_prefill"]
 MLRA = syn.WORKLOADS["mlra_decode"]
 L2_FLUSH_BYTES = 512 << 20
+NOMINAL_HBM_GBS = 7900.0  # the HBM3e bandwidth NVIDIA quotes for GB300 (context beside the measured peak)
 # DRAM bytes (read + write) of one decode attention launch on this workload,
 # from an ncu capture of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum); None whenever the kernel changes until it is
@@ -386,7 +387,8 @@ def run_ours(args, rank, world, device):
                      "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "peak_source": peak_src,
                      "kernel_ms": round(kms, 5), "traffic": DECODE_TRAFFIC_BYTES,
-                     "traffic_unit": "bytes per launch"},
+                     "traffic_unit": "bytes per launch",
+                     "nominal": {"peak": NOMINAL_HBM_GBS, "frac": round(achieved / NOMINAL_HBM_GBS, 4)}},
         "decode_call": {"what": "one mla_decode call: absorption, split-KV attention, merge, W_UV",
                         "ms": round(cms, 5), "bytes": call_bytes,
                         "bytes_are": "cache rows read + W_UK + W_UV + q_nope + q_rope read + o written",

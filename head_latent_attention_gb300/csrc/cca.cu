@@ -3,25 +3,28 @@
 // "frankenstein-transformer", latent/cca_attn.py (CCAAttention,
 // CCGQAAttention): attention runs inside a compressed latent.  The launches
 // of one forward call, on B sequences of S tokens (T = B S rows):
-//   1. the down-projections x -> [qk | v1 | W_V2 x] (tcgen05 GEMMs writing
-//      column slices of one bf16 buffer);
-//   2. cca_conv0_v_kernel: the depth-wise causal convolution of qk (fp32
-//      out) and the values (value-shift reads the previous row's W_V2 x),
-//      as fp16;
-//   3. cca_qk_kernel: per (row tile, head) the grouped causal convolution,
+//   1. the down-projections x -> [qk | v1 | W_V2 x] (one grouped tcgen05
+//      GEMM writing column slices of one bf16 buffer);
+//   2. cca_v_kernel: the values as fp16 (value-shift reads the previous
+//      row's W_V2 x);
+//   3. cca_qk_tc_kernel: per (128 token rows, head) the depth-wise causal
+//      convolution, the grouped causal convolution on the tensor cores,
 //      q-k-mean, L2 normalisation, key temperature and half-split RoPE,
 //      writing the query (bf16) and key (fp16) operands of the attention;
 //   4. the causal flash prefill kernel (tcgen05) with grouped key/value
 //      heads;
 //   5. the output projection GEMM.
-// The convolutions and the normalisation are small (a few hundred MACs per
-// output) and run on the CUDA cores; the contractions on the tensor cores.
+// The depth-wise convolution and the normalisation run on the CUDA cores; the
+// grouped convolution (K = d_h x taps per output) and the projections on the
+// tensor cores.
 #include <math.h>
 #include <string.h>
 
 #include <algorithm>
 #include <new>
 #include <vector>
+
+#include <cudaTypedefs.h>
 
 #include "mla_internal.cuh"
 #include "ptx.cuh"
@@ -34,17 +37,20 @@ struct mla_cca_handle {
 };
 
 namespace mla {
+
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols, int64_t ld, int box_cols,
+                    int box_rows);
+
 namespace {
 
 constexpr double kLog2eCca = 1.4426950408889634;
 constexpr int kMaxTapsSeq = 8;
 constexpr int kMaxTapsCh = 4;
-constexpr int kRowsPerBlock = 32;  // token rows per cca_qk_kernel block
 
 size_t cca_round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct CcaWs {
-    size_t start_pos, pre, c0, q, k, v, o, split, end;
+    size_t start_pos, pre, q, k, v, o, w1img, split, end;
 };
 
 // x [M, K] W^T into columns [col, col + N) of out (row stride ldc).
@@ -61,222 +67,455 @@ GemmArgs cca_linear(const void *x, int64_t M, int K, const void *W, int N, void 
     return g;
 }
 
-// Split-K partial sums the largest of the call's GEMMs needs (few tokens).
+// The down-projections as one grouped GEMM over x's rows: output columns
+// [W_QK x | W_V1 x | W_V2 x] (or [W_QK x | W_V x]) of one [T, P + Lkv] buffer.
+GemmArgs cca_down_proj(const mla_cca_config &c, const void *x, int64_t T, const mla_cca_weights *w, void *pre,
+                       uint32_t *status)
+{
+    const int P = c.q_latent + c.kv_latent, Lkv = c.kv_latent, Wp = P + Lkv, K = c.d_model;
+    GemmArgs g = cca_linear(x, T, K, nullptr, P, pre, Wp, 0, status);
+    auto seg = [&](const void *W, int N, int col) {
+        GemmSegment s;
+        s.B = Mat2D{W, N, K, K};
+        s.epi = g.epi;
+        s.epi.out = (char *)pre + (size_t)col * 2;
+        s.N = N;
+        return s;
+    };
+    g.seg[0] = seg(w ? w->W_QK : nullptr, P, 0);
+    if (c.value_shift) {
+        g.nseg = 3;
+        g.seg[1] = seg(w ? w->W_V1 : nullptr, Lkv / 2, P);
+        g.seg[2] = seg(w ? w->W_V2 : nullptr, Lkv / 2, P + Lkv / 2);
+    } else {
+        g.nseg = 2;
+        g.seg[1] = seg(w ? w->W_V : nullptr, Lkv, P);
+    }
+    return g;
+}
+
+// Split-K partial sums the larger of the call's two GEMMs needs (few tokens).
 size_t cca_split_bytes(const mla_cca_config &c, int64_t T, int num_sms)
 {
-    const int P = c.q_latent + c.kv_latent;
-    const int n[4] = {P, c.kv_latent / 2, c.kv_latent, c.d_model};
-    const int k[4] = {c.d_model, c.d_model, c.d_model, c.q_latent};
-    size_t most = 0;
-    for (int i = 0; i < 4; ++i) {
-        GemmArgs g = cca_linear(nullptr, T, k[i], nullptr, n[i], nullptr, n[i], 0, nullptr);
-        most = std::max(most, gemm_tc_workspace(g, num_sms));
-    }
-    return most;
+    const GemmArgs down = cca_down_proj(c, nullptr, T, nullptr, nullptr, nullptr);
+    const GemmArgs out = cca_linear(nullptr, T, c.q_latent, nullptr, c.d_model, nullptr, c.d_model, 0, nullptr);
+    return std::max(gemm_tc_workspace(down, num_sms), gemm_tc_workspace(out, num_sms));
 }
 
 // Scratch of one forward call: the projections [T, P + Lkv] (bf16), the
-// depth-wise convolution [T, P] (fp32), the attention operands q (bf16), k
-// and v (fp16), its output o (bf16) and the GEMMs' split-K partials.
+// attention operands q (bf16), k and v (fp16), its output o (bf16), the
+// channel convolution's operand image (fp16, heads x taps x d_h x d_h) and
+// the GEMMs' split-K partials.
 CcaWs cca_ws(const mla_cca_config &c, int B, int S, int num_sms)
 {
     const size_t T = (size_t)B * S, P = (size_t)c.q_latent + c.kv_latent;
     CcaWs w;
     w.start_pos = kWsHeader;
     w.pre = cca_round_up(w.start_pos + (size_t)B * 4, 256);
-    w.c0 = cca_round_up(w.pre + T * (P + c.kv_latent) * 2, 256);
-    w.q = cca_round_up(w.c0 + (c.conv_layers >= 1 ? T * P * 4 : 0), 256);
+    w.q = cca_round_up(w.pre + T * (P + c.kv_latent) * 2, 256);
     w.k = cca_round_up(w.q + T * c.q_latent * 2, 256);
     w.v = cca_round_up(w.k + T * c.kv_latent * 2, 256);
     w.o = cca_round_up(w.v + T * c.kv_latent * 2, 256);
-    w.split = cca_round_up(w.o + T * c.q_latent * 2, 256);
+    const size_t dh = (size_t)c.q_latent / c.n_heads;
+    const size_t k1 = c.conv_layers >= 2 ? (size_t)c.conv_kernel_ch : 1;
+    w.w1img = cca_round_up(w.o + T * c.q_latent * 2, 256);
+    w.split = cca_round_up(w.w1img + (size_t)(c.n_heads + c.n_kv_heads) * k1 * dh * dh * 2, 256);
     w.end = cca_round_up(w.split + cca_split_bytes(c, (int64_t)T, num_sms), 256);
     return w;
 }
 
-__device__ __forceinline__ __half to_f16_sat(float v, bool &over)
-{
-    over |= ptx::beyond_f16(v);
-    return __float2half_rn(fminf(fmaxf(v, -65504.f), 65504.f));
-}
-
-// Columns [0, P) of each row: the depth-wise causal convolution of the packed
-// qk (taps k0, left zero padding within the row's sequence), to fp32.
-// Columns [P, P + Lkv): the values to fp16; with value-shift the second half
-// is the previous row's W_V2 x (zero for a sequence's first token).  With no
-// convolution only the value columns are run (col0 = P).
+// The values to fp16: columns [P, P + Lkv) of each row, eight channels per
+// thread.  With value-shift the second half is the previous row's W_V2 x
+// (zero for a sequence's first token).
 __global__ void __launch_bounds__(256)
-    cca_conv0_v_kernel(const bf16 *__restrict__ pre, int64_t T, int S, int P, int Lkv, int col0, int k0,
-                       const bf16 *__restrict__ w0, float *__restrict__ c0, __half *__restrict__ v, int value_shift,
-                       uint32_t *status)
+    cca_v_kernel(const bf16 *__restrict__ pre, int64_t T, int S, int P, int Lkv, __half *__restrict__ v,
+                 int value_shift, uint32_t *status)
 {
     ptx::pdl_trigger();
     ptx::pdl_wait();
-    const int Wp = P + Lkv, ncols = Wp - col0;
+    const int nc = Lkv / 8, Wp = P + Lkv;
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= T * ncols) return;
-    const int64_t r = i / ncols;
-    const int c = (int)(i % ncols) + col0;
-    const int t = (int)(r % S);
-    if (c < P) {
-        float acc = 0.f;
-        for (int j = 0; j < k0; ++j) {
-            const int back = k0 - 1 - j;  // row r - back feeds tap j
-            if (t >= back) acc += __bfloat162float(w0[(int64_t)c * k0 + j]) * __bfloat162float(pre[(r - back) * Wp + c]);
-        }
-        c0[r * P + c] = acc;
-        return;
-    }
-    const int cv = c - P;
-    float val;
-    if (value_shift && cv >= Lkv / 2) val = t >= 1 ? __bfloat162float(pre[(r - 1) * Wp + c]) : 0.f;
-    else val = __bfloat162float(pre[r * Wp + c]);
+    if (i >= T * nc) return;
+    const int64_t r = i / nc;
+    const int c = (int)(i % nc) * 8;
+    const bool shifted = value_shift && c >= Lkv / 2;
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (!shifted || r % S >= 1) w = *reinterpret_cast<const uint4 *>(pre + (r - (shifted ? 1 : 0)) * Wp + P + c);
     bool over = false;
-    v[r * Lkv + cv] = to_f16_sat(val, over);
+    uint4 o;
+    o.x = ptx::bf16x2_to_f16x2(w.x, over);
+    o.y = ptx::bf16x2_to_f16x2(w.y, over);
+    o.z = ptx::bf16x2_to_f16x2(w.z, over);
+    o.w = ptx::bf16x2_to_f16x2(w.w, over);
+    *reinterpret_cast<uint4 *>(v + r * Lkv + c) = o;
     if (over && status) atomicOr(status, kStatusF16Range);
 }
 
 struct CcaQkParams {
-    const bf16 *pre;     // [T, P + Lkv] packed projections
-    const float *c0;     // [T, P] after the depth-wise convolution, or null (none)
-    const bf16 *w1;      // [P, d_h, k1] grouped convolution, or null
+    const bf16 *pre;      // [T, P + Lkv] packed projections
+    const bf16 *w0;       // [P, k0] depth-wise convolution, or null (none)
+    const uint8_t *w1img; // per head, per tap: the channel convolution's operand image (cca_w1_image_kernel)
     int64_t T;
-    int S, P, Lkv, Lq, Hq, gs, k1, conv_layers, qk_mean;
-    float k_scale;       // exp(key temperature)
-    const float2 *rope;  // [max_seq, d_h / 2]
-    bf16 *q;             // [T, Lq]
-    __half *k;           // [T, Lkv]
+    int S, P, Lkv, Lq, Hq, gs, k0, k1, slots, qk_mean;
+    float k_scale;        // exp(key temperature)
+    const float2 *rope;   // [max_seq, d_h / 2]
+    bf16 *q;              // [T, Lq]
+    __half *k;            // [T, Lkv]
     uint32_t *status;
 };
 
-// One block per (kRowsPerBlock token rows, head g): query heads g < Hq, key
-// heads after them.  The head's grouped-convolution weights are staged once
-// in shared memory, transposed to [tap][in][out] so that the threads of a
-// warp (consecutive output channels) read consecutive words.  Thread (o, y)
-// produces channel o of rows y, y + kRowThreads, ...: the grouped causal
-// convolution of the depth-wise output (one group of d_h channels per head),
-// q-k-mean, the L2 normalisation over the head's channels to norm sqrt(d_h)
-// (keys times exp(beta)), and RoPE with half-split pairs (o, o + d_h / 2) at
-// the row's position.
-constexpr int kRowThreads = 4;                            // thread rows per block
-constexpr int kRowsPerThread = kRowsPerBlock / kRowThreads;
+// One CTA per (128 token rows, head g): query heads g < Hq, key heads after
+// them; thread m owns row r0 + m.  The grouped causal convolution (one
+// group of d_h channels per head) is a contraction over (tap, input
+// channel):
+//   u[r, o] = sum_j sum_i a[r - (k1 - 1 - j), i] W1[g d_h + o, i, j],
+// where a is the depth-wise causal convolution of the packed projections and
+// rows before the sequence's first token are zero.  The steps:
+//   - TMA copies the head's projection tile (the 128 rows, the channel
+//     convolution's halo and the depth-wise one's, zero outside [0, T)) and a
+//     bulk copy brings the tap weights W_j[o, i] (fp16, prepared once per
+//     call as the MMA operand image);
+//   - the threads compute a once per row from the tile and write each tap's
+//     row-shifted copy A_j[n] = a[r0 + n - (k1 - 1 - j)] (fp16, zero where
+//     the shift crosses the sequence start);
+//   - one thread issues k1 * d_h / 16 MMAs (M = 128 rows, N = d_h output
+//     channels, K = 16) accumulating into tensor memory; taps that do not fit
+//     in shared memory at once run in passes;
+//   - thread m reads row m back from tensor-memory lane m and applies
+//     q-k-mean, the L2 normalisation to norm sqrt(d_h) (keys times exp(beta))
+//     and RoPE with half-split pairs (o, o + d_h / 2) at the row's position.
+// Without the channel convolution W is the identity (k1 = 1); without the
+// depth-wise convolution a is the projection itself.  Every wait is bounded.
+constexpr int kQkRows = 128;
 
 template <int DH>
-struct QkSmem {
-    static constexpr size_t kW = (size_t)kMaxTapsCh * DH * DH * 2;            // bf16 weights [tap][in][out]
-    static constexpr size_t kIn = (size_t)(kRowsPerBlock + kMaxTapsCh - 1) * DH * 4;
-    static constexpr size_t kVal = (size_t)kRowsPerBlock * DH * 4;
-    static constexpr size_t kRed = (size_t)kRowsPerBlock * (DH / 32) * 4;
-    static constexpr size_t kBytes = kW + kIn + kVal + kRed;
+struct QkTc {
+    static constexpr int kA = kQkRows * DH * 2;  // one shifted input copy
+    static constexpr int kW = DH * DH * 2;       // one tap of the weights
+    static constexpr int kMaxSlots = DH == 64 ? 4 : 2;  // taps resident at once
+    static constexpr int kPosBytes = 160 * 4;            // tile rows' positions (at most 144 rows)
+    // Rows of the projection tile (a multiple of 8: whole swizzle atoms): the
+    // CTA's rows and both convolutions' halos.
+    __host__ __device__ static int tile_rows(int k0, int k1)
+    {
+        return (kQkRows + (k1 - 1) + (k0 > 0 ? k0 - 1 : 0) + 7) / 8 * 8;
+    }
+    static size_t bytes(int slots, int k0, int k1)
+    {
+        return (size_t)slots * (kA + kW) + (size_t)tile_rows(k0, k1) * DH * 2 + (size_t)DH * kMaxTapsSeq * 4 +
+               kPosBytes + 64 + 1024;
+    }
 };
 
+// Byte offset of 16-byte chunk c (channels 8c .. 8c + 7) of row n in a tile
+// of `rows` rows laid out as the 128-byte swizzle places it (TMA copies, and
+// K-major MMA operands): 64-channel column blocks of rows x 128 bytes, the
+// chunk index XOR-ed with the row's position in its 8-row, 1024-byte atom.
+__device__ __forceinline__ uint32_t sw128_offset(int rows, int n, int c)
+{
+    return (uint32_t)((c >> 3) * rows * 128 + n * 128 + (((c & 7) ^ (n & 7)) << 4));
+}
+
+__device__ __forceinline__ uint4 pack8_f16(const float (&a)[8], bool &over)
+{
+    uint4 o;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) over |= ptx::beyond_f16(a[q]);
+    o.x = ptx::pack_f16_satfinite(a[0], a[1]);
+    o.y = ptx::pack_f16_satfinite(a[2], a[3]);
+    o.z = ptx::pack_f16_satfinite(a[4], a[5]);
+    o.w = ptx::pack_f16_satfinite(a[6], a[7]);
+    return o;
+}
+
+__device__ __forceinline__ void unpack8_bf16(const uint4 &w, float (&a)[8])
+{
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        a[2 * q] = __uint_as_float(u[q] << 16);
+        a[2 * q + 1] = __uint_as_float(u[q] & 0xffff0000u);
+    }
+}
+
+// The channel convolution's weights as the qk kernel copies them: per head g
+// (grid y) and tap j, W_j[o, i] = W1[g d_h + o, i, j] in fp16 (the identity
+// without the convolution) in the K-major 128-byte-swizzle operand layout.
 template <int DH>
-__global__ void __launch_bounds__(DH * kRowThreads) cca_qk_kernel(CcaQkParams p)
+__global__ void __launch_bounds__(256) cca_w1_image_kernel(const bf16 *__restrict__ w1, int k1, uint8_t *img,
+                                                           uint32_t *status)
 {
     ptx::pdl_trigger();
     ptx::pdl_wait();
-    constexpr int R = kRowsPerBlock, RT = kRowsPerThread, half = DH / 2;
-    using Sm = QkSmem<DH>;
-    extern __shared__ __align__(16) uint8_t sm[];
-    bf16 *wsm = reinterpret_cast<bf16 *>(sm);                               // [k1][DH in][DH out]
-    float (*cin)[DH] = reinterpret_cast<float (*)[DH]>(sm + Sm::kW);       // rows r0 - halo + i
-    float (*val)[DH] = reinterpret_cast<float (*)[DH]>(sm + Sm::kW + Sm::kIn);
-    float (*red)[DH / 32] = reinterpret_cast<float (*)[DH / 32]>(sm + Sm::kW + Sm::kIn + Sm::kVal);
-    const int o = threadIdx.x, y = threadIdx.y, tid = y * DH + o;
+    constexpr int kChunks = DH / 8, kPerTap = DH * kChunks;
     const int g = blockIdx.y;
-    const int64_t r0 = (int64_t)blockIdx.x * R;
-    const int ch = g * DH + o;  // packed channel
-    const int conv2 = p.conv_layers == 2;
-    const int halo = conv2 ? p.k1 - 1 : 0;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= k1 * kPerTap) return;
+    const int j = e / kPerTap, o = (e % kPerTap) / kChunks, c = e % kChunks;
+    float a[8];
+    if (w1) {
+        const bf16 *src = w1 + ((int64_t)(g * DH + o) * DH + 8 * c) * k1 + j;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a[q] = __bfloat162float(src[q * k1]);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) a[q] = 8 * c + q == o ? 1.f : 0.f;
+    }
+    bool over = false;
+    *reinterpret_cast<uint4 *>(img + ((size_t)g * k1 + j) * QkTc<DH>::kW + sw128_offset(DH, o, c)) = pack8_f16(a, over);
+    if (over && status) atomicOr(status, kStatusF16Range);
+}
+
+template <int DH>
+__global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
+    cca_qk_tc_kernel(const __grid_constant__ CUtensorMap tx, CcaQkParams p)
+{
+    using C = QkTc<DH>;
+    constexpr int half = DH / 2, kChunks = DH / 8;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int slots = p.slots, k0 = p.k0, k1 = p.k1;
+    const int halo = k1 - 1, halo0 = k0 > 0 ? k0 - 1 : 0;
+    const int Ub = C::tile_rows(k0, k1);
+    uint8_t *sA = smem;                                                   // slots x kA
+    uint8_t *sW = sA + (size_t)slots * C::kA;                             // slots x kW
+    uint8_t *sX = sW + (size_t)slots * C::kW;                             // Ub x DH projections
+    float *sW0 = reinterpret_cast<float *>(sX + (size_t)Ub * DH * 2);     // [k0][DH]
+    int *spos = reinterpret_cast<int *>(sW0 + DH * kMaxTapsSeq);          // [Ub] position in sequence, -1 outside
+    uint64_t *x_full = reinterpret_cast<uint64_t *>(spos + C::kPosBytes / 4);
+    uint64_t *w_full = x_full + 1;
+    uint64_t *mma_done = x_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(x_full + 3);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int m = threadIdx.x, warp = m / 32;
+    const int g = blockIdx.y, ch0 = g * DH;  // the head's first packed channel
+    // Rows fit in 32 bits (the host checks T).
+    const int T = (int)p.T;
+    const int r0 = blockIdx.x * kQkRows, r = r0 + m;
+    const int u0 = r0 - halo - halo0;        // global row of tile row 0
+    const bool live = r < T;
     const int Wp = p.P + p.Lkv;
-    if (conv2) {
-        // w1[(g DH + out) DH + in][tap] -> wsm[tap][in][out]
-        const bf16 *wg = p.w1 + (int64_t)g * DH * DH * p.k1;
-        for (int e = tid; e < DH * DH * p.k1; e += DH * kRowThreads) {
-            const int j = e % p.k1, i = (e / p.k1) % DH, oo = e / (p.k1 * DH);
-            wsm[(j * DH + i) * DH + oo] = wg[e];
-        }
+    const uint8_t *img = p.w1img + (size_t)g * k1 * C::kW;
+    bool over = false;
+    int w_loads = 0;  // weight copies issued (thread 0)
+
+    if (m == 0) {
+        ptx::mbar_init(x_full, 1);
+        ptx::mbar_init(w_full, 1);
+        ptx::mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tx);
     }
-    for (int i = y; i < R + halo; i += kRowThreads) {
-        const int64_t r = r0 - halo + i;
-        float a = 0.f;
-        if (r >= 0 && r < p.T) a = p.c0 ? p.c0[r * p.P + ch] : __bfloat162float(p.pre[r * Wp + ch]);
-        cin[i][o] = a;
+    // Depth-wise weights of the head's channels, [tap][channel] (immutable:
+    // before the wait).
+    for (int e = m; e < DH * k0; e += kQkRows)
+        sW0[(e % k0) * DH + e / k0] = __bfloat162float(p.w0[(int64_t)ch0 * k0 + e]);
+    for (int u = m; u < Ub; u += kQkRows) {
+        const int row = u0 + u;
+        spos[u] = row >= 0 && row < T ? row % p.S : -1;
     }
     __syncthreads();
-    float acc[RT];
-    int tpos[RT];
-#pragma unroll
-    for (int k = 0; k < RT; ++k) {
-        const int64_t r = r0 + y + k * kRowThreads;
-        tpos[k] = r < p.T ? (int)(r % p.S) : 0;
-        acc[k] = conv2 ? 0.f : cin[y + k * kRowThreads][o];
+    // The projections and the weight image come from earlier kernels.
+    ptx::pdl_wait();
+    if (warp == 0) ptx::tmem_alloc(tmem_slot, DH);
+    if (m == 0) {
+        ptx::mbar_expect_tx(x_full, (uint32_t)(DH / 64) * Ub * 128);
+        for (int kc = 0; kc < DH / 64; ++kc)
+            ptx::tma_load_2d(sX + (size_t)kc * Ub * 128, &tx, x_full, ch0 + 64 * kc, u0);
+        const int nt = min(slots, k1);
+        ptx::mbar_expect_tx(w_full, (uint32_t)(nt * C::kW));
+        ptx::bulk_load(sW, img, (uint32_t)(nt * C::kW), w_full);
+        w_loads = 1;
     }
-    if (conv2) {
-        // Tap j of row r reads row r - (k1 - 1 - j), within the row's sequence only.
-        for (int j = 0; j < p.k1; ++j) {
-            const int back = p.k1 - 1 - j;
-            const bf16 *wj = wsm + (size_t)j * DH * DH + o;
-#pragma unroll 4
-            for (int i = 0; i < DH; ++i) {
-                const float wv = __bfloat162float(wj[i * DH]);
-#pragma unroll
-                for (int k = 0; k < RT; ++k)
-                    if (tpos[k] >= back) acc[k] += wv * cin[y + k * kRowThreads + j][i];
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    bool ok = __syncthreads_and(ptx::mbar_wait(x_full, 0, abort_flag));
+
+    int pass = 0;
+    for (int j0 = 0; ok && j0 < k1; j0 += slots, ++pass) {
+        const int nt = min(slots, k1 - j0);
+        if (pass > 0) {
+            // The slots are rewritten once the previous pass's MMAs have read them.
+            ok = __syncthreads_and(ptx::mbar_wait(mma_done, (pass - 1) & 1, abort_flag));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            if (m == 0) {
+                ptx::mbar_expect_tx(w_full, (uint32_t)(nt * C::kW));
+                ptx::bulk_load(sW, img + (size_t)j0 * C::kW, (uint32_t)(nt * C::kW), w_full);
+                ++w_loads;
             }
         }
-    }
-#pragma unroll
-    for (int k = 0; k < RT; ++k) {
-        const int yy = y + k * kRowThreads;
-        const int64_t r = r0 + yy;
-        if (p.qk_mean && r < p.T) {
-            // Query head g: (q_pre,g + k_pre of its group) / 2; key head j: the
-            // average of that over its group's query heads.
-            const bf16 *row = p.pre + r * Wp;
-            if (g < p.Hq) {
-                acc[k] += 0.5f * (__bfloat162float(row[g * DH + o]) + __bfloat162float(row[p.Lq + (g / p.gs) * DH + o]));
+        // Depth-wise output a[s] for s = r0 - halo + i, i in [0, 128 + halo)
+        // (tile row i + halo0),
+        // once per (row, 8-channel chunk), written to every shifted copy it
+        // feeds: A_j[n] = a[r0 + n - back_j] (back_j = k1 - 1 - j) at
+        // n = i + back_j - halo, zero when row r0 + n lies fewer than back_j
+        // rows into its sequence.  Consecutive threads take consecutive rows.
+        const int n_rows = kQkRows + halo;
+#pragma unroll 1
+        for (int e = m; e < n_rows * kChunks; e += kQkRows) {
+            const int i = e % n_rows, c = e / n_rows;
+            const int u = i + halo0;  // tile row of s
+            const int ts = spos[u];
+            float a[8];
+            if (k0 == 0) {
+                unpack8_bf16(*reinterpret_cast<const uint4 *>(sX + sw128_offset(Ub, u, c)), a);
             } else {
-                const int jh = g - p.Hq;
-                float qs = 0.f;
-                for (int h = jh * p.gs; h < (jh + 1) * p.gs; ++h) qs += __bfloat162float(row[h * DH + o]);
-                acc[k] += 0.5f * (__bfloat162float(row[p.Lq + jh * DH + o]) + qs / (float)p.gs);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) a[q] = 0.f;
+                // Tap jj reads row srow - (k0 - 1 - jj), within srow's sequence.
+                for (int jj = 0; jj < k0; ++jj) {
+                    const int b0 = k0 - 1 - jj;
+                    if (ts < b0) continue;
+                    float x[8];
+                    unpack8_bf16(*reinterpret_cast<const uint4 *>(sX + sw128_offset(Ub, u - b0, c)), x);
+                    const float4 wa = *reinterpret_cast<const float4 *>(sW0 + jj * DH + 8 * c);
+                    const float4 wb = *reinterpret_cast<const float4 *>(sW0 + jj * DH + 8 * c + 4);
+                    a[0] = fmaf(wa.x, x[0], a[0]);
+                    a[1] = fmaf(wa.y, x[1], a[1]);
+                    a[2] = fmaf(wa.z, x[2], a[2]);
+                    a[3] = fmaf(wa.w, x[3], a[3]);
+                    a[4] = fmaf(wb.x, x[4], a[4]);
+                    a[5] = fmaf(wb.y, x[5], a[5]);
+                    a[6] = fmaf(wb.z, x[6], a[6]);
+                    a[7] = fmaf(wb.w, x[7], a[7]);
+                }
+            }
+            const uint4 packed = pack8_f16(a, over);
+            for (int s = 0; s < nt; ++s) {
+                const int back = k1 - 1 - (j0 + s), n = i + back - halo;
+                if (n < 0 || n >= kQkRows) continue;
+                const bool in_seq = spos[n + halo + halo0] >= back;
+                *reinterpret_cast<uint4 *>(sA + (size_t)s * C::kA + sw128_offset(kQkRows, n, c)) =
+                    in_seq ? packed : make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        float ss = acc[k] * acc[k];
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (m == 0) {
+            if (ptx::mbar_wait(w_full, pass & 1, abort_flag)) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idesc = ptx::idesc_f16(kQkRows, DH, false, false);
+                for (int s = 0; s < nt; ++s) {
+                    const uint32_t a0 = ptx::smem_u32(sA + (size_t)s * C::kA);
+                    const uint32_t b0 = ptx::smem_u32(sW + (size_t)s * C::kW);
 #pragma unroll
-        for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-        if ((o & 31) == 0) red[yy][o >> 5] = ss;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < RT; ++k) {
-        const int yy = y + k * kRowThreads;
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < DH / 32; ++w) tot += red[yy][w];
-        float sc = sqrtf((float)DH) / fmaxf(sqrtf(tot), 1e-6f);
-        if (g >= p.Hq) sc *= p.k_scale;
-        val[yy][o] = acc[k] * sc;
-    }
-    __syncthreads();
-    const int i = o < half ? o : o - half;
-#pragma unroll
-    for (int k = 0; k < RT; ++k) {
-        const int yy = y + k * kRowThreads;
-        const int64_t r = r0 + yy;
-        if (r >= p.T) continue;
-        const float2 cs = p.rope[(int64_t)tpos[k] * half + i];
-        const float x0 = val[yy][i], x1 = val[yy][i + half];
-        const float out = o < half ? x0 * cs.x - x1 * cs.y : x0 * cs.y + x1 * cs.x;
-        if (g < p.Hq) {
-            p.q[r * p.Lq + g * DH + o] = __float2bfloat16_rn(out);
-        } else {
-            bool over = false;
-            p.k[r * p.Lkv + (g - p.Hq) * DH + o] = to_f16_sat(out, over);
-            if (over && p.status) atomicOr(p.status, kStatusF16Range);
+                    for (int kk = 0; kk < DH / 16; ++kk)
+                        ptx::mma_bf16(tmem,
+                                      ptx::sdesc_sw128(a0 + (kk >> 2) * (kQkRows * 128) + (kk & 3) * 32, 16, 1024),
+                                      ptx::sdesc_sw128(b0 + (kk >> 2) * (DH * 128) + (kk & 3) * 32, 16, 1024), idesc,
+                                      (j0 + s > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(mma_done);
+            } else {
+                *abort_flag = 1;
+            }
         }
     }
+    if (ok) ok = __syncthreads_and(ptx::mbar_wait(mma_done, (pass - 1) & 1, abort_flag));
+
+    if (ok) {
+        ptx::tc_fence_after();
+        float v[DH];
+#pragma unroll
+        for (int cc = 0; cc < DH / 32; ++cc) {
+            uint32_t w[32];
+            ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc * 32, w);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[cc * 32 + q] = __uint_as_float(w[q]);
+        }
+        if (live) {
+            if (p.qk_mean) {
+                // Query head g: + (q_g + k_(g / gs)) / 2 of the projections; key
+                // head jh: + (k_jh + the mean of its group's query heads) / 2.
+                const int u = m + halo + halo0;  // tile row of r
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    float a[8];
+                    unpack8_bf16(*reinterpret_cast<const uint4 *>(sX + sw128_offset(Ub, u, c)), a);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[8 * c + q] = fmaf(0.5f, a[q], v[8 * c + q]);
+                }
+                const bool key = g >= p.Hq;
+                const int other = key ? (g - p.Hq) * p.gs : p.Hq + g / p.gs;  // first partner head
+                const int n_other = key ? p.gs : 1;
+                const float w_other = 0.5f / (float)n_other;
+                const uint4 *row = reinterpret_cast<const uint4 *>(p.pre + (int64_t)r * Wp);
+#pragma unroll 1
+                for (int h = other; h < other + n_other; ++h) {
+                    uint4 b[kChunks];
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) b[c] = row[h * kChunks + c];
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c) {
+                        float x[8];
+                        unpack8_bf16(b[c], x);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) v[8 * c + q] = fmaf(w_other, x[q], v[8 * c + q]);
+                    }
+                }
+            }
+            float ss = 0.f;
+#pragma unroll
+            for (int o = 0; o < DH; ++o) ss = fmaf(v[o], v[o], ss);
+            float sc = sqrtf((float)DH) / fmaxf(sqrtf(ss), 1e-6f);
+            if (g >= p.Hq) sc *= p.k_scale;
+            const float4 *cs = reinterpret_cast<const float4 *>(p.rope + (int64_t)spos[m + halo + halo0] * half);
+#pragma unroll
+            for (int i2 = 0; i2 < half / 2; ++i2) {
+                const float4 e = cs[i2];  // (cos, sin) of pairs 2 i2 and 2 i2 + 1
+#pragma unroll
+                for (int d = 0; d < 2; ++d) {
+                    const int i = 2 * i2 + d;
+                    const float cv = d ? e.z : e.x, sv = d ? e.w : e.y;
+                    const float x0 = v[i] * sc, x1 = v[i + half] * sc;
+                    v[i] = x0 * cv - x1 * sv;
+                    v[i + half] = x0 * sv + x1 * cv;
+                }
+            }
+            if (g < p.Hq) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.q + (int64_t)r * p.Lq + ch0);
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    dst[c] = make_uint4(ptx::pack_bf16(v[8 * c], v[8 * c + 1]), ptx::pack_bf16(v[8 * c + 2], v[8 * c + 3]),
+                                        ptx::pack_bf16(v[8 * c + 4], v[8 * c + 5]),
+                                        ptx::pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.k + (int64_t)r * p.Lkv + (ch0 - p.Lq));
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c) {
+                    float a[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) a[q] = v[8 * c + q];
+                    dst[c] = pack8_f16(a, over);
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        // Copies still in flight after a timeout land before the shared
+        // memory is released.
+        if (!ok && m == 0) {
+            volatile int never = 0;
+            ptx::mbar_wait(x_full, 0, &never);
+            if (w_loads > 0) ptx::mbar_wait(w_full, (w_loads - 1) & 1, &never);
+        }
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, DH);
+    }
+    ptx::pdl_trigger();
+    if (over && p.status) atomicOr(p.status, kStatusF16Range);
+    if (m == 0 && !ok && p.status) atomicOr(p.status, kStatusTimeout);
 }
 
 }  // namespace
@@ -387,60 +626,65 @@ mla_status mla_cca_forward(mla_cca_handle *h, const mla_cca_weights *w, const vo
     mla_status st;
     if ((st = cuda(cudaMemsetAsync(d_sp, 0, sizeof(int32_t) * B, s))) != MLA_OK) return st;
 
-    // 1. Down-projections into column slices of pre: [W_QK x | W_V1 x | W_V2 x] (or [W_QK x | W_V x]).
+    // 1. Down-projections (one grouped GEMM) into column slices of pre:
+    //    [W_QK x | W_V1 x | W_V2 x] (or [W_QK x | W_V x]).
     float *split = (float *)(wb + L.split);
     auto gemm = [&](GemmArgs g) -> mla_status {
         g.split_ws = split;  // GEMMs run one after another on the stream: one split region serves all
         if (!gemm_tc_supported(g)) return MLA_ERR_UNSUPPORTED;
         return cuda(gemm_tc(g, h->num_sms, s));
     };
-    if ((st = gemm(cca_linear(x, T, c.d_model, w->W_QK, P, pre, Wp, 0, status))) != MLA_OK) return st;
-    if (c.value_shift) {
-        if ((st = gemm(cca_linear(x, T, c.d_model, w->W_V1, Lkv / 2, pre, Wp, P, status))) != MLA_OK) return st;
-        if ((st = gemm(cca_linear(x, T, c.d_model, w->W_V2, Lkv / 2, pre, Wp, P + Lkv / 2, status))) != MLA_OK)
-            return st;
-    } else if ((st = gemm(cca_linear(x, T, c.d_model, w->W_V, Lkv, pre, Wp, P, status))) != MLA_OK) {
-        return st;
-    }
+    if ((st = gemm(cca_down_proj(c, x, T, w, pre, status))) != MLA_OK) return st;
 
-    // 2. Depth-wise convolution (fp32) and the values (fp16).
-    float *c0 = c.conv_layers >= 1 ? (float *)(wb + L.c0) : nullptr;
+    // 2. The values (fp16).
     __half *v = (__half *)(wb + L.v);
     {
-        const int col0 = c0 ? 0 : P;
-        const int64_t n = T * (Wp - col0);
-        st = cuda(launch_ex(cca_conv0_v_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1, (const bf16 *)pre,
-                            T, S, P, Lkv, col0, c.conv_layers >= 1 ? c.conv_kernel_seq : 1, (const bf16 *)w->conv0, c0,
-                            v, c.value_shift, status));
+        const int64_t n = T * (Lkv / 8);
+        st = cuda(launch_ex(cca_v_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, 1, (const bf16 *)pre, T,
+                            S, P, Lkv, v, c.value_shift, status));
         note_launch();
         if (st != MLA_OK) return st;
     }
 
-    // 3. Grouped convolution, q-k-mean, normalisation, temperature, RoPE.
+    // 3. Both convolutions, q-k-mean, normalisation, temperature, RoPE.
     CcaQkParams q;
-    q.pre = pre; q.c0 = c0; q.w1 = (const bf16 *)w->conv1;
+    q.pre = pre;
+    q.w0 = c.conv_layers >= 1 ? (const bf16 *)w->conv0 : nullptr;
+    q.w1img = (const uint8_t *)(wb + L.w1img);
     q.T = T; q.S = S; q.P = P; q.Lkv = Lkv; q.Lq = c.q_latent; q.Hq = c.n_heads;
     q.gs = c.n_heads / c.n_kv_heads;
+    q.k0 = c.conv_layers >= 1 ? c.conv_kernel_seq : 0;
     q.k1 = c.conv_layers >= 2 ? c.conv_kernel_ch : 1;
-    q.conv_layers = c.conv_layers; q.qk_mean = c.qk_mean;
+    q.qk_mean = c.qk_mean;
     q.k_scale = (float)exp(c.key_temp);
     q.rope = h->rope_table;
     q.q = (bf16 *)(wb + L.q);
     q.k = (__half *)(wb + L.k);
     q.status = status;
     {
-        const dim3 grid((unsigned)((T + kRowsPerBlock - 1) / kRowsPerBlock), (unsigned)(c.n_heads + c.n_kv_heads));
+        const int heads = c.n_heads + c.n_kv_heads;
+        const bf16 *w1 = c.conv_layers >= 2 ? (const bf16 *)w->conv1 : nullptr;
+        uint8_t *img = (uint8_t *)(wb + L.w1img);
+        const dim3 grid((unsigned)((T + kQkRows - 1) / kQkRows), (unsigned)heads);
+        const dim3 igrid((unsigned)((q.k1 * dh * dh / 8 + 255) / 256), (unsigned)heads);
         static std::atomic<int> smem64{-1}, smem128{-1};
-        if (dh == 64) {
-            st = cuda(smem_limit_once(smem64, (const void *)cca_qk_kernel<64>, (int)QkSmem<64>::kBytes));
-            if (st == MLA_OK)
-                st = cuda(launch_ex(cca_qk_kernel<64>, grid, dim3(64, kRowThreads), QkSmem<64>::kBytes, s, 1, q));
-        } else {
-            st = cuda(smem_limit_once(smem128, (const void *)cca_qk_kernel<128>, (int)QkSmem<128>::kBytes));
-            if (st == MLA_OK)
-                st = cuda(launch_ex(cca_qk_kernel<128>, grid, dim3(128, kRowThreads), QkSmem<128>::kBytes, s, 1, q));
-        }
-        note_launch();
+        auto run = [&](auto image_kernel, auto qk_kernel, auto cfg, std::atomic<int> &smem_set) -> mla_status {
+            using Q = decltype(cfg);
+            CUtensorMap tx;
+            if (!make_tmap_bf16(&tx, pre, T, Wp, Wp, 64, Q::tile_rows(q.k0, q.k1))) return MLA_ERR_CUDA;
+            mla_status r = cuda(launch_ex(image_kernel, igrid, dim3(256), 0, s, 1, w1, q.k1, img, status));
+            note_launch();
+            if (r != MLA_OK) return r;
+            q.slots = std::min(q.k1, Q::kMaxSlots);
+            r = cuda(smem_limit_once(smem_set, (const void *)qk_kernel,
+                                     (int)Q::bytes(Q::kMaxSlots, kMaxTapsSeq, kMaxTapsCh)));
+            if (r == MLA_OK)
+                r = cuda(launch_ex(qk_kernel, grid, dim3(kQkRows), Q::bytes(q.slots, q.k0, q.k1), s, 1, tx, q));
+            note_launch();
+            return r;
+        };
+        st = dh == 64 ? run(cca_w1_image_kernel<64>, cca_qk_tc_kernel<64>, QkTc<64>{}, smem64)
+                      : run(cca_w1_image_kernel<128>, cca_qk_tc_kernel<128>, QkTc<128>{}, smem128);
         if (st != MLA_OK) return st;
     }
 

@@ -189,6 +189,17 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
+// Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned) from global memory into this CTA's shared memory, completing on
+// `bar` (transaction bytes).
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy (TMA,
 // tcgen05.mma operands).
 __device__ __forceinline__ void fence_proxy_async_smem()

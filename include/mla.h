@@ -284,9 +284,12 @@ mla_status mla_out_proj_static(mla_handle *h, const mla_weights *w, const void *
  *  - RoPE with half-split pairs at positions 0..S-1 in the latent;
  *  - causal softmax attention, scale 1/sqrt(d_h), query head h reading
  *    key/value head g(h); y = W_O o.
- * CCA is the case n_kv_heads == n_heads.  bfloat16 only (tensor cores for the
- * projections and the attention, CUDA cores for the convolutions and the
- * normalisation); d_h in {64, 128}. */
+ * CCA is the case n_kv_heads == n_heads.  bfloat16 in and out; the grouped
+ * convolution, the projections and the attention run on the tensor cores
+ * (the convolution and the attention's keys and values with fp16 operands:
+ * values beyond fp16's range saturate and set status bit 16), the
+ * depth-wise convolution and the normalisation on the CUDA cores; d_h in
+ * {64, 128}. */
 typedef struct {
     int d_model, n_heads, n_kv_heads, q_latent, kv_latent;
     int conv_layers;      /* 0, 1 or 2 */
