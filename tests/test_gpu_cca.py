@@ -70,6 +70,25 @@ def test_cca_parity(mla, w):
     run(mla, w)
 
 
+@pytest.mark.parametrize("w", [
+    # Many sequence starts inside one 128-row tile: sequences shorter than
+    # either convolution's filter, so both causal paddings and the row shifts
+    # of every tap cross sequence starts.
+    BASE.replace(name="short_seqs", batch=37, seq=3, conv_kernel_seq=5, conv_kernel_ch=4),
+    BASE.replace(name="single_token", batch=9, seq=1),
+    # The widest filters: 8 depth-wise taps; 4 channel taps in one pass at
+    # d_h = 64 and in two passes (two taps each) at d_h = 128.
+    BASE.replace(name="widest_filters", conv_kernel_seq=8, conv_kernel_ch=4, seed=2),
+    syn.CcaWorkload("dh128_four_taps", d_model=512, n_heads=2, n_kv_heads=2, q_latent=256, kv_latent=256, batch=2,
+                    seq=140, conv_kernel_ch=4),
+    # An odd number of heads in all (3 query heads, 1 key/value head).
+    syn.CcaWorkload("odd_heads", d_model=256, n_heads=3, n_kv_heads=1, q_latent=192, kv_latent=64, batch=2, seq=130,
+                    value_shift=False),
+], ids=lambda w: w.name)
+def test_cca_edges(mla, w):
+    run(mla, w)
+
+
 @pytest.mark.parametrize("name", ["cca_prefill", "ccgqa_prefill"])
 def test_cca_full_sampled(mla, name):
     w = syn.CCA_WORKLOADS[name]
