@@ -165,7 +165,7 @@ struct CcaQkParams {
 };
 
 // One CTA per (128 token rows, head g): query heads g < Hq, key heads after
-// them; thread m owns row r0 + m.  The grouped causal convolution (one
+// them; 256 threads.  The grouped causal convolution (one
 // group of d_h channels per head) is a contraction over (tap, input
 // channel):
 //   u[r, o] = sum_j sum_i a[r - (k1 - 1 - j), i] W1[g d_h + o, i, j],
@@ -181,12 +181,15 @@ struct CcaQkParams {
 //   - one thread issues k1 * d_h / 16 MMAs (M = 128 rows, N = d_h output
 //     channels, K = 16) accumulating into tensor memory; taps that do not fit
 //     in shared memory at once run in passes;
-//   - thread m reads row m back from tensor-memory lane m and applies
-//     q-k-mean, the L2 normalisation to norm sqrt(d_h) (keys times exp(beta))
-//     and RoPE with half-split pairs (o, o + d_h / 2) at the row's position.
+//   - two threads per row read row m back from tensor-memory lane m, each
+//     taking half of the RoPE pairs (o, o + d_h / 2), and apply q-k-mean, the
+//     L2 normalisation to norm sqrt(d_h) (keys times exp(beta); the two
+//     partial sums of squares meet in shared memory) and RoPE at the row's
+//     position.
 // Without the channel convolution W is the identity (k1 = 1); without the
 // depth-wise convolution a is the projection itself.  Every wait is bounded.
 constexpr int kQkRows = 128;
+constexpr int kQkThreads = 256;  // two threads per row in the epilogue
 
 template <int DH>
 struct QkTc {
@@ -194,6 +197,7 @@ struct QkTc {
     static constexpr int kW = DH * DH * 2;       // one tap of the weights
     static constexpr int kMaxSlots = DH == 64 ? 4 : 2;  // taps resident at once
     static constexpr int kPosBytes = 160 * 4;            // tile rows' positions (at most 144 rows)
+    static constexpr int kRedBytes = kQkRows * 2 * 4;    // per row, the two threads' partial squared norms
     // Rows of the projection tile (a multiple of 8: whole swizzle atoms): the
     // CTA's rows and both convolutions' halos.
     __host__ __device__ static int tile_rows(int k0, int k1)
@@ -203,7 +207,7 @@ struct QkTc {
     static size_t bytes(int slots, int k0, int k1)
     {
         return (size_t)slots * (kA + kW) + (size_t)tile_rows(k0, k1) * DH * 2 + (size_t)DH * kMaxTapsSeq * 4 +
-               kPosBytes + 64 + 1024;
+               kPosBytes + kRedBytes + 64 + 1024;
     }
 };
 
@@ -267,7 +271,7 @@ __global__ void __launch_bounds__(256) cca_w1_image_kernel(const bf16 *__restric
 }
 
 template <int DH>
-__global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
+__global__ void __launch_bounds__(kQkThreads, DH == 64 ? 2 : 1)
     cca_qk_tc_kernel(const __grid_constant__ CUtensorMap tx, CcaQkParams p)
 {
     using C = QkTc<DH>;
@@ -282,13 +286,16 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
     uint8_t *sX = sW + (size_t)slots * C::kW;                             // Ub x DH projections
     float *sW0 = reinterpret_cast<float *>(sX + (size_t)Ub * DH * 2);     // [k0][DH]
     int *spos = reinterpret_cast<int *>(sW0 + DH * kMaxTapsSeq);          // [Ub] position in sequence, -1 outside
-    uint64_t *x_full = reinterpret_cast<uint64_t *>(spos + C::kPosBytes / 4);
+    float (*red)[2] = reinterpret_cast<float (*)[2]>(spos + C::kPosBytes / 4);
+    uint64_t *x_full = reinterpret_cast<uint64_t *>(red + kQkRows);
     uint64_t *w_full = x_full + 1;
     uint64_t *mma_done = x_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(x_full + 3);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    const int m = threadIdx.x, warp = m / 32;
+    // Thread tid: row m = tid % 128 (tensor-memory lane m; warps w and w + 4
+    // share a lane quarter) and half hf = tid / 128 of the row's RoPE pairs.
+    const int tid = threadIdx.x, warp = tid / 32, m = tid % kQkRows, hf = tid / kQkRows;
     const int g = blockIdx.y, ch0 = g * DH;  // the head's first packed channel
     // Rows fit in 32 bits (the host checks T).
     const int T = (int)p.T;
@@ -300,7 +307,7 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
     bool over = false;
     int w_loads = 0;  // weight copies issued (thread 0)
 
-    if (m == 0) {
+    if (tid == 0) {
         ptx::mbar_init(x_full, 1);
         ptx::mbar_init(w_full, 1);
         ptx::mbar_init(mma_done, 1);
@@ -310,9 +317,9 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
     }
     // Depth-wise weights of the head's channels, [tap][channel] (immutable:
     // before the wait).
-    for (int e = m; e < DH * k0; e += kQkRows)
+    for (int e = tid; e < DH * k0; e += kQkThreads)
         sW0[(e % k0) * DH + e / k0] = __bfloat162float(p.w0[(int64_t)ch0 * k0 + e]);
-    for (int u = m; u < Ub; u += kQkRows) {
+    for (int u = tid; u < Ub; u += kQkThreads) {
         const int row = u0 + u;
         spos[u] = row >= 0 && row < T ? row % p.S : -1;
     }
@@ -320,7 +327,7 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
     // The projections and the weight image come from earlier kernels.
     ptx::pdl_wait();
     if (warp == 0) ptx::tmem_alloc(tmem_slot, DH);
-    if (m == 0) {
+    if (tid == 0) {
         ptx::mbar_expect_tx(x_full, (uint32_t)(DH / 64) * Ub * 128);
         for (int kc = 0; kc < DH / 64; ++kc)
             ptx::tma_load_2d(sX + (size_t)kc * Ub * 128, &tx, x_full, ch0 + 64 * kc, u0);
@@ -343,7 +350,7 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
             ok = __syncthreads_and(ptx::mbar_wait(mma_done, (pass - 1) & 1, abort_flag));
             if (!ok) break;
             ptx::tc_fence_after();
-            if (m == 0) {
+            if (tid == 0) {
                 ptx::mbar_expect_tx(w_full, (uint32_t)(nt * C::kW));
                 ptx::bulk_load(sW, img + (size_t)j0 * C::kW, (uint32_t)(nt * C::kW), w_full);
                 ++w_loads;
@@ -357,7 +364,7 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
         // rows into its sequence.  Consecutive threads take consecutive rows.
         const int n_rows = kQkRows + halo;
 #pragma unroll 1
-        for (int e = m; e < n_rows * kChunks; e += kQkRows) {
+        for (int e = tid; e < n_rows * kChunks; e += kQkThreads) {
             const int i = e % n_rows, c = e / n_rows;
             const int u = i + halo0;  // tile row of s
             const int ts = spos[u];
@@ -397,7 +404,7 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
-        if (m == 0) {
+        if (tid == 0) {
             if (ptx::mbar_wait(w_full, pass & 1, abort_flag)) {
                 ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_f16(kQkRows, DH, false, false);
@@ -420,80 +427,92 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
     if (ok) ok = __syncthreads_and(ptx::mbar_wait(mma_done, (pass - 1) & 1, abort_flag));
 
     if (ok) {
+        // This thread's columns: RoPE pairs i in [hf QH, hf QH + QH), i.e.
+        // columns c0 + [0, QH) in v[0, QH) and c0 + half + [0, QH) in
+        // v[QH, 2 QH).
+        constexpr int QH = half / 2, kCq = QH / 8;
+        const int c0 = hf * QH;
         ptx::tc_fence_after();
-        float v[DH];
+        float v[2 * QH];
+        const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16);
 #pragma unroll
-        for (int cc = 0; cc < DH / 32; ++cc) {
-            uint32_t w[32];
-            ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + cc * 32, w);
+        for (int part = 0; part < 2; ++part) {
+            uint32_t w[QH];
+            if constexpr (QH == 32) ptx::tmem_ld32(lane_base + c0 + part * half, w);
+            else ptx::tmem_ld16(lane_base + c0 + part * half, w);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[cc * 32 + q] = __uint_as_float(w[q]);
+            for (int q = 0; q < QH; ++q) v[part * QH + q] = __uint_as_float(w[q]);
         }
-        if (live) {
-            if (p.qk_mean) {
-                // Query head g: + (q_g + k_(g / gs)) / 2 of the projections; key
-                // head jh: + (k_jh + the mean of its group's query heads) / 2.
-                const int u = m + halo + halo0;  // tile row of r
+        if (live && p.qk_mean) {
+            // Query head g: + (q_g + k_(g / gs)) / 2 of the projections; key
+            // head jh: + (k_jh + the mean of its group's query heads) / 2.
+            const int u = m + halo + halo0;  // tile row of r
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
-                    float a[8];
-                    unpack8_bf16(*reinterpret_cast<const uint4 *>(sX + sw128_offset(Ub, u, c)), a);
+            for (int j = 0; j < 2 * kCq; ++j) {
+                const int c = c0 / 8 + (j % kCq) + (j / kCq) * (half / 8);
+                float a[8];
+                unpack8_bf16(*reinterpret_cast<const uint4 *>(sX + sw128_offset(Ub, u, c)), a);
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) v[8 * c + q] = fmaf(0.5f, a[q], v[8 * c + q]);
-                }
-                const bool key = g >= p.Hq;
-                const int other = key ? (g - p.Hq) * p.gs : p.Hq + g / p.gs;  // first partner head
-                const int n_other = key ? p.gs : 1;
-                const float w_other = 0.5f / (float)n_other;
-                const uint4 *row = reinterpret_cast<const uint4 *>(p.pre + (int64_t)r * Wp);
+                for (int q = 0; q < 8; ++q) v[8 * j + q] = fmaf(0.5f, a[q], v[8 * j + q]);
+            }
+            const bool key = g >= p.Hq;
+            const int other = key ? (g - p.Hq) * p.gs : p.Hq + g / p.gs;  // first partner head
+            const int n_other = key ? p.gs : 1;
+            const float w_other = 0.5f / (float)n_other;
+            const uint4 *row = reinterpret_cast<const uint4 *>(p.pre + (int64_t)r * Wp);
 #pragma unroll 1
-                for (int h = other; h < other + n_other; ++h) {
-                    uint4 b[kChunks];
+            for (int h = other; h < other + n_other; ++h) {
+                uint4 b[2 * kCq];
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) b[c] = row[h * kChunks + c];
+                for (int j = 0; j < 2 * kCq; ++j) b[j] = row[h * kChunks + c0 / 8 + (j % kCq) + (j / kCq) * (half / 8)];
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c) {
-                        float x[8];
-                        unpack8_bf16(b[c], x);
+                for (int j = 0; j < 2 * kCq; ++j) {
+                    float x[8];
+                    unpack8_bf16(b[j], x);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) v[8 * c + q] = fmaf(w_other, x[q], v[8 * c + q]);
-                    }
+                    for (int q = 0; q < 8; ++q) v[8 * j + q] = fmaf(w_other, x[q], v[8 * j + q]);
                 }
             }
-            float ss = 0.f;
+        }
+        float ss = 0.f;
 #pragma unroll
-            for (int o = 0; o < DH; ++o) ss = fmaf(v[o], v[o], ss);
-            float sc = sqrtf((float)DH) / fmaxf(sqrtf(ss), 1e-6f);
+        for (int o = 0; o < 2 * QH; ++o) ss = fmaf(v[o], v[o], ss);
+        red[m][hf] = ss;
+        __syncthreads();
+        if (live) {
+            const float tot = red[m][0] + red[m][1];
+            float sc = sqrtf((float)DH) / fmaxf(sqrtf(tot), 1e-6f);
             if (g >= p.Hq) sc *= p.k_scale;
-            const float4 *cs = reinterpret_cast<const float4 *>(p.rope + (int64_t)spos[m + halo + halo0] * half);
+            const float4 *cs = reinterpret_cast<const float4 *>(p.rope + (int64_t)spos[m + halo + halo0] * half + c0);
 #pragma unroll
-            for (int i2 = 0; i2 < half / 2; ++i2) {
-                const float4 e = cs[i2];  // (cos, sin) of pairs 2 i2 and 2 i2 + 1
+            for (int i2 = 0; i2 < QH / 2; ++i2) {
+                const float4 e = cs[i2];  // (cos, sin) of pairs c0 + 2 i2 and c0 + 2 i2 + 1
 #pragma unroll
                 for (int d = 0; d < 2; ++d) {
                     const int i = 2 * i2 + d;
                     const float cv = d ? e.z : e.x, sv = d ? e.w : e.y;
-                    const float x0 = v[i] * sc, x1 = v[i + half] * sc;
+                    const float x0 = v[i] * sc, x1 = v[i + QH] * sc;
                     v[i] = x0 * cv - x1 * sv;
-                    v[i + half] = x0 * sv + x1 * cv;
+                    v[i + QH] = x0 * sv + x1 * cv;
                 }
             }
             if (g < p.Hq) {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.q + (int64_t)r * p.Lq + ch0);
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    dst[c] = make_uint4(ptx::pack_bf16(v[8 * c], v[8 * c + 1]), ptx::pack_bf16(v[8 * c + 2], v[8 * c + 3]),
-                                        ptx::pack_bf16(v[8 * c + 4], v[8 * c + 5]),
-                                        ptx::pack_bf16(v[8 * c + 6], v[8 * c + 7]));
+                for (int j = 0; j < 2 * kCq; ++j)
+                    dst[c0 / 8 + (j % kCq) + (j / kCq) * (half / 8)] =
+                        make_uint4(ptx::pack_bf16(v[8 * j], v[8 * j + 1]), ptx::pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                                   ptx::pack_bf16(v[8 * j + 4], v[8 * j + 5]),
+                                   ptx::pack_bf16(v[8 * j + 6], v[8 * j + 7]));
             } else {
                 uint4 *dst = reinterpret_cast<uint4 *>(p.k + (int64_t)r * p.Lkv + (ch0 - p.Lq));
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c) {
+                for (int j = 0; j < 2 * kCq; ++j) {
                     float a[8];
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) a[q] = v[8 * c + q];
-                    dst[c] = pack8_f16(a, over);
+                    for (int q = 0; q < 8; ++q) a[q] = v[8 * j + q];
+                    dst[c0 / 8 + (j % kCq) + (j / kCq) * (half / 8)] = pack8_f16(a, over);
                 }
             }
         }
@@ -504,7 +523,7 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
     if (warp == 0) {
         // Copies still in flight after a timeout land before the shared
         // memory is released.
-        if (!ok && m == 0) {
+        if (!ok && tid == 0) {
             volatile int never = 0;
             ptx::mbar_wait(x_full, 0, &never);
             if (w_loads > 0) ptx::mbar_wait(w_full, (w_loads - 1) & 1, &never);
@@ -515,7 +534,7 @@ __global__ void __launch_bounds__(kQkRows, DH == 64 ? 2 : 1)
     }
     ptx::pdl_trigger();
     if (over && p.status) atomicOr(p.status, kStatusF16Range);
-    if (m == 0 && !ok && p.status) atomicOr(p.status, kStatusTimeout);
+    if (tid == 0 && !ok && p.status) atomicOr(p.status, kStatusTimeout);
 }
 
 }  // namespace
@@ -679,7 +698,7 @@ mla_status mla_cca_forward(mla_cca_handle *h, const mla_cca_weights *w, const vo
             r = cuda(smem_limit_once(smem_set, (const void *)qk_kernel,
                                      (int)Q::bytes(Q::kMaxSlots, kMaxTapsSeq, kMaxTapsCh)));
             if (r == MLA_OK)
-                r = cuda(launch_ex(qk_kernel, grid, dim3(kQkRows), Q::bytes(q.slots, q.k0, q.k1), s, 1, tx, q));
+                r = cuda(launch_ex(qk_kernel, grid, dim3(kQkThreads), Q::bytes(q.slots, q.k0, q.k1), s, 1, tx, q));
             note_launch();
             return r;
         };
