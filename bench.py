@@ -325,7 +325,9 @@ def run_ours(args, rank, world, device):
     # End to end through the C ABI from pinned host buffers: H2D of the step's
     # inputs (token activations, positions, lengths: one pinned staging
     # buffer, one copy) and D2H of its output, captured with the step in one
-    # graph.
+    # graph.  Both copies go through mla_copy: the SMs move the bytes over the
+    # host link and the copies chain with the step's kernels like any other
+    # launch of the library.
     nx, ni = x.numel() * 2, B * 4
     inp_h = torch.empty(nx + 2 * ni, dtype=torch.uint8).pin_memory()
     inp_h[:nx].copy_(torch.from_numpy(np.ascontiguousarray(xs).view(np.uint8).reshape(-1)))
@@ -338,9 +340,9 @@ def run_ours(args, rank, world, device):
     sl_d = inp_d[nx + ni:].view(torch.int32)
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2):
-        inp_d.copy_(inp_h, non_blocking=True)
+        check(mla.mla_copy(inp_d, inp_h), "mla_copy (inputs)")
         step(x_d, pos_d, sl_d)
-        y_h.copy_(y, non_blocking=True)
+        check(mla.mla_copy(y_h, y), "mla_copy (output)")
     for _ in range(2):
         g2.replay()
     eev = timing_events(K)
@@ -355,6 +357,7 @@ def run_ours(args, rank, world, device):
     t3 = time.time()
     sampler.mark(t2, t3)
     e2e_ms = sum(a.elapsed_time(b) for a, b in eev) / K
+    launches += (launches_per_step + 2) * K  # the end-to-end graph: the step and its two copies
     h2d = inp_h.numel()
     d2h = y_h.numel() * 2
 

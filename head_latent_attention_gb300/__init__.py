@@ -40,7 +40,7 @@ EXPORTS = ("mla_check_config", "mla_create", "mla_destroy", "mla_workspace_size"
            "mla_get_device_status", "mla_status_string", "mla_launch_count",
            "mla_set_profile_events", "mla_out_proj_static", "mla_set_wait_limit", "mla_create_shard",
            "mla_cca_check_config", "mla_cca_create", "mla_cca_destroy", "mla_cca_workspace_size",
-           "mla_cca_forward", "mla_cca_get_device_status")
+           "mla_cca_forward", "mla_cca_get_device_status", "mla_copy")
 MLA_PROFILE_DECODE_ATTENTION = 0
 MLA_PROFILE_PREFILL_ATTENTION = 1
 MLA_PROFILE_DECODE_CALL = 2
@@ -110,6 +110,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "mla_launch_count": (ctypes.c_uint64, []),
         "mla_set_profile_events": (I, [I, P, P]),
         "mla_set_wait_limit": (I, [L]),
+        "mla_copy": (I, [P, P, S, P]),
         "mla_cca_check_config": (I, [P]),
         "mla_cca_create": (I, [P, ctypes.POINTER(P)]),
         "mla_cca_destroy": (None, [P]),
@@ -301,6 +302,21 @@ def mla_get_device_status(h: Handle, ws: Optional[torch.Tensor], stream=None):
 
 def mla_launch_count() -> int:
     return load_library().mla_launch_count()
+
+
+def mla_copy(dst: torch.Tensor, src: torch.Tensor, stream=None) -> int:
+    """Stream-ordered copy of src into dst (same byte size) by the SMs; either
+    may be a CUDA tensor or a pinned CPU tensor."""
+    for t in (dst, src):
+        if not t.is_contiguous():
+            raise ValueError("mla_copy needs contiguous tensors")
+        if not t.is_cuda and not t.is_pinned():
+            raise ValueError("mla_copy needs CUDA or pinned CPU tensors")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("mla_copy needs tensors of the same byte size")
+    return load_library().mla_copy(ctypes.c_void_p(dst.data_ptr()), ctypes.c_void_p(src.data_ptr()), nbytes,
+                                   _stream(stream))
 
 
 def mla_set_wait_limit(cycles: int) -> int:

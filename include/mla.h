@@ -343,6 +343,20 @@ mla_status mla_cca_get_device_status(mla_cca_handle *h, void *ws, void *stream, 
 /* Static English text for a status code. */
 const char *mla_status_string(mla_status s);
 
+/* ---- Staging ----
+ *
+ * Copy `bytes` from src to dst on the stream, with the SMs rather than a copy
+ * engine.  Either pointer may be device memory or pinned host memory
+ * (cudaHostAlloc / cudaHostRegister), which a kernel reaches over the host
+ * link through the same pointer under unified addressing; the copy is
+ * launched like the library's other kernels (programmatic dependent launch),
+ * so staging a step's inputs and reading back its result chain with the
+ * step's kernels.  Any alignment; 16-byte aligned buffers copy as 16-byte
+ * vectors.  Returns MLA_ERR_INVALID_ARG for a null pointer, a pointer no
+ * kernel can reach (unregistered pageable host memory) or overlapping ranges,
+ * MLA_ERR_CUDA if the launch fails.  Nothing is checked on the device. */
+mla_status mla_copy(void *dst, const void *src, size_t bytes, void *stream);
+
 /* ---- Diagnostics (used by the benchmark; not needed for computing) ---- */
 
 /* Number of kernels this library has launched in this process so far. */

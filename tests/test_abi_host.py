@@ -111,6 +111,8 @@ def test_null_handle_paths(lib):
                         None) == lib.MLA_ERR_INVALID_ARG
     assert L.mla_out_proj(None, None, None, 1, None, None, 0, None) == lib.MLA_ERR_INVALID_ARG
     assert L.mla_out_proj_static(None, None, None, 1, None, None) == lib.MLA_ERR_INVALID_ARG
+    assert L.mla_copy(None, None, 16, None) == lib.MLA_ERR_INVALID_ARG
+    assert L.mla_copy(None, None, 0, None) == lib.MLA_OK  # nothing to copy
     L.mla_destroy(None)
 
 
