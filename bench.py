@@ -102,8 +102,11 @@ def decode_flops(lens) -> float:
 def prefill_flops(w=PREFILL) -> float:
     T = w.batch * w.seq
     H = w.n_heads
-    proj = 2 * T * (w.d_model * (w.r_q + w.r_kv + w.d_rope) + w.r_q * H * (w.d_nope + w.d_rope)
-                    + w.r_kv * H * (w.d_nope + w.d_v) + H * w.d_v * w.d_model)
+    # The query: compressed (W_DQ, then W_UQ and W_QR) or, in the small-model
+    # form (r_q = 0), one W_Q.
+    q_proj = (w.d_model * w.r_q + w.r_q * H * (w.d_nope + w.d_rope)) if w.r_q else w.d_model * H * w.d_nope
+    proj = 2 * T * (w.d_model * (w.r_kv + w.d_rope) + q_proj + w.r_kv * H * (w.d_nope + w.d_v)
+                    + H * w.d_v * w.d_model)
     attn = w.batch * H * (w.seq * (w.seq + 1) / 2) * 2 * ((w.d_nope + w.d_rope) + w.d_v)
     return proj + attn, attn
 
@@ -408,6 +411,7 @@ def run_ours(args, rank, world, device):
         out["prefill"] = pre
     if args.small:
         out["small_lm_decode"] = run_small_decode(args, device)
+        out["small_lm_prefill"] = run_prefill(args, device, syn.WORKLOADS["small_lm_prefill"])
     if args.cca:
         out["cca_prefill"] = run_cca(args, device, "cca_prefill")
         out["ccgqa_prefill"] = run_cca(args, device, "ccgqa_prefill")
@@ -420,11 +424,16 @@ def run_ours(args, rank, world, device):
     return out
 
 
-def run_prefill(args, lay_device):
+def run_prefill(args, lay_device, w=None):
+    """One prefill layer step (projection with the cache append, causal
+    attention, output projection) of the DeepSeek-V2 prefill workload, or of
+    another prefill workload `w` (the small-model form: no decoupled RoPE
+    key, half-split RoPE on the decompressed query and keys)."""
     import torch
     import head_latent_attention_gb300 as mla
     hbm_peak, tf_peak, tf_sust, peak_src = peaks()
-    w = PREFILL if not args.prefill_batch else PREFILL.replace(batch=args.prefill_batch)
+    if w is None:
+        w = PREFILL if not args.prefill_batch else PREFILL.replace(batch=args.prefill_batch)
     B, S = w.batch, w.seq
     lay = build_layer(w, lay_device, B, S, B * S, S)
     xs, _ = syn.activations(w, B * S)
@@ -435,7 +444,7 @@ def run_prefill(args, lay_device):
 
     dt = torch.bfloat16
     qn = torch.empty(B * S, w.n_heads, w.d_nope, dtype=dt, device=lay_device)
-    qr = torch.empty(B * S, w.n_heads, w.d_rope, dtype=dt, device=lay_device)
+    qr = torch.empty(B * S, w.n_heads, w.d_rope, dtype=dt, device=lay_device) if w.d_rope else None
     o = torch.empty(B, S, w.n_heads, w.d_v, dtype=dt, device=lay_device)
     y = torch.empty(B * S, w.d_model, dtype=dt, device=lay_device)
 
@@ -450,8 +459,11 @@ def run_prefill(args, lay_device):
 
     # Like the decode step: one graph of the layer step without timing hooks
     # (the step's figure) and one with events around the attention kernel
-    # (its figure), replayed alternately.  The step moves several GB, far
-    # more than L2 holds, so no flush is needed between replays.
+    # (its figure), replayed alternately.  The DeepSeek-V2 step moves several
+    # GB, far more than L2 holds; a smaller workload's step fits in L2, so L2
+    # is flushed before each replay (outside the events).
+    footprint = B * S * (w.d_model * 4 + (w.r_kv + w.d_rope) * 2 + w.n_heads * (2 * w.d_nope + 2 * w.d_v)) * 2
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=lay_device) if footprint < (1 << 30) else None
     for _ in range(2):
         step()
     torch.cuda.synchronize()
@@ -472,9 +484,13 @@ def run_prefill(args, lay_device):
     ev = timing_events(K)
     step_ms, kern_ms = [], []
     for i in range(K):
+        if flush is not None:
+            flush.zero_()
         ev[i][0].record(stream)
         g.replay()
         ev[i][1].record(stream)
+        if flush is not None:
+            flush.zero_()
         g_k.replay()
         ke.synchronize()
         kern_ms.append(kb.elapsed_time(ke))
@@ -487,8 +503,9 @@ def run_prefill(args, lay_device):
     katt = attn / (kms * 1e-3) / 1e12
     del lay, g, g_k
     torch.cuda.empty_cache()
-    return {"workload": "dsv2_prefill", "batch": B, "seq": S, "steps": K,
+    return {"workload": w.name, "batch": B, "seq": S, "steps": K,
             "timing": "graph of the layer step; attention kernel events in a second graph of it",
+            "l2": "flushed before each replay" if flush is not None else "step traffic far above L2: no flush",
             "ms_per_step": round(ms, 4), "step_ms": spread(step_ms), "tflops": round(tf, 2), "unit": "TFLOP/s",
             "frac_of_bf16_peak": round(tf / tf_peak, 4), "flops_per_step": total,
             "roofline": {"bound": "tensor", "kernel": "causal flash attention",
