@@ -82,6 +82,15 @@ def test_work_accounting_matches_the_workload_figures():
     assert attn == 4 * 128 * (4096 * 4097 / 2) * 2 * (192 + 128)
     assert total - attn == 2 * 149_225_472 * T
     assert total == pytest.approx(7.64e12, rel=2e-3)
+    # Small-model prefill (B=8, S=1024, d_model 512, 8 heads of 64, r_kv 256,
+    # an uncompressed W_Q): the projections W_DKV, W_Q, W_UK, W_UV, W_O are
+    # 917,504 MACs = 1.835 MFLOP per token; the attention
+    # B * H * S(S+1)/2 * 2 * (64 + 64).
+    import mla_synth as syn
+    total, attn = bench.prefill_flops(syn.WORKLOADS["small_lm_prefill"])
+    assert attn == 8 * 8 * (1024 * 1025 / 2) * 2 * (64 + 64)
+    assert total - attn == 2 * 917_504 * 8 * 1024
+    assert total == pytest.approx(23.6e9, rel=3e-3)
     # Decode: 1152 cache bytes per cached token (512 latent + 64 rope, bf16).
     import numpy as np
     assert bench.decode_bytes(np.array([1, 2, 3])) == 6 * 1152
