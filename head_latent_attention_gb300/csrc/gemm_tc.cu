@@ -7,9 +7,11 @@
 //   warp 1      MMA issuer: tcgen05.mma M=128, N=BN, K=16 into one of two
 //               tensor-memory accumulators (so the epilogue of one tile
 //               overlaps the main loop of the next);
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator rows (one row per
-//               thread), RoPE on column pairs, bfloat16 conversion, and the
-//               store to the output or to the (sequence, position) cache row.
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator rows (one row per
+//               thread; the two warps of a lane quadrant take half of the
+//               tile's columns each), RoPE on column pairs, bfloat16
+//               conversion, and the store to the output or to the
+//               (sequence, position) cache row.
 // Every mbarrier wait is bounded: on timeout the CTA raises the status word's
 // timeout bit, stops issuing, drains its own copies and frees tensor memory.
 #include <cudaTypedefs.h>
@@ -24,7 +26,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;  // two per tensor-memory lane quadrant, each half of a tile's columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kGroupM = 16;  // raster: 16 M-tiles share each sweep over N (L2 reuse)
 
 struct TcGemmParams {
@@ -38,6 +41,7 @@ struct TcGemmParams {
     Epilogue epi[kMaxSeg];
     uint32_t *status;
     long long wait_cycles;     // give-up limit of the pipeline waits
+    int tma_store;             // epilogue writes through the output tensor maps (staged 32 x 64 chunks)
 };
 
 template <int BN>
@@ -46,7 +50,8 @@ struct Cfg {
     static constexpr int kABytes = kBM * kBK * 2;
     static constexpr int kBBytes = BN * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kSmem = kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int kEpiBytes = kEpiWarps * 4096;  // per epilogue warp: 32 rows x 64 columns, bf16/fp16
+    static constexpr int kSmem = kStages * kStageBytes + kEpiBytes + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr int kTmemCols = 2 * BN;
 };
 
@@ -77,37 +82,89 @@ __device__ __forceinline__ int segment_start(const TcGemmParams &p, int sg)
     return sg == 0 ? 0 : (sg == 1 ? p.seg_n0[1] : p.seg_n0[2]);
 }
 
-// Epilogue e applied to columns [n0, n0 + NC) of its segment.
+// RoPE of row m's columns [n0, n0 + NC) of its segment, in place (NC covers
+// whole half-split groups: the chunk starts on a group boundary).  False,
+// with the position flag raised, when the row's position is out of range.
+template <int NC>
+__device__ __forceinline__ bool apply_rope(const Epilogue &e, int m, int n0, float (&v)[64])
+{
+    if (e.rope_mode == kRopeNone) return true;
+    const int pos = e.rope_pos ? e.rope_pos[m] : m;
+    if (pos < 0 || pos >= e.max_seq) {
+        if (n0 == 0 && e.status) atomicOr(e.status, kStatusPos);
+        return false;
+    }
+    const int dim = e.rope_dim, half = dim / 2;
+    const float2 *tab = e.rope_table + (int64_t)pos * half;
+    if (e.rope_mode == kRopeInterleaved) {
+#pragma unroll
+        for (int i = 0; i < NC / 2; ++i) {
+            const float2 cs = tab[((n0 + 2 * i) % dim) >> 1];
+            const float x0 = v[2 * i], x1 = v[2 * i + 1];
+            v[2 * i] = x0 * cs.x - x1 * cs.y;
+            v[2 * i + 1] = x0 * cs.y + x1 * cs.x;
+        }
+    } else if (dim == 64) {
+        // Pairs (i, i + 32) of each 64-column group: compile-time indices
+        // keep v in registers.
+#pragma unroll
+        for (int g = 0; g < NC; g += 64)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float2 cs = tab[i];
+                const float x0 = v[g + i], x1 = v[g + i + 32];
+                v[g + i] = x0 * cs.x - x1 * cs.y;
+                v[g + i + 32] = x0 * cs.y + x1 * cs.x;
+            }
+    } else {
+        // Narrower groups: runtime indices, on a local copy.
+        float t[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) t[j] = v[j];
+        for (int g = 0; g < NC; g += dim)
+            for (int i = 0; i < half; ++i) {
+                const float2 cs = tab[i];
+                const float x0 = t[g + i], x1 = t[g + i + half];
+                t[g + i] = x0 * cs.x - x1 * cs.y;
+                t[g + i + half] = x0 * cs.y + x1 * cs.x;
+            }
+#pragma unroll
+        for (int j = 0; j < NC; ++j) v[j] = t[j];
+    }
+    return true;
+}
+
+// The 16-bit words of NC output values: fp16 operands of the prefill
+// attention saturate at 65504 and raise the range flag (rows of batch entry z
+// that no query sees excepted), the rest is bfloat16.
+template <int NC>
+__device__ __forceinline__ void pack_out(const Epilogue &e, int z, int m, const float (&v)[64], uint32_t (&w)[32])
+{
+    if (e.out_f16) {
+        bool over = false;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) over |= ptx::beyond_f16(v[i]);
+        if (over && e.range_start && m >= e.range_start[z] + e.range_len) over = false;
+        if (over && e.status) atomicOr(e.status, kStatusF16Range);
+#pragma unroll
+        for (int i = 0; i < NC / 2; ++i) w[i] = ptx::pack_f16_satfinite(v[2 * i], v[2 * i + 1]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < NC / 2; ++i) w[i] = ptx::pack_bf16(v[2 * i], v[2 * i + 1]);
+    }
+}
+
+// Epilogue e applied to columns [n0, n0 + NC) of its segment, stored by this
+// thread.  A row whose RoPE position is out of range is written as zeros
+// (or, for a cache row, not written).
 template <int NC>
 __device__ __forceinline__ void store_chunk_seg(const TcGemmParams &p, const Epilogue &e, int z, int m, int n0,
                                                 float (&v)[64])
 {
-    if (e.rope_mode != kRopeNone) {
-        const int pos = e.rope_pos ? e.rope_pos[m] : m;
-        if (pos < 0 || pos >= e.max_seq) {
-            if (n0 == 0 && e.status) atomicOr(e.status, kStatusPos);
-            return;
-        }
-        const int dim = e.rope_dim, half = dim / 2;
-        const float2 *tab = e.rope_table + (int64_t)pos * half;
-        if (e.rope_mode == kRopeInterleaved) {
+    if (!apply_rope<NC>(e, m, n0, v)) {
+        if (e.row_seq) return;
 #pragma unroll
-            for (int i = 0; i < NC / 2; ++i) {
-                const float2 cs = tab[((n0 + 2 * i) % dim) >> 1];
-                const float x0 = v[2 * i], x1 = v[2 * i + 1];
-                v[2 * i] = x0 * cs.x - x1 * cs.y;
-                v[2 * i + 1] = x0 * cs.y + x1 * cs.x;
-            }
-        } else {
-            // NC covers whole groups: the chunk starts on a group boundary.
-            for (int g = 0; g < NC; g += dim)
-                for (int i = 0; i < half; ++i) {
-                    const float2 cs = tab[i];
-                    const float x0 = v[g + i], x1 = v[g + i + half];
-                    v[g + i] = x0 * cs.x - x1 * cs.y;
-                    v[g + i + half] = x0 * cs.y + x1 * cs.x;
-                }
-        }
+        for (int i = 0; i < NC; ++i) v[i] = 0.f;
     }
     uint16_t *dst;
     if (e.row_seq) {
@@ -120,26 +177,25 @@ __device__ __forceinline__ void store_chunk_seg(const TcGemmParams &p, const Epi
     } else {
         dst = (uint16_t *)e.out + (int64_t)z * e.batch_stride + (int64_t)m * e.ldc + n0;
     }
-    if (e.out_f16) {
-        // fp16 operands of the prefill attention: values beyond fp16's range
-        // saturate at 65504 and raise the range flag.
-        bool over = false;
+    uint32_t w[32];
+    pack_out<NC>(e, z, m, v, w);
 #pragma unroll
-        for (int i = 0; i < NC; ++i) over |= ptx::beyond_f16(v[i]);
-        if (over && e.range_start && m >= e.range_start[z] + e.range_len) over = false;
-        if (over && e.status) atomicOr(e.status, kStatusF16Range);
+    for (int i = 0; i < NC / 2; i += 4)
+        *reinterpret_cast<uint4 *>(dst + 2 * i) = make_uint4(w[i], w[i + 1], w[i + 2], w[i + 3]);
+}
+
+// Row m's 64 output columns [n0, n0 + 64) of its segment as the 32 words of
+// a staged tensor store: zeros for rows past M (which the store clips) and
+// for rows whose RoPE position is out of range.
+__device__ __forceinline__ void stage_words_seg(const TcGemmParams &p, const Epilogue &e, int z, int m, int n0,
+                                                float (&v)[64], uint32_t (&w)[32])
+{
+    if (m >= p.M || !apply_rope<64>(e, m, n0, v)) {
 #pragma unroll
-        for (int i = 0; i < NC; i += 8)
-            *reinterpret_cast<uint4 *>(dst + i) =
-                make_uint4(ptx::pack_f16_satfinite(v[i], v[i + 1]), ptx::pack_f16_satfinite(v[i + 2], v[i + 3]),
-                           ptx::pack_f16_satfinite(v[i + 4], v[i + 5]), ptx::pack_f16_satfinite(v[i + 6], v[i + 7]));
-    } else {
-#pragma unroll
-        for (int i = 0; i < NC; i += 8)
-            *reinterpret_cast<uint4 *>(dst + i) =
-                make_uint4(ptx::pack_bf16(v[i], v[i + 1]), ptx::pack_bf16(v[i + 2], v[i + 3]),
-                           ptx::pack_bf16(v[i + 4], v[i + 5]), ptx::pack_bf16(v[i + 6], v[i + 7]));
+        for (int i = 0; i < 32; ++i) w[i] = 0u;
+        return;
     }
+    pack_out<64>(e, z, m, v, w);
 }
 
 // Epilogue of one accumulator row chunk of NC columns starting at output
@@ -167,7 +223,8 @@ template <int BN, bool kBMN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-                   TcGemmParams p)
+                   const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
+                   const __grid_constant__ CUtensorMap tmC2, TcGemmParams p)
 {
     using C = Cfg<BN>;
     constexpr int S = C::kStages;
@@ -175,7 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sA = smem;
     uint8_t *sB = smem + S * C::kABytes;
-    uint64_t *full = (uint64_t *)(sB + S * C::kBBytes);
+    uint8_t *sEpi = sB + S * C::kBBytes;  // epilogue staging, 4 KB per epilogue warp (1024-byte aligned)
+    uint64_t *full = (uint64_t *)(sEpi + C::kEpiBytes);
     uint64_t *empty = full + S;
     uint64_t *acc_full = empty + S;
     uint64_t *acc_empty = acc_full + 2;
@@ -191,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&acc_full[i], 1);
-            ptx::mbar_init(&acc_empty[i], 4);
+            ptx::mbar_init(&acc_empty[i], kEpiWarps);
         }
         ptx::mbar_init(mma_drain, 1);
         *abort_flag = 0;
@@ -344,6 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         ptx::pdl_wait();
         const int quad = warp % 4;  // tensor-memory lane quadrant this warp may access
+        // Warps w and w + 4 share a quadrant and split the tile's columns:
+        // half eh takes [eh BN / 2, (eh + 1) BN / 2) (RoPE in the half-split
+        // form needs whole 64-column groups: at BN = 64 half 0 takes them all).
+        const int eh = (warp - 2) / 4;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
@@ -362,9 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after();
             const int m = mt * kBM + quad * 32 + lane;
             const uint32_t tbase = tmem + acc * BN + ((uint32_t)(quad * 32) << 16);
+            const int c_lo = eh * (BN / 2), c_hi = c_lo + BN / 2;
             if (p.partial) {
                 // Split-K: raw fp32 partial sums; the reduce kernel applies the epilogue.
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = c_lo; c < c_hi; c += 32) {
                     uint32_t r0[32];
                     ptx::tmem_ld32(tbase + c, r0);
                     ptx::tmem_ld_wait();
@@ -378,8 +441,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             __uint_as_float(r0[i + 2]), __uint_as_float(r0[i + 3]));
                     }
                 }
+            } else if (p.tma_store) {
+                // Whole 64-column chunks: converted, staged in this warp's
+                // 32-row buffer in the 128-byte swizzle and written by one
+                // tensor store, which clips rows past M and columns past the
+                // segment.  At BN = 64 half 0 takes the tile.
+                const int s_lo = BN >= 128 ? c_lo : (eh == 0 ? 0 : BN), s_hi = BN >= 128 ? c_hi : BN;
+                uint8_t *buf = sEpi + (warp - 2) * 4096;
+                for (int c = s_lo; c < s_hi; c += 64) {
+                    uint32_t r0[32], r1[32];
+                    ptx::tmem_ld32(tbase + c, r0);
+                    ptx::tmem_ld32(tbase + c + 32, r1);
+                    ptx::tmem_ld_wait();
+                    float v[64];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) { v[i] = __uint_as_float(r0[i]); v[32 + i] = __uint_as_float(r1[i]); }
+                    const int ng = nt * BN + c;
+                    const int sgc = segment_of(p, ng);
+                    const int n0 = ng - segment_start(p, sgc);
+                    uint32_t w[32];
+                    if (sgc == 0) stage_words_seg(p, p.epi[0], z, m, n0, v, w);
+                    else if (sgc == 1) stage_words_seg(p, p.epi[1], z, m, n0, v, w);
+                    else stage_words_seg(p, p.epi[2], z, m, n0, v, w);
+                    // The previous store from this buffer has read it.
+                    if (lane == 0) ptx::bulk_wait_group_read0();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint4 *>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                            make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const CUtensorMap *tmC = sgc == 0 ? &tmC0 : (sgc == 1 ? &tmC1 : &tmC2);
+                        ptx::tma_store_3d(tmC, buf, n0, mt * kBM + quad * 32, z);
+                        ptx::bulk_commit_group();
+                    }
+                }
             } else if (half_rope) {
-                for (int c = 0; c < BN; c += 64) {
+                const int h_lo = BN >= 128 ? c_lo : (eh == 0 ? 0 : BN), h_hi = BN >= 128 ? c_hi : BN;
+                for (int c = h_lo; c < h_hi; c += 64) {
                     uint32_t r0[32], r1[32];
                     ptx::tmem_ld32(tbase + c, r0);
                     ptx::tmem_ld32(tbase + c + 32, r1);
@@ -390,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_chunk<64>(p, z, m, nt * BN + c, v);
                 }
             } else {
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = c_lo; c < c_hi; c += 32) {
                     uint32_t r0[32];
                     ptx::tmem_ld32(tbase + c, r0);
                     ptx::tmem_ld_wait();
@@ -406,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1;
         }
+        if (lane == 0) ptx::bulk_wait_group0();  // this warp's tensor stores are complete
         if (!ok) *abort_flag = 1;
     }
 
@@ -498,6 +600,26 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
                      box_cols * 2 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Output map of one segment for the staged tensor-store epilogue: 16-bit
+// elements, [batch][rows][cols] with the given row and batch strides
+// (elements), 64-column x 32-row boxes in the 128-byte swizzle.  The store
+// clips at every dimension's end, so a tile never writes into the next
+// batch entry's rows.
+static bool make_tmap_out(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
+                          int64_t batch_stride)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const int64_t bstride = batch > 1 ? batch_stride : rows * ld;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+    cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(bstride * 2)};
+    cuuint32_t box[3] = {64, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
 }
 
 // The column segments of a product (one, unless the call is grouped) and the
@@ -636,13 +758,25 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     for (int i = ns; i < kMaxSeg; ++i) p.epi[i] = sg[0].epi;
     p.status = sg[0].epi.status;
     p.wait_cycles = gemm_wait_cycles();
+    // Staged tensor stores for plain row-major outputs: not for split-K
+    // partials, nor for rows scattered to cache positions.
+    CUtensorMap tc[kMaxSeg];
+    bool tma = pl.splits == 1;
+    for (int i = 0; i < ns && tma; ++i) {
+        const Epilogue &e = sg[i].epi;
+        tma = !e.row_seq && (a.batch == 1 || (e.batch_stride * 2) % 16 == 0) &&
+              make_tmap_out(&tc[i], e.out, a.M, sg[i].N, e.ldc, a.batch, e.batch_stride);
+    }
+    p.tma_store = tma ? 1 : 0;
+    if (!tma) tc[0] = ta;  // unused placeholders
+    for (int i = tma ? ns : 1; i < kMaxSeg; ++i) tc[i] = tc[0];
     if (pl.splits > 1 && !a.split_ws) return cudaErrorInvalidValue;
     const int units = p.tiles_m * p.tiles_n * a.batch * p.splits;
     static std::atomic<int> smem_dev{-1};
     cudaError_t e = smem_limit_once(smem_dev, (const void *)gemm_tc_kernel<BN, kBMN>, C::kSmem);
     if (e != cudaSuccess) return e;
     e = launch_ex(gemm_tc_kernel<BN, kBMN>, dim3(std::min(units, num_sms)), dim3(kThreads), C::kSmem, s, 1, ta,
-                  tb[0], tb[1], tb[2], p);
+                  tb[0], tb[1], tb[2], tc[0], tc[1], tc[2], p);
     note_launch();
     if (e != cudaSuccess) return e;
     if (pl.splits > 1) {

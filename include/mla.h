@@ -176,8 +176,9 @@ size_t mla_workspace_size(const mla_handle *h, int batch, int max_len,
  *             [T, H, d_nope]; q_rope must be NULL
  *  MLRA:      cache.lat[seq, pos] = W_DKV x, q_nope = W_Q x; q_rope NULL
  * x [T, d_model]; seq_idx, pos: device int32 [T].  T == 0 is a no-op.
- * Tokens whose seq_idx or pos is out of range are skipped and flagged in the
- * workspace status word.  Workspace: the c_Q intermediate (DECOUPLED). */
+ * Tokens whose seq_idx or pos is out of range are skipped (no cache row is
+ * written; their query rows are zero) and flagged in the workspace status
+ * word.  Workspace: the c_Q intermediate (DECOUPLED). */
 mla_status mla_project_latent(mla_handle *h, const mla_weights *w, const void *x,
                               int64_t T, const int32_t *seq_idx, const int32_t *pos,
                               const mla_cache *cache, void *q_nope, void *q_rope,
