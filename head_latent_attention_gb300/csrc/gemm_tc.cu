@@ -96,7 +96,22 @@ __device__ __forceinline__ bool apply_rope(const Epilogue &e, int m, int n0, flo
     }
     const int dim = e.rope_dim, half = dim / 2;
     const float2 *tab = e.rope_table + (int64_t)pos * half;
-    if (e.rope_mode == kRopeInterleaved) {
+    if (e.rope_mode == kRopeInterleaved && dim == 64 && NC == 64 && n0 % 64 == 0) {
+        // One whole group: its 32 (cos, sin) pairs in 16 16-byte loads (a
+        // table row is 256 bytes, 16-byte aligned).
+        const float4 *tab4 = reinterpret_cast<const float4 *>(tab);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float4 cs = tab4[i];
+            float x0 = v[4 * i], x1 = v[4 * i + 1];
+            v[4 * i] = x0 * cs.x - x1 * cs.y;
+            v[4 * i + 1] = x0 * cs.y + x1 * cs.x;
+            x0 = v[4 * i + 2];
+            x1 = v[4 * i + 3];
+            v[4 * i + 2] = x0 * cs.z - x1 * cs.w;
+            v[4 * i + 3] = x0 * cs.w + x1 * cs.z;
+        }
+    } else if (e.rope_mode == kRopeInterleaved) {
 #pragma unroll
         for (int i = 0; i < NC / 2; ++i) {
             const float2 cs = tab[((n0 + 2 * i) % dim) >> 1];
