@@ -617,20 +617,19 @@ bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t rows, int64_t cols,
     return r == CUDA_SUCCESS;
 }
 
-// Output map of one segment for the staged tensor-store epilogue: 16-bit
-// elements, [batch][rows][cols] with the given row and batch strides
-// (elements), 64-column x 32-row boxes in the 128-byte swizzle.  The store
-// clips at every dimension's end, so a tile never writes into the next
-// batch entry's rows.
-static bool make_tmap_out(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
-                          int64_t batch_stride)
+// Map for tensor stores of 16-bit elements laid out [batch][rows][cols] with
+// the given row and batch strides (elements): 64-column x box_rows boxes in
+// the 128-byte swizzle.  The store clips at every dimension's end, so a tile
+// never writes past its own batch entry's rows.
+bool make_tmap_store16(CUtensorMap *m, void *ptr, int64_t rows, int64_t cols, int64_t ld, int64_t batch,
+                       int64_t batch_stride, int box_rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
     const int64_t bstride = batch > 1 ? batch_stride : rows * ld;
     cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
     cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), (cuuint64_t)(bstride * 2)};
-    cuuint32_t box[3] = {64, 32, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
@@ -780,7 +779,7 @@ static cudaError_t launch(const GemmArgs &a, const GemmPlan &pl, int num_sms, cu
     for (int i = 0; i < ns && tma; ++i) {
         const Epilogue &e = sg[i].epi;
         tma = !e.row_seq && (a.batch == 1 || (e.batch_stride * 2) % 16 == 0) &&
-              make_tmap_out(&tc[i], e.out, a.M, sg[i].N, e.ldc, a.batch, e.batch_stride);
+              make_tmap_store16(&tc[i], e.out, a.M, sg[i].N, e.ldc, a.batch, e.batch_stride, 32);
     }
     p.tma_store = tma ? 1 : 0;
     if (!tma) tc[0] = ta;  // unused placeholders
