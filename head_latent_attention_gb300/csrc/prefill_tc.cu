@@ -250,11 +250,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ptx::mbar_wait(&bar->q_full[q], 0, abort_flag)) ok = false;
             if (ok) {
                 // Values beyond fp16's range saturate and raise the range flag.
+                // The row's eight 16-byte chunks are visited in swizzled order
+                // (chunk j sits at position j ^ (r % 8)): each is converted in
+                // place, and a warp's 32 rows then spread over all banks
+                // instead of all hitting the same four.
                 bool over = false;
                 for (int a = 0; a < NQ; ++a) {
                     uint4 *row = reinterpret_cast<uint4 *>(sQ + a * kQ * 128 + r * 128);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = jj ^ (r & 7);
                         uint4 w = row[j];
                         w.x = ptx::bf16x2_to_f16x2(w.x, over);
                         w.y = ptx::bf16x2_to_f16x2(w.y, over);
