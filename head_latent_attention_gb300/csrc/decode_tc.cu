@@ -70,6 +70,15 @@ constexpr int kXRowBytes = kBKV * 2;
 constexpr int kXWarpBytes = 32 * kXRowBytes;
 constexpr int kXBytes = kH * kXRowBytes;
 constexpr uint32_t kXTx = kXBytes;                    // one exchange = one bulk copy of a whole buffer
+// Position of 16-byte chunk c within row `lane` of an exchange block.  Rows
+// are 96 bytes (six chunks) apart, so eight consecutive rows would cover only
+// four of the eight 16-byte bank groups; rotating the chunks of rows with
+// lane % 8 >= 4 by one spreads every eight lanes over all eight.
+__device__ __forceinline__ int xpos(int c, int lane)
+{
+    const int p = c + ((lane >> 2) & 1);
+    return p >= kBKV / 8 ? p - kBKV / 8 : p;
+}
 constexpr int kOffX = kStages * kStageBytes;
 // P (bf16, 128 heads x 48 keys) as the A operand of P.V: K-major without
 // swizzle, 8-row x 16-byte core matrices, the six core matrices of an 8-row
@@ -580,7 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < kBKV / 8; ++c)
-                *reinterpret_cast<uint4 *>(my_stage + 4 * c) =
+                *reinterpret_cast<uint4 *>(my_stage + 4 * xpos(c, lane)) =
                     make_uint4(own_next[4 * c], own_next[4 * c + 1], own_next[4 * c + 2], own_next[4 * c + 3]);
             ptx::fence_proxy_async_smem();
             __syncwarp();
@@ -621,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         reinterpret_cast<const uint32_t *>(smem + kOffX + grp * kXBytes + xblk + lane * kXRowBytes);
 #pragma unroll
                     for (int c = 0; c < kBKV / 8; ++c) {
-                        const uint4 v = *reinterpret_cast<const uint4 *>(xr + 4 * c);
+                        const uint4 v = *reinterpret_cast<const uint4 *>(xr + 4 * xpos(c, lane));
                         const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
