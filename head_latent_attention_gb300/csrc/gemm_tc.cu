@@ -68,9 +68,6 @@ __device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int
     nt = r / gm;
 }
 
-// Epilogue of one accumulator row chunk of NC columns (8, 32 or 64; RoPE in
-// the half-split form needs whole 64-column groups) starting at output
-// column n0 of row m of batch entry z.
 // Segment of output column n (constant indices only: a dynamically indexed
 // kernel parameter would be copied to local memory).
 __device__ __forceinline__ int segment_of(const TcGemmParams &p, int n)
