@@ -841,6 +841,13 @@ __device__ __forceinline__ int last_range_at_or_before(const int *range_start, i
     return lo;
 }
 
+// Batches and range counts up to these sizes keep their prefix sums and
+// range starts in shared memory for the binary searches below (each probe
+// of a global copy would be a dependent L2 round trip; the scheduler sits
+// between the query projection and the attention).
+constexpr int kSchedSmemSeqs = 8192;
+constexpr int kSchedSmemRanges = 1024;
+
 __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *seq_lens, int B, int max_seq, int n,
                                                                int seg_cost, DecodeSched sc, uint32_t *status)
 {
@@ -850,10 +857,17 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
     // its own wait.
     ptx::pdl_trigger();
     ptx::pdl_wait();
-    int *prefix = sc.prefix;
+    __shared__ int s_prefix[kSchedSmemSeqs + 1];
+    __shared__ int s_range[kSchedSmemRanges + 1];
     __shared__ int warp_sums[32];
     __shared__ int carry;
-    if (threadIdx.x == 0) { carry = 0; prefix[0] = 0; }
+    const bool prefix_smem = B <= kSchedSmemSeqs, range_smem = n <= kSchedSmemRanges;
+    int *prefix = sc.prefix;
+    if (threadIdx.x == 0) {
+        carry = 0;
+        prefix[0] = 0;
+        s_prefix[0] = 0;
+    }
     __syncthreads();
     for (int base = 0; base < B; base += 1024) {
         const int i = base + threadIdx.x;
@@ -882,12 +896,18 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
         }
         __syncthreads();
         const int incl = v + ((threadIdx.x >> 5) ? warp_sums[(threadIdx.x >> 5) - 1] : 0) + carry;
-        if (i < B) prefix[i + 1] = incl;
+        if (i < B) {
+            prefix[i + 1] = incl;
+            if (prefix_smem) s_prefix[i + 1] = incl;
+        }
         __syncthreads();
         if (threadIdx.x == 1023) carry = incl;
         __syncthreads();
     }
-    const int total = prefix[B];
+    // (A thread's global writes are visible to the block after the barrier
+    // above when the sums do not fit in shared memory.)
+    const int *pf = prefix_smem ? s_prefix : prefix;
+    const int total = pf[B];
     const int chunk = max(128, (total + n - 1) / n);
     if (threadIdx.x == 0) *sc.chunk = chunk;
     // Range starts.  With a segment cost, cost position x of the sequence
@@ -905,34 +925,36 @@ __global__ void __launch_bounds__(1024) decode_schedule_kernel(const int32_t *se
             int lo = 0, hi = B;  // last b with C(b) <= x
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
-                if ((long long)prefix[mid] + (long long)mid * seg_cost <= x) lo = mid;
+                if ((long long)pf[mid] + (long long)mid * seg_cost <= x) lo = mid;
                 else hi = mid - 1;
             }
             if (lo >= B) {
                 st = total;
             } else {
-                const long long off = x - ((long long)prefix[lo] + (long long)lo * seg_cost) - seg_cost;
-                const int len = prefix[lo + 1] - prefix[lo];
-                st = prefix[lo] + (int)min((long long)len, max(0ll, off));
+                const long long off = x - ((long long)pf[lo] + (long long)lo * seg_cost) - seg_cost;
+                const int len = pf[lo + 1] - pf[lo];
+                st = pf[lo] + (int)min((long long)len, max(0ll, off));
             }
         }
         sc.range_start[c] = st;
+        if (range_smem) s_range[c] = st;
     }
     __syncthreads();
+    const int *rs = range_smem ? s_range : sc.range_start;
     for (int c = threadIdx.x; c < n; c += blockDim.x) {
-        const int st = sc.range_start[c], en = sc.range_start[c + 1];
+        const int st = rs[c], en = rs[c + 1];
         int lo = 0, hi = B;  // first b with prefix[b + 1] > st
         while (lo < hi) {
             const int mid = (lo + hi) >> 1;
-            if (prefix[mid + 1] > st) hi = mid;
+            if (pf[mid + 1] > st) hi = mid;
             else lo = mid + 1;
         }
         sc.range_b0[c] = st < en ? lo : B;
     }
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
-        const int lo = prefix[b], hi = prefix[b + 1];
-        sc.seq_fc[b] = hi > lo ? last_range_at_or_before(sc.range_start, n, lo) : -1;
-        sc.seq_lc[b] = hi > lo ? last_range_at_or_before(sc.range_start, n, hi - 1) : -1;
+        const int lo = pf[b], hi = pf[b + 1];
+        sc.seq_fc[b] = hi > lo ? last_range_at_or_before(rs, n, lo) : -1;
+        sc.seq_lc[b] = hi > lo ? last_range_at_or_before(rs, n, hi - 1) : -1;
     }
 }
 
