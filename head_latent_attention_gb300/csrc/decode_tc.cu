@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // and warps 6..9 the odd ones, each thread the whole row of its tile,
         // so two tiles are in flight.  The running reference max passes
         // from one group to the other tile by tile through shared memory,
-        // ordered by a producer/consumer named barrier per lane quarter.
+        // ordered by a producer/consumer mbarrier per lane quarter.
         const int quad = warp % 4, grp = (warp - 2) / 4;
         const int h = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -509,8 +509,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // This CTA's 288 query columns of row h into tensor memory (lanes =
         // heads, bf16 pairs per 32-bit column, lower column in the low half,
         // which is how consecutive bf16 values sit in memory), written by the
-        // group that sends the segment's first tile.
-        auto load_q = [&](int b, int nseg) -> bool {
+        // group that sends the segment's first tile (part 0).  The first
+        // segment's query is split between the groups, both idle at the
+        // start: group 0 writes latent columns [0, 128) and the rope columns
+        // (part 1), group 1 latent columns [128, 256) (part 2); they meet at a
+        // named barrier before group 0 arrives on q_full for both.
+        auto load_q = [&](int b, int nseg, int part) -> bool {
             if (nseg > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait(&bar->q_empty, (nseg - 1) & 1, abort_flag)))
                 return false;
             ptx::tc_fence_after();
@@ -534,17 +538,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ptx::tmem_st32(tmem + lane_off + kQCol + c * 32, w);
             };
+            if (part != 2) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) vr[i] = row_ok ? rs[i] : make_uint4(0, 0, 0, 0);
-            fetch(va, 0);
-            fetch(vb, 1);
-            put(va, 0);
-            fetch(va, 2);
-            put(vb, 1);
-            fetch(vb, 3);
-            put(va, 2);
-            put(vb, 3);
-            {
+                for (int i = 0; i < 4; ++i) vr[i] = row_ok ? rs[i] : make_uint4(0, 0, 0, 0);
+            }
+            if (part == 0) {
+                fetch(va, 0);
+                fetch(vb, 1);
+                put(va, 0);
+                fetch(va, 2);
+                put(vb, 1);
+                fetch(vb, 3);
+                put(va, 2);
+                put(vb, 3);
+            } else {
+                const int c0 = part == 1 ? 0 : 2;
+                fetch(va, c0);
+                fetch(vb, c0 + 1);
+                put(va, c0);
+                put(vb, c0 + 1);
+            }
+            if (part != 2) {
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -554,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(&bar->q_full);
+            if (part != 0) asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory");
+            if (part != 2) ptx::mbar_arrive(&bar->q_full);
             return true;
         };
         // Row h of the partial scores of this group's tiles, scaled to log2
@@ -598,9 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         TileCursor nx;  // the next tile of this group to send (sends run two tiles ahead)
         nx.init(win, p.sc.prefix, p.B);
+        // Both groups take this branch or neither (the range is the CTA's),
+        // and nothing in it can fail before the named barrier.
+        if (nx.valid) load_q(nx.b, 0, grp + 1);
         if (grp == 1 && nx.valid) nx.step();
         if (ok && nx.valid) {
-            if ((nx.t == 0 && !load_q(nx.b, nx.nseg)) || !send(nx.g)) fail();
+            if ((nx.t == 0 && nx.nseg > 0 && !load_q(nx.b, nx.nseg, 0)) || !send(nx.g)) fail();
 #pragma unroll
             for (int j = 0; j < kBKV / 2; ++j) own[j] = own_next[j];
             nx.step();
@@ -672,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 //    (P.V(g) cannot finish before P(g) exists).
                 if (g >= 2 && !ptx::mbar_wait(&bar->pv_done[grp], ((g >> 1) - 1) & 1, abort_flag)) { fail(); break; }
                 if (nx.valid) {
-                    if (nx.t == 0 && !load_q(nx.b, nx.nseg)) { fail(); break; }
+                    if (nx.t == 0 && !load_q(nx.b, nx.nseg, 0)) { fail(); break; }
                     if (!send(nx.g)) { fail(); break; }
                     nx.step();
                     if (nx.valid) nx.step();
