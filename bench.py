@@ -42,7 +42,7 @@ NOMINAL_HBM_GBS = 7900.0  # the HBM3e bandwidth NVIDIA quotes for GB300 (context
 # from an ncu capture of the current kernel (dram__bytes_read.sum +
 # dram__bytes_write.sum); None whenever the kernel changes until it is
 # captured again.
-DECODE_TRAFFIC_BYTES = 217250304  # 213,544,704 read + 3,705,600 written
+DECODE_TRAFFIC_BYTES = 217263616  # 213,548,288 read + 3,715,328 written
 
 
 def max_over_ranks(vals, world: int, device):
